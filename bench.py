@@ -1,0 +1,418 @@
+"""Benchmark of the KDA forward pass on GB300.
+
+One step = one kda_fwd call over the fixed-length prefill workload
+B=1, T=8192, H=96, K=V=128 (bf16 q/k/v/g/beta/out, bf16 initial state, fp32
+final state; seeded synthetic inputs shaped like the FlashKDA H20 benchmark
+on the pages).  Inputs are resident in HBM before the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun, one rank per GPU) every
+rank runs its own replica of the workload (weak scaling: the (sequence, head)
+recurrences are independent, so there is no collective on the data path);
+time is the max over ranks.  ``--impl reference`` times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "prefill_t8192_h96"
+METRIC = "KDA fwd tokens/s at T=8192 H=96 D=128 bf16; % of tensor/HBM roofline"
+K = V = 128
+C = 16
+# Algorithmic work of the chunked method per (token, head):
+#   flops: 6KV (state reads S^T q, S^T k-side w, state update) + 2C(3K + 2V)
+#          (A_kk, A_qk, w; u and A_qk U)  = 118,784
+#   bytes: q, k, g, v (2 B x 128 each), beta (2 B), out (2 B x 128) = 1,282
+# plus, per (sequence, head), the initial state read and the final state write.
+FLOP_PER_TH = 6 * K * V + 2 * C * (3 * K + 2 * V)
+BYTES_PER_TH = 4 * 2 * 128 + 2 + 2 * 128
+# Per-kernel algorithmic work (the split of the figures above between kernels):
+#   intra_kernel: reads q, k, v, g, beta; A_kk, A_qk, w, u contractions
+#   state_kernel: writes out and the states; S^T q, U, state update, A_qk U
+KERNEL_FLOP_PER_TH = {"intra_kernel": 2 * C * (3 * K + V), "state_kernel": 6 * K * V + 2 * C * V}
+KERNEL_BYTES_PER_TH = {"intra_kernel": 4 * 2 * 128 + 2, "state_kernel": 2 * 128}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "of measured"
+    return 6800.0, 1900.0, "of fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for ln in open(self.path):
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else 0.0,
+                             "hw": parts[5], "hwt": parts[6], "swt": parts[7], "pcap": parts[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        mx = max(r["max"] for r in rows)
+        loaded = [r for r in rows if r["power"] > 0.2 * max(x["power"] for x in rows)] or rows
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                          ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+            if any(r[key].lower() == "active" for r in loaded):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl != "reference" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg, device=None):
+    if pg is not None:
+        if device is not None:
+            pg.barrier(device_ids=[device.index])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, x: float, device=None) -> float:
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device if device is not None else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def source_digest(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "gated_delta_rule_39_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the kernel's
+    source has not changed since the capture; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    if rec.get("source_digest") != source_digest(*rec.get("sources", [])):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+def run_cuda(args, world, rank, local, pg):
+    import numpy as np
+    import torch
+
+    import synth
+    import gated_delta_rule_39_gb300 as kda
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    kda.load_library()
+    d = synth.make_workload(WORKLOAD, seed=rank)
+    B, T, H, _ = d["q"].shape
+    N = d["N"]
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+    x = {n: bf16(d[n]) for n in ("q", "k", "v", "g", "beta")}
+    A_log = torch.from_numpy(d["A_log"]).to(device)
+    dt_bias = torch.from_numpy(d["dt_bias"]).to(device)
+    s0 = bf16(d["initial_state"])
+    out = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=device)
+    s1 = torch.empty((N, H, K, V), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        kda.kda_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], d["scale"], out, A_log, dt_bias,
+                    d["lower_bound"], initial_state=s0, final_state=s1, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    err = kda.kda_fwd_get_error(stream)
+    if err != 0:
+        raise RuntimeError(f"device error after warm-up: {kda.kda_status_string(err)}")
+
+    # ---- timed region: K steps, launch timing on the launch stream -------------
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.__enter__()
+    kda.kda_profile_enable(True)
+    barrier(pg, device)
+    torch.cuda.synchronize(device)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(pg, device)
+    elapsed_ms = ev0.elapsed_time(ev1)
+    prof = kda.kda_profile_read()
+    kda.kda_profile_enable(False)
+    if sampler:
+        sampler.__exit__(None, None, None)
+    elapsed_ms = max_over_ranks(pg, elapsed_ms, device)
+
+    tokens_per_step = B * T
+    value = world * tokens_per_step * args.steps / (elapsed_ms / 1e3)
+    ms_per_step = elapsed_ms / args.steps
+    launches = sum(n for _, n in prof.values())
+
+    # ---- roofline of the dominant kernel and of the whole call --------------------
+    hbm, tflops, src = peaks()
+    th = B * T * H
+    dom = max(prof, key=lambda n: prof[n][0])
+    dom_ms = prof[dom][0] / max(1, prof[dom][1])
+    dom_flop = KERNEL_FLOP_PER_TH.get(dom, 0) * th
+    dom_bytes = KERNEL_BYTES_PER_TH.get(dom, 0) * th
+    if dom == "state_kernel":
+        dom_bytes += N * H * K * V * (2 + 4)   # bf16 initial state read, fp32 final write
+    t_hbm = dom_bytes / (hbm * 1e9)
+    t_tc = dom_flop / (tflops * 1e12)
+    if t_tc >= t_hbm:
+        roof = {"bound": "tensor", "achieved": dom_flop / (dom_ms * 1e-3) / 1e12, "peak": tflops,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": dom_bytes / (dom_ms * 1e-3) / 1e9, "peak": hbm,
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = dom
+    roof["kernel_ms"] = dom_ms
+    roof["traffic"] = ncu_traffic(dom)
+    roof["peak_source"] = src
+    path_bytes = BYTES_PER_TH * th + N * H * K * V * (2 + 4)
+    path_flop = FLOP_PER_TH * th
+    t_roof = max(path_bytes / (hbm * 1e9), path_flop / (tflops * 1e12))
+    path_roof = {"bound": "hbm" if path_bytes / (hbm * 1e9) >= path_flop / (tflops * 1e12)
+                 else "tensor",
+                 "roofline_ms": t_roof * 1e3, "measured_ms": ms_per_step,
+                 "frac": t_roof * 1e3 / ms_per_step, "bytes": path_bytes, "flop": path_flop,
+                 "peak_source": src}
+
+    # ---- end-to-end through the host-buffer entry point ---------------------------
+    e2e = None
+    if not args.no_e2e:
+        hx = {n: torch.from_numpy(np.ascontiguousarray(d[n]).view(np.int16)).view(torch.bfloat16)
+              .pin_memory() for n in ("q", "k", "v", "g", "beta", "initial_state")}
+        hA = torch.from_numpy(d["A_log"]).pin_memory()
+        hdt = torch.from_numpy(d["dt_bias"]).pin_memory()
+        hout = torch.empty((B, T, H, V), dtype=torch.bfloat16).pin_memory()
+        hs1 = torch.empty((N, H, K, V), dtype=torch.float32).pin_memory()
+
+        def host_step():
+            kda.kda_fwd_host(hx["q"], hx["k"], hx["v"], hx["g"], hx["beta"], d["scale"], hout,
+                             hA, hdt, d["lower_bound"], initial_state=hx["initial_state"],
+                             final_state=hs1, stream=stream, device=device)
+
+        host_step()
+        e2e_steps = max(1, min(args.steps, 5))
+        barrier(pg, device)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            host_step()
+        t1 = time.perf_counter()
+        e2e_s = max_over_ranks(pg, t1 - t0, device)
+        h2d = sum(t.numel() * t.element_size() for t in hx.values()) + hA.numel() * 4 + hdt.numel() * 4
+        d2h = hout.numel() * 2 + hs1.numel() * 4
+        e2e = {"value": world * tokens_per_step * e2e_steps / e2e_s, "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "entry_point": "kda_fwd_host"}
+
+    # ---- CPU oracle on a bounded sample (rank 0, N = 1 only) -----------------------
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(d, target_s=args.cpu_seconds)
+
+    clocks = sampler.summary() if sampler else None
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "compute": "f16 and tf32 tensor-core MMA, f32 accumulate",
+                "data": "synthetic (seeded; shapes of the pages' T=8192 H=96 D=128 benchmark)",
+                "config": {"workload": WORKLOAD, "B": B, "T": T, "H": H, "K": K, "V": V,
+                           "initial_state": "bf16", "final_state": "f32",
+                           "l2": "inputs larger than L2 (1.02 GB read+written per step vs "
+                                 "126 MB L2); no flush",
+                           "parallelism": f"replicas x{world}"},
+                "roofline": roof, "path_roofline": path_roof, "cpu_baseline": cpu,
+                "e2e": e2e, "gpu_launches": launches,
+                "kernel_ms": {n: (ms / max(1, c)) for n, (ms, c) in prof.items() if c},
+                "clocks": clocks}
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(d, target_s: float = 12.0):
+    """Time the fp64 oracle on a subset of heads (full T) of the same inputs."""
+    import oracle
+    H = d["q"].shape[2]
+    T = d["q"].shape[1]
+    threads = oracle.default_threads()
+    # the oracle works on float64 copies; convert once outside the timing
+    conv = {n: oracle.bf16_bits_to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")}
+    s0 = oracle.bf16_bits_to_f64(d["initial_state"]) if d.get("initial_state") is not None else None
+
+    def run(heads):
+        t0 = time.perf_counter()
+        oracle.kda_fwd(conv["q"], conv["k"], conv["v"], conv["g"], conv["beta"], d["scale"],
+                       d["A_log"], d["dt_bias"], d["lower_bound"], initial_state=s0,
+                       heads=heads, n_threads=threads)
+        return time.perf_counter() - t0
+
+    probe = min(H, threads)
+    t_probe = run(list(range(probe)))
+    n_heads = int(min(H, max(probe, round(probe * target_s / max(t_probe, 1e-3)))))
+    if n_heads > probe:
+        t = run(list(range(n_heads)))
+    else:
+        n_heads, t = probe, t_probe
+    tokens_equiv = T * n_heads / H
+    return {"value": tokens_equiv / t, "unit": "tokens/s", "cores": min(threads, n_heads),
+            "kind": "oracle",
+            "sample": f"{n_heads} of {H} heads x {T} tokens of {WORKLOAD}; tokens/s counts "
+                      f"a token as all {H} heads ({t:.1f} s)"}
+
+
+def run_reference(args, world, rank, local, pg):
+    """The base contract's reference arm: here the fp64 CPU oracle, on rank 0."""
+    if rank != 0:
+        return
+    import synth
+    import oracle
+    d = synth.make_workload(WORKLOAD, seed=0)
+    H = d["q"].shape[2]
+    T = d["q"].shape[1]
+    threads = oracle.default_threads()
+    conv = {n: oracle.bf16_bits_to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")}
+    s0 = oracle.bf16_bits_to_f64(d["initial_state"])
+    heads_per_step = min(H, threads)
+
+    def step():
+        oracle.kda_fwd(conv["q"], conv["k"], conv["v"], conv["g"], conv["beta"], d["scale"],
+                       d["A_log"], d["dt_bias"], d["lower_bound"], initial_state=s0,
+                       heads=list(range(heads_per_step)), n_threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    t = time.perf_counter() - t0
+    value = T * heads_per_step / H * args.steps / t
+    sample = (f"{heads_per_step} of {H} heads x {T} tokens of {WORKLOAD} per step; tokens/s "
+              f"counts a token as all {H} heads")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": 1, "T": T, "H": H, "K": K, "V": V},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "cuda":
+        print("note: warm-up raised to 3 steps", file=sys.stderr)
+        args.warmup = 3
+    world, rank, local, pg = dist_setup(args)
+    if args.gpus != world and world > 1:
+        print(f"note: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank, local, pg)
+        else:
+            run_cuda(args, world, rank, local, pg)
+    finally:
+        if pg is not None:
+            pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

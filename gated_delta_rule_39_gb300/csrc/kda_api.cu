@@ -1,0 +1,423 @@
+// Host side of the C ABI declared in include/kda.h: argument validation,
+// stream-ordered scratch memory, kernel launches, error word, launch timing.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+// Device-side error word (one per device: every device that loads the module
+// holds its own instance).  Kernels receive its address.
+__device__ int g_error_word;
+
+constexpr int kMaxDevices = 64;
+constexpr float kLowerBoundMin = -5.5f;  // 16 * 5.5 / ln 2 = 127 bits of decay per chunk
+
+struct DeviceInfo {
+    bool ready = false;
+    bool arch_ok = false;
+    int* err = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_setup(int* dev_out, int** err_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        d.arch_ok = (major == 10 && minor == 3);
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return KDA_ERR_CUDA;
+        d.err = static_cast<int*>(p);
+        // keep freed scratch in the device's default pool instead of returning
+        // it to the driver at every synchronisation
+        cudaMemPool_t pool;
+        if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+            uint64_t thr = UINT64_MAX;
+            cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+        }
+        d.ready = true;
+    }
+    *dev_out = dev;
+    *err_out = d.err;
+    return d.arch_ok ? KDA_OK : KDA_ERR_ARCH;
+}
+
+// ---- launch timing ------------------------------------------------------------
+struct TimingRecord {
+    int kernel;
+    cudaEvent_t start, stop;
+};
+struct Profiler {
+    std::mutex mu;
+    bool on = false;
+    std::vector<TimingRecord> pending;
+    std::vector<cudaEvent_t> free_events;
+    double total_ms[KDA_NUM_KERNELS] = {};
+    long long launches[KDA_NUM_KERNELS] = {};
+} g_prof;
+
+cudaEvent_t prof_event() {
+    if (!g_prof.free_events.empty()) {
+        cudaEvent_t e = g_prof.free_events.back();
+        g_prof.free_events.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+template <class F>
+cudaError_t timed_launch(int kernel, cudaStream_t s, F&& launch) {
+    bool on;
+    {
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        on = g_prof.on;
+    }
+    if (!on) return launch();
+    cudaEvent_t a, b;
+    {
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        a = prof_event();
+        b = prof_event();
+    }
+    cudaEventRecord(a, s);
+    cudaError_t e = launch();
+    cudaEventRecord(b, s);
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    g_prof.pending.push_back({kernel, a, b});
+    return e;
+}
+
+// ---- sizes ------------------------------------------------------------------
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+    int chunk_bound = 0;
+    int chunks_per_seq = 0;
+    size_t off_map = 0, off_qg = 0, off_kd = 0, off_w = 0, off_u = 0, off_aqk = 0, off_gc = 0;
+    size_t bytes = 0;
+};
+
+Layout plan(int B, int T, int H, int N, bool varlen) {
+    Layout L;
+    if (varlen) {
+        L.chunk_bound = T / kChunk + N + 1;
+    } else {
+        L.chunks_per_seq = (T + kChunk - 1) / kChunk;
+        L.chunk_bound = B * L.chunks_per_seq;
+    }
+    const size_t jh = (size_t)L.chunk_bound * H;
+    size_t off = 0;
+    L.off_map = off;
+    if (varlen) off += align_up(sizeof(int) * ((size_t)N + 1 + L.chunk_bound + N + 1));
+    L.off_qg = off;  off += align_up(jh * kChunk * kDim * sizeof(__half));
+    L.off_kd = off;  off += align_up(jh * kChunk * kDim * sizeof(__half));
+    L.off_w = off;   off += align_up(jh * kChunk * kDim * sizeof(__half));
+    L.off_u = off;   off += align_up(jh * kChunk * kDim * sizeof(__half));
+    L.off_aqk = off; off += align_up(jh * kChunk * kChunk * sizeof(__half));
+    L.off_gc = off;  off += align_up(jh * kDim * sizeof(float));
+    L.bytes = (jh == 0 && !varlen) ? 0 : off;
+    return L;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// Host-side checks shared by kda_fwd and kda_fwd_host; no CUDA call.
+int validate(const void* q, const void* k, const void* v, const void* g, const void* beta,
+             float scale, const void* out, const float* A_log, const float* dt_bias,
+             float lower_bound, const void* s0, int s0_dtype, const void* s1, int s1_dtype,
+             const int32_t* cu, int num_seqs, int B, int T, int H, int K, int V, bool check_align) {
+    if (K != kDim || V != kDim) return KDA_ERR_UNSUPPORTED_DIM;
+    if (B < 1 || T < 0 || H < 1) return KDA_ERR_SHAPE;
+    if (cu) {
+        if (B != 1 || num_seqs < 1) return KDA_ERR_SHAPE;
+    }
+    const long long tok = (long long)B * T;
+    if (tok * H * kDim >= (1LL << 31)) return KDA_ERR_SHAPE;
+    if (cu && (long long)num_seqs * H * kDim * kDim >= (1LL << 40)) return KDA_ERR_SHAPE;
+    if (tok > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL;
+    if (!A_log || !dt_bias) return KDA_ERR_NULL;
+    if (s0 && s0_dtype != KDA_BF16 && s0_dtype != KDA_F32) return KDA_ERR_DTYPE;
+    if (s1 && s1_dtype != KDA_BF16 && s1_dtype != KDA_F32) return KDA_ERR_DTYPE;
+    if (!std::isfinite(scale)) return KDA_ERR_ARG;
+    if (!(lower_bound >= kLowerBoundMin && lower_bound <= 0.0f)) return KDA_ERR_ARG;
+    if (check_align) {
+        for (const void* p : {q, k, v, g, static_cast<const void*>(out)})
+            if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return KDA_ERR_ALIGN;
+    }
+    const size_t n_qk = (size_t)tok * H * kDim * 2, n_b = (size_t)tok * H * 2;
+    for (const void* p : {q, k, v, g})
+        if (overlaps(out, n_qk, p, n_qk)) return KDA_ERR_ALIAS;
+    if (overlaps(out, n_qk, beta, n_b)) return KDA_ERR_ALIAS;
+    const int N = cu ? num_seqs : B;
+    const size_t ns = (size_t)N * H * kDim * kDim;
+    if (s0 && s1) {
+        const size_t b0 = ns * (s0_dtype == KDA_F32 ? 4 : 2), b1 = ns * (s1_dtype == KDA_F32 ? 4 : 2);
+        if (overlaps(s0, b0, s1, b1) && (s0 != s1 || s0_dtype != s1_dtype)) return KDA_ERR_ALIAS;
+    }
+    if (s1 && overlaps(out, n_qk, s1, ns * (s1_dtype == KDA_F32 ? 4 : 2))) return KDA_ERR_ALIAS;
+    return KDA_OK;
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+const char* kda_status_string(int status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_NULL: return "KDA_ERR_NULL: a required pointer is NULL";
+        case KDA_ERR_SHAPE: return "KDA_ERR_SHAPE: inconsistent or out-of-range sizes";
+        case KDA_ERR_UNSUPPORTED_DIM: return "KDA_ERR_UNSUPPORTED_DIM: only K = V = 128";
+        case KDA_ERR_ALIGN: return "KDA_ERR_ALIGN: q, k, v, g and out must be 16-byte aligned";
+        case KDA_ERR_DTYPE: return "KDA_ERR_DTYPE: state dtype must be KDA_BF16 or KDA_F32";
+        case KDA_ERR_LAUNCH: return "KDA_ERR_LAUNCH: kernel launch failed";
+        case KDA_ERR_DEVICE_TIMEOUT: return "KDA_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
+        case KDA_ERR_BAD_SEQLENS: return "KDA_ERR_BAD_SEQLENS: cu_seqlens must rise from 0 to T";
+        case KDA_ERR_ARCH: return "KDA_ERR_ARCH: needs a compute capability 10.3 (sm_103) GPU";
+        case KDA_ERR_ALLOC: return "KDA_ERR_ALLOC: scratch allocation failed";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
+        case KDA_ERR_ARG: return "KDA_ERR_ARG: scale must be finite, lower_bound in [-5.5, 0]";
+        case KDA_ERR_ALIAS: return "KDA_ERR_ALIAS: out overlaps an input or states alias unsafely";
+        default: return "unknown kda_status";
+    }
+}
+
+size_t kda_fwd_workspace_bytes(int B, int T, int H, int num_seqs, int varlen) {
+    if (B < 1 || T < 0 || H < 1) return 0;
+    const int N = varlen ? num_seqs : B;
+    return plan(B, T, H, N, varlen != 0).bytes;
+}
+
+int kda_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+            float scale, void* out, const float* A_log, const float* dt_bias, float lower_bound,
+            const void* initial_state, int initial_state_dtype, void* final_state,
+            int final_state_dtype, const int32_t* cu_seqlens, int num_seqs, int B, int T, int H,
+            int K, int V, void* stream) {
+    int rc = validate(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
+                      initial_state_dtype, final_state, final_state_dtype, cu_seqlens, num_seqs,
+                      B, T, H, K, V, true);
+    if (rc != KDA_OK) return rc;
+    int dev = 0;
+    int* err = nullptr;
+    rc = device_setup(&dev, &err);
+    if (rc != KDA_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool varlen = cu_seqlens != nullptr;
+    const int N = varlen ? num_seqs : B;
+    const Layout L = plan(B, T, H, N, varlen);
+
+    unsigned char* ws = nullptr;
+    if (L.bytes > 0) {
+        if (cudaMallocAsync(reinterpret_cast<void**>(&ws), L.bytes, s) != cudaSuccess) {
+            cudaGetLastError();
+            return KDA_ERR_ALLOC;
+        }
+    }
+    Problem P;
+    P.q = static_cast<const __nv_bfloat16*>(q);
+    P.k = static_cast<const __nv_bfloat16*>(k);
+    P.v = static_cast<const __nv_bfloat16*>(v);
+    P.g = static_cast<const __nv_bfloat16*>(g);
+    P.beta = static_cast<const __nv_bfloat16*>(beta);
+    P.out = static_cast<__nv_bfloat16*>(out);
+    P.A_log = A_log;
+    P.dt_bias = dt_bias;
+    P.scale = scale;
+    P.lower_bound = lower_bound;
+    P.init_state = initial_state;
+    P.init_dtype = initial_state_dtype;
+    P.final_state = final_state;
+    P.final_dtype = final_state_dtype;
+    P.cu_seqlens = cu_seqlens;
+    P.N = N;
+    P.T = T;
+    P.H = H;
+    P.chunks_per_seq = L.chunks_per_seq;
+    P.chunk_bound = L.chunk_bound;
+
+    ChunkMap M{};
+    if (varlen) {
+        int* m = reinterpret_cast<int*>(ws + L.off_map);
+        M.chunk_first = m;
+        M.chunk_seq = m + (N + 1);
+        M.seq_order = M.chunk_seq + L.chunk_bound;
+        M.valid = M.seq_order + N;
+    }
+    Workspace W;
+    W.qg = reinterpret_cast<__half*>(ws + L.off_qg);
+    W.kd = reinterpret_cast<__half*>(ws + L.off_kd);
+    W.wneg = reinterpret_cast<__half*>(ws + L.off_w);
+    W.u = reinterpret_cast<__half*>(ws + L.off_u);
+    W.aqk = reinterpret_cast<__half*>(ws + L.off_aqk);
+    W.gc = reinterpret_cast<float*>(ws + L.off_gc);
+
+    cudaError_t e = cudaSuccess;
+    if (varlen)
+        e = timed_launch(KDA_KERNEL_CHUNKMAP, s, [&] { return launch_chunkmap(P, M, err, s); });
+    if (e == cudaSuccess && P.chunk_bound > 0)
+        e = timed_launch(KDA_KERNEL_INTRA, s, [&] { return launch_intra(P, M, W, s); });
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_STATE, s, [&] { return launch_state(P, M, W, s); });
+    if (ws) cudaFreeAsync(ws, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_LAUNCH;
+    }
+    return KDA_OK;
+}
+
+int kda_fwd_get_error(void* stream) {
+    int dev = 0;
+    int* err = nullptr;
+    int rc = device_setup(&dev, &err);
+    if (rc == KDA_ERR_CUDA) return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    return word;
+}
+
+int kda_fwd_host(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                 float scale, void* out, const float* A_log, const float* dt_bias,
+                 float lower_bound, const void* initial_state, int initial_state_dtype,
+                 void* final_state, int final_state_dtype, const int32_t* cu_seqlens, int num_seqs,
+                 int B, int T, int H, int K, int V, void* stream) {
+    int rc = validate(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
+                      initial_state_dtype, final_state, final_state_dtype, cu_seqlens, num_seqs,
+                      B, T, H, K, V, false);
+    if (rc != KDA_OK) return rc;
+    if (cu_seqlens) {
+        if (cu_seqlens[0] != 0 || cu_seqlens[num_seqs] != T) return KDA_ERR_BAD_SEQLENS;
+        for (int n = 0; n < num_seqs; ++n)
+            if (cu_seqlens[n + 1] < cu_seqlens[n]) return KDA_ERR_BAD_SEQLENS;
+    }
+    int dev = 0;
+    int* err = nullptr;
+    rc = device_setup(&dev, &err);
+    if (rc != KDA_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t tok = (size_t)B * T;
+    const int N = cu_seqlens ? num_seqs : B;
+    const size_t n_qk = tok * H * kDim * 2, n_b = tok * H * 2;
+    const size_t n_s = (size_t)N * H * kDim * kDim;
+    const size_t b_s0 = initial_state ? n_s * (initial_state_dtype == KDA_F32 ? 4 : 2) : 0;
+    const size_t b_s1 = final_state ? n_s * (final_state_dtype == KDA_F32 ? 4 : 2) : 0;
+    const size_t b_cu = cu_seqlens ? sizeof(int32_t) * (num_seqs + 1) : 0;
+    const size_t sizes[] = {n_qk, n_qk, n_qk, n_qk, n_b, n_qk, sizeof(float) * H,
+                            sizeof(float) * H * kDim, b_s0, b_s1, b_cu};
+    size_t total = 0, offs[11];
+    for (int i = 0; i < 11; ++i) {
+        offs[i] = total;
+        total += align_up(sizes[i]);
+    }
+    unsigned char* d = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&d), total, s) != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_ALLOC;
+    }
+    const void* hsrc[] = {q, k, v, g, beta, nullptr, A_log, dt_bias, initial_state, nullptr,
+                          cu_seqlens};
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < 11 && e == cudaSuccess; ++i)
+        if (hsrc[i] && sizes[i])
+            e = cudaMemcpyAsync(d + offs[i], hsrc[i], sizes[i], cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) {
+        rc = kda_fwd(d + offs[0], d + offs[1], d + offs[2], d + offs[3], d + offs[4], scale,
+                     d + offs[5], reinterpret_cast<const float*>(d + offs[6]),
+                     reinterpret_cast<const float*>(d + offs[7]), lower_bound,
+                     initial_state ? d + offs[8] : nullptr, initial_state_dtype,
+                     final_state ? d + offs[9] : nullptr, final_state_dtype,
+                     cu_seqlens ? reinterpret_cast<const int32_t*>(d + offs[10]) : nullptr,
+                     num_seqs, B, T, H, K, V, stream);
+        if (rc == KDA_OK && n_qk)
+            e = cudaMemcpyAsync(out, d + offs[5], n_qk, cudaMemcpyDeviceToHost, s);
+        if (rc == KDA_OK && e == cudaSuccess && final_state)
+            e = cudaMemcpyAsync(final_state, d + offs[9], b_s1, cudaMemcpyDeviceToHost, s);
+    }
+    cudaFreeAsync(d, s);
+    if (cudaStreamSynchronize(s) != cudaSuccess) e = cudaErrorUnknown;
+    if (rc != KDA_OK) return rc;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+int kda_profile_enable(int on) {
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    if (on) {
+        for (auto& r : g_prof.pending) {
+            cudaEventSynchronize(r.stop);
+            g_prof.free_events.push_back(r.start);
+            g_prof.free_events.push_back(r.stop);
+        }
+        g_prof.pending.clear();
+        for (int i = 0; i < KDA_NUM_KERNELS; ++i) {
+            g_prof.total_ms[i] = 0.0;
+            g_prof.launches[i] = 0;
+        }
+    }
+    g_prof.on = on != 0;
+    return KDA_OK;
+}
+
+int kda_profile_read(double* total_ms, long long* launches) {
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    int rc = KDA_OK;
+    for (auto& r : g_prof.pending) {
+        float ms = 0.0f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) {
+            cudaGetLastError();
+            rc = KDA_ERR_CUDA;
+        } else {
+            g_prof.total_ms[r.kernel] += ms;
+            g_prof.launches[r.kernel] += 1;
+        }
+        g_prof.free_events.push_back(r.start);
+        g_prof.free_events.push_back(r.stop);
+    }
+    g_prof.pending.clear();
+    for (int i = 0; i < KDA_NUM_KERNELS; ++i) {
+        if (total_ms) total_ms[i] = g_prof.total_ms[i];
+        if (launches) launches[i] = g_prof.launches[i];
+    }
+    return rc;
+}
+
+const char* kda_kernel_name(int kernel_id) {
+    switch (kernel_id) {
+        case KDA_KERNEL_CHUNKMAP: return "chunkmap_kernel";
+        case KDA_KERNEL_INTRA: return "intra_kernel";
+        case KDA_KERNEL_STATE: return "state_kernel";
+        default: return "unknown";
+    }
+}
+
+}  // extern "C"

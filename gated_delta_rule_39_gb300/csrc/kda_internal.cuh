@@ -1,0 +1,185 @@
+// Internal definitions shared by the KDA forward kernels (sm_103a).
+//
+// Numerics (what each value is stored as, and why):
+//   - gates, cumulative log-decays and their powers of two: fp32
+//   - decay-ratio products A_kk = diag(b) (K*2^G)(K*2^-G)^T and
+//     A_qk = (Q*2^G)(K*2^-G)^T: tf32 tensor-core MMA with fp32 accumulate.
+//     2^-G reaches 2^115 inside a 16-token chunk, which needs an 8-bit
+//     exponent, and the 10-bit tf32 mantissa keeps these products accurate.
+//   - every operand of the sequential state recurrence (state copy, w, u, U,
+//     Q*2^G, K*2^(G_C-G), A_qk, the WY inverse): fp16 with fp32 accumulate.
+//     All of them are bounded by O(1) in magnitude (the inverse's inputs lie
+//     in [-1, 1], "Moonshot AI Open-Sources FlashKDA", "What makes the kernel
+//     fast": fp16 16x16 inversion), and fp16 carries 3 more mantissa bits
+//     than bf16; values that underflow fp16 are below 2^-24 of the state scale.
+//   - the recurrent state itself: fp32 accumulators.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+constexpr int kDim = 128;       // K = V
+constexpr int kChunk = 16;      // tokens per chunk ("What makes the kernel fast": chunk 16)
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---- problem description shared by all kernels ------------------------------
+struct Problem {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const __nv_bfloat16* g;
+    const __nv_bfloat16* beta;
+    __nv_bfloat16* out;
+    const float* A_log;
+    const float* dt_bias;
+    float scale;
+    float lower_bound;
+    const void* init_state;
+    int init_dtype;
+    void* final_state;
+    int final_dtype;
+    const int* cu_seqlens;   // device, or nullptr for fixed length
+    int N;                   // sequences
+    int T;                   // tokens per sequence (fixed) or total tokens (varlen)
+    int H;
+    int chunks_per_seq;      // fixed length: ceil(T/16)
+    int chunk_bound;         // number of chunk slots in the workspace
+};
+
+// Chunk table built on the device for varlen calls.
+struct ChunkMap {
+    int* chunk_first;   // [N+1] first global chunk of each sequence
+    int* chunk_seq;     // [chunk_bound] owning sequence of each chunk, -1 = unused
+    int* seq_order;     // [N] sequences, longest first
+    int* valid;         // [1] 1 if cu_seqlens passed validation
+};
+
+// Per-(chunk, head) intermediates written by the intra-chunk kernel and read
+// by the state kernel.  Index jh = chunk * H + head.
+struct Workspace {
+    __half* qg;     // [jh][16][128]  Q * 2^G
+    __half* kd;     // [jh][16][128]  K * 2^(G_C - G)
+    __half* wneg;   // [jh][16][128]  -(T diag(b) (K * 2^G))
+    __half* u;      // [jh][16][128]  T diag(b) V
+    __half* aqk;    // [jh][16][16]   inclusive-lower Q.K decay products
+    float* gc;      // [jh][128]      2^G_C (decay over the whole chunk)
+};
+
+// Device error word helpers.
+__device__ __forceinline__ void set_error(int* err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// ---- PTX wrappers ------------------------------------------------------------
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// sigmoid(x) = 1 / (1 + 2^(-x log2 e))
+__device__ __forceinline__ float sigmoid_fast(float x) {
+    return rcp_approx(1.0f + ex2_approx(-x * kLog2e));
+}
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// D += A(16x16 f16, row) * B(16x8 f16, col), fp32 accumulate
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// D += A(16x8 tf32, row) * B(8x8 tf32, col), fp32 accumulate
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)),
+                 "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::);
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// ---- chunk -> tokens ----------------------------------------------------------
+struct ChunkSpan {
+    int seq;     // owning sequence, -1 if the slot is unused
+    int tok0;    // first token row
+    int len;     // valid tokens (1..16)
+};
+
+__device__ __forceinline__ ChunkSpan chunk_span(const Problem& P, const ChunkMap& M, int j) {
+    ChunkSpan s;
+    if (P.cu_seqlens == nullptr) {
+        int n = j / P.chunks_per_seq;
+        int c = j - n * P.chunks_per_seq;
+        s.seq = n < P.N ? n : -1;
+        s.tok0 = n * P.T + c * kChunk;
+        s.len = min(kChunk, P.T - c * kChunk);
+    } else {
+        int n = (*M.valid) ? M.chunk_seq[j] : -1;
+        s.seq = n;
+        if (n >= 0) {
+            int c = j - M.chunk_first[n];
+            int start = P.cu_seqlens[n];
+            int end = P.cu_seqlens[n + 1];
+            s.tok0 = start + c * kChunk;
+            s.len = min(kChunk, end - s.tok0);
+        } else {
+            s.tok0 = 0;
+            s.len = 0;
+        }
+    }
+    return s;
+}
+
+// Host-side launchers (defined in the kernel translation units).
+cudaError_t launch_chunkmap(const Problem& P, const ChunkMap& M, int* err, cudaStream_t s);
+cudaError_t launch_intra(const Problem& P, const ChunkMap& M, const Workspace& W,
+                         cudaStream_t s);
+cudaError_t launch_state(const Problem& P, const ChunkMap& M, const Workspace& W,
+                         cudaStream_t s);
+
+}  // namespace kda

@@ -1,0 +1,154 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention forward pass.
+ *
+ * The operation (one independent recurrence per sequence n and head h; the
+ * state S is a K x V matrix, K = V = 128):
+ *
+ *   gate   gl[t,c] = lower_bound * sigmoid(exp(A_log[h]) * (g[t,h,c] + dt_bias[h,c]))
+ *   decay  alpha_t = exp(gl[t,:])                  (per channel, in (exp(lower_bound), 1))
+ *   write  b_t     = sigmoid(beta[t,h])
+ *   state  S_t     = (I - b_t k_t k_t^T) Diag(alpha_t) S_{t-1} + b_t k_t v_t^T
+ *   output o_t     = scale * S_t^T q_t
+ *
+ * Sources: "Moonshot AI Rilis FlashKDA" (captivela.com): the forward pass
+ * takes q, k, v, the pre-activation gate g, beta logits, scale, out, A_log,
+ * dt_bias and lower_bound; sigmoid is applied to beta inside the kernel;
+ * initial and final states are optional and may be bf16 or fp32; q, k, v, g
+ * are bf16 [B,T,H,K|V], beta bf16 [B,T,H], A_log / dt_bias / lower_bound fp32;
+ * cu_seqlens selects variable-length batching; only K = V = 128.
+ * "Moonshot AI Open-Sources FlashKDA" (alphasignal.ai), "Why KDA?": KDA is
+ * Gated DeltaNet with channel-wise gating.  The pages print no formula: the
+ * recurrence above is the gated delta rule with a diagonal decay, and the
+ * gate formula is the reading that makes lower_bound the lower bound of the
+ * per-token log-decay.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers (kda_fwd_host: HOST pointers),
+ *     row-major with the last dimension contiguous, owned by the caller.
+ *     The library keeps no pointer after a call returns.
+ *   - Returns KDA_OK (0) or a negative kda_status.  Argument checks run on the
+ *     host before anything is launched; a rejected call launches nothing and
+ *     writes nothing.
+ *   - kda_fwd is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and never synchronises.  Errors found on the device
+ *     (a malformed cu_seqlens) are recorded in a per-device error word and
+ *     reported by kda_fwd_get_error.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of the optional recurrent states. */
+typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_NULL = -1,            /* a required pointer is NULL                        */
+    KDA_ERR_SHAPE = -2,           /* B, T, H, num_seqs inconsistent or out of range    */
+    KDA_ERR_UNSUPPORTED_DIM = -3, /* K != 128 or V != 128                              */
+    KDA_ERR_ALIGN = -4,           /* q, k, v, g or out not 16-byte aligned             */
+    KDA_ERR_DTYPE = -5,           /* state dtype is neither KDA_BF16 nor KDA_F32       */
+    KDA_ERR_LAUNCH = -6,          /* a kernel launch failed                            */
+    KDA_ERR_DEVICE_TIMEOUT = -7,  /* a bounded device-side wait gave up                */
+    KDA_ERR_BAD_SEQLENS = -8,     /* cu_seqlens not 0 .. T non-decreasing (device)     */
+    KDA_ERR_ARCH = -9,            /* current device is not compute capability 10.3     */
+    KDA_ERR_ALLOC = -10,          /* workspace allocation failed                       */
+    KDA_ERR_CUDA = -11,           /* another CUDA runtime error                        */
+    KDA_ERR_ARG = -12,            /* scale or lower_bound outside the supported range  */
+    KDA_ERR_ALIAS = -13           /* out overlaps an input, or states alias unsafely   */
+} kda_status;
+
+/*
+ * kda_fwd -- KDA forward (prefill) pass.
+ *
+ *   q, k, g     bf16 [B, T, H, K]        v, out   bf16 [B, T, H, V]
+ *   beta        bf16 [B, T, H]           logits; sigmoid is applied inside
+ *   scale       multiplies the output    (finite)
+ *   A_log       fp32 [H]                 dt_bias  fp32 [H, K]
+ *   lower_bound fp32 scalar, in [-5.45, 0]: the per-token log-decay lies in
+ *               [lower_bound, 0]; with 16-token chunks this keeps every
+ *               decay ratio inside the fp32 exponent range
+ *   initial_state  NULL (zero state) or [N, H, K, V] of initial_state_dtype
+ *   final_state    NULL (not written) or [N, H, K, V] of final_state_dtype
+ *               State element [n][h][i][j] is S[i][j]: row i = key channel,
+ *               column j = value channel.  fp32 -> bf16 writes round to
+ *               nearest even.  initial_state and final_state may be the
+ *               same buffer if their dtypes match.
+ *   cu_seqlens  NULL: B sequences of T tokens, N = B.
+ *               Else int32 [num_seqs + 1] DEVICE array of token offsets,
+ *               0 = cu[0] <= cu[1] <= ... <= cu[num_seqs] = T, with B == 1
+ *               and N = num_seqs.  Zero-length sequences are allowed (their
+ *               final state is their initial state).  Checked on the device:
+ *               a malformed array sets KDA_ERR_BAD_SEQLENS in the error word
+ *               and the call then writes neither out nor final_state.
+ *   B, T, H     B >= 1, T >= 0, H >= 1; B*T*H*128 < 2^31
+ *   K, V        must both be 128 (KDA_ERR_UNSUPPORTED_DIM otherwise)
+ *   stream      cudaStream_t to run on
+ *
+ * q, k, v, g and out must be 16-byte aligned; out must not overlap any input.
+ * Scratch memory is taken from the stream-ordered allocator
+ * (cudaMallocAsync / cudaFreeAsync on `stream`) and returned before the call's
+ * work completes; the call does not synchronise.
+ */
+int kda_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+            float scale, void* out, const float* A_log, const float* dt_bias,
+            float lower_bound, const void* initial_state, int initial_state_dtype,
+            void* final_state, int final_state_dtype, const int32_t* cu_seqlens,
+            int num_seqs, int B, int T, int H, int K, int V, void* stream);
+
+/*
+ * kda_fwd_host -- the same operation on HOST buffers (end-to-end entry point).
+ *
+ * Same arguments and layouts as kda_fwd, except that every pointer
+ * (cu_seqlens included) is a host pointer; pinned memory makes the copies
+ * asynchronous.  The call allocates device buffers on `stream`, copies the
+ * inputs host -> device, runs kda_fwd, copies out (and final_state)
+ * device -> host, frees the buffers and synchronises `stream` before
+ * returning, so the outputs are ready on return.  cu_seqlens is validated on
+ * the host (KDA_ERR_BAD_SEQLENS) before anything is copied.
+ */
+int kda_fwd_host(const void* q, const void* k, const void* v, const void* g,
+                 const void* beta, float scale, void* out, const float* A_log,
+                 const float* dt_bias, float lower_bound, const void* initial_state,
+                 int initial_state_dtype, void* final_state, int final_state_dtype,
+                 const int32_t* cu_seqlens, int num_seqs, int B, int T, int H, int K, int V,
+                 void* stream);
+
+/*
+ * kda_fwd_get_error -- synchronise `stream`, then return and clear the current
+ * device's error word: KDA_OK, KDA_ERR_BAD_SEQLENS or KDA_ERR_DEVICE_TIMEOUT
+ * (or KDA_ERR_CUDA if the synchronisation itself failed).
+ */
+int kda_fwd_get_error(void* stream);
+
+/* Human-readable name of a kda_status value (static string, never NULL). */
+const char* kda_status_string(int status);
+
+/* Bytes of scratch memory kda_fwd takes from the stream-ordered allocator for
+ * the given problem (0 for an empty problem).  Host-only, no CUDA call. */
+size_t kda_fwd_workspace_bytes(int B, int T, int H, int num_seqs, int varlen);
+
+/* ---- launch accounting (for measurement; off by default) ------------------
+ *
+ * kda_profile_enable(1) makes every later kda_fwd record a CUDA event before
+ * and after each of its kernel launches, on the launch stream; enable(0)
+ * stops recording.  Enabling clears the totals.  kda_profile_read
+ * synchronises on the recorded events and returns, per kernel id
+ * (KDA_KERNEL_*), the summed device time in milliseconds and the number of
+ * launches since the last enable.  Arrays must hold KDA_NUM_KERNELS entries.
+ * Returns KDA_OK, or KDA_ERR_CUDA. */
+enum { KDA_KERNEL_CHUNKMAP = 0, KDA_KERNEL_INTRA = 1, KDA_KERNEL_STATE = 2, KDA_NUM_KERNELS = 3 };
+int kda_profile_enable(int on);
+int kda_profile_read(double* total_ms, long long* launches);
+const char* kda_kernel_name(int kernel_id);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_H_ */
