@@ -39,11 +39,9 @@ C = 16
 # plus, per (sequence, head), the initial state read and the final state write.
 FLOP_PER_TH = 6 * K * V + 2 * C * (3 * K + 2 * V)
 BYTES_PER_TH = 4 * 2 * 128 + 2 + 2 * 128
-# Per-kernel algorithmic work (the split of the figures above between kernels):
-#   intra_kernel: reads q, k, v, g, beta; A_kk, A_qk, w, u contractions
-#   state_kernel: writes out and the states; S^T q, U, state update, A_qk U
-KERNEL_FLOP_PER_TH = {"intra_kernel": 2 * C * (3 * K + V), "state_kernel": 6 * K * V + 2 * C * V}
-KERNEL_BYTES_PER_TH = {"intra_kernel": 4 * 2 * 128 + 2, "state_kernel": 2 * 128}
+# The fused kernel does the whole path, so its algorithmic work is the path's.
+KERNEL_FLOP_PER_TH = {"fused_kernel": FLOP_PER_TH}
+KERNEL_BYTES_PER_TH = {"fused_kernel": BYTES_PER_TH}
 
 
 def peaks():
@@ -180,7 +178,11 @@ def run_cuda(args, world, rank, local, pg):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     kda.load_library()
-    d = synth.make_workload(WORKLOAD, seed=rank)
+    if args.heads:
+        w = synth.WORKLOADS[WORKLOAD]
+        d = synth.make_inputs(w.B, w.T, args.heads, seed=rank, init_dtype=w.init_dtype)
+    else:
+        d = synth.make_workload(WORKLOAD, seed=rank)
     B, T, H, _ = d["q"].shape
     N = d["N"]
 
@@ -240,7 +242,7 @@ def run_cuda(args, world, rank, local, pg):
     dom_ms = prof[dom][0] / max(1, prof[dom][1])
     dom_flop = KERNEL_FLOP_PER_TH.get(dom, 0) * th
     dom_bytes = KERNEL_BYTES_PER_TH.get(dom, 0) * th
-    if dom == "state_kernel":
+    if dom == "fused_kernel":
         dom_bytes += N * H * K * V * (2 + 4)   # bf16 initial state read, fp32 final write
     t_hbm = dom_bytes / (hbm * 1e9)
     t_tc = dom_flop / (tflops * 1e12)
@@ -300,12 +302,16 @@ def run_cuda(args, world, rank, local, pg):
 
     clocks = sampler.summary() if sampler else None
     if rank == 0:
+        if args.heads:
+            line_workload = f"{WORKLOAD} with H={H} (profiling case, not a bench line)"
+        else:
+            line_workload = WORKLOAD
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "compute": "f16 and tf32 tensor-core MMA, f32 accumulate",
                 "data": "synthetic (seeded; shapes of the pages' T=8192 H=96 D=128 benchmark)",
-                "config": {"workload": WORKLOAD, "B": B, "T": T, "H": H, "K": K, "V": V,
+                "config": {"workload": line_workload, "B": B, "T": T, "H": H, "K": K, "V": V,
                            "initial_state": "bf16", "final_state": "f32",
                            "l2": "inputs larger than L2 (1.02 GB read+written per step vs "
                                  "126 MB L2); no flush",
@@ -397,6 +403,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--heads", type=int, default=0,
+                    help="profiling only: run the workload with this many heads instead")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "cuda":
         print("note: warm-up raised to 3 steps", file=sys.stderr)

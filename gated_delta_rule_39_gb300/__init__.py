@@ -23,8 +23,8 @@ _LIB_PATH = os.path.join(_HERE, "_lib", "libkda.so")
 
 KDA_BF16 = 0
 KDA_F32 = 1
-KDA_NUM_KERNELS = 3
-KERNEL_NAMES = ("chunkmap_kernel", "intra_kernel", "state_kernel")
+KDA_NUM_KERNELS = 2
+KERNEL_NAMES = ("seqmap_kernel", "fused_kernel")
 
 _lib = None
 _vp = ctypes.c_void_p

@@ -102,37 +102,14 @@ cudaError_t timed_launch(int kernel, cudaStream_t s, F&& launch) {
     return e;
 }
 
-// ---- sizes ------------------------------------------------------------------
+// ---- scratch ------------------------------------------------------------------
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
-struct Layout {
-    int chunk_bound = 0;
-    int chunks_per_seq = 0;
-    size_t off_map = 0, off_qg = 0, off_kd = 0, off_w = 0, off_u = 0, off_aqk = 0, off_gc = 0;
-    size_t bytes = 0;
-};
-
-Layout plan(int B, int T, int H, int N, bool varlen) {
-    Layout L;
-    if (varlen) {
-        L.chunk_bound = T / kChunk + N + 1;
-    } else {
-        L.chunks_per_seq = (T + kChunk - 1) / kChunk;
-        L.chunk_bound = B * L.chunks_per_seq;
-    }
-    const size_t jh = (size_t)L.chunk_bound * H;
-    size_t off = 0;
-    L.off_map = off;
-    if (varlen) off += align_up(sizeof(int) * ((size_t)N + 1 + L.chunk_bound + N + 1));
-    L.off_qg = off;  off += align_up(jh * kChunk * kDim * sizeof(__half));
-    L.off_kd = off;  off += align_up(jh * kChunk * kDim * sizeof(__half));
-    L.off_w = off;   off += align_up(jh * kChunk * kDim * sizeof(__half));
-    L.off_u = off;   off += align_up(jh * kChunk * kDim * sizeof(__half));
-    L.off_aqk = off; off += align_up(jh * kChunk * kChunk * sizeof(__half));
-    L.off_gc = off;  off += align_up(jh * kDim * sizeof(float));
-    L.bytes = (jh == 0 && !varlen) ? 0 : off;
-    return L;
+// Scratch of one call: the varlen sequence map (longest-first order + valid
+// flag); fixed-length calls need none.
+size_t scratch_bytes(int N, bool varlen) {
+    return varlen ? align_up(sizeof(int) * ((size_t)N + 1)) : 0;
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -207,8 +184,7 @@ const char* kda_status_string(int status) {
 
 size_t kda_fwd_workspace_bytes(int B, int T, int H, int num_seqs, int varlen) {
     if (B < 1 || T < 0 || H < 1) return 0;
-    const int N = varlen ? num_seqs : B;
-    return plan(B, T, H, N, varlen != 0).bytes;
+    return scratch_bytes(varlen ? num_seqs : B, varlen != 0);
 }
 
 int kda_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
@@ -227,11 +203,11 @@ int kda_fwd(const void* q, const void* k, const void* v, const void* g, const vo
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool varlen = cu_seqlens != nullptr;
     const int N = varlen ? num_seqs : B;
-    const Layout L = plan(B, T, H, N, varlen);
+    const size_t bytes = scratch_bytes(N, varlen);
 
-    unsigned char* ws = nullptr;
-    if (L.bytes > 0) {
-        if (cudaMallocAsync(reinterpret_cast<void**>(&ws), L.bytes, s) != cudaSuccess) {
+    int* scratch = nullptr;
+    if (bytes > 0) {
+        if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), bytes, s) != cudaSuccess) {
             cudaGetLastError();
             return KDA_ERR_ALLOC;
         }
@@ -255,33 +231,18 @@ int kda_fwd(const void* q, const void* k, const void* v, const void* g, const vo
     P.N = N;
     P.T = T;
     P.H = H;
-    P.chunks_per_seq = L.chunks_per_seq;
-    P.chunk_bound = L.chunk_bound;
 
-    ChunkMap M{};
+    SeqMap M{};
     if (varlen) {
-        int* m = reinterpret_cast<int*>(ws + L.off_map);
-        M.chunk_first = m;
-        M.chunk_seq = m + (N + 1);
-        M.seq_order = M.chunk_seq + L.chunk_bound;
-        M.valid = M.seq_order + N;
+        M.seq_order = scratch;
+        M.valid = scratch + N;
     }
-    Workspace W;
-    W.qg = reinterpret_cast<__half*>(ws + L.off_qg);
-    W.kd = reinterpret_cast<__half*>(ws + L.off_kd);
-    W.wneg = reinterpret_cast<__half*>(ws + L.off_w);
-    W.u = reinterpret_cast<__half*>(ws + L.off_u);
-    W.aqk = reinterpret_cast<__half*>(ws + L.off_aqk);
-    W.gc = reinterpret_cast<float*>(ws + L.off_gc);
-
     cudaError_t e = cudaSuccess;
     if (varlen)
-        e = timed_launch(KDA_KERNEL_CHUNKMAP, s, [&] { return launch_chunkmap(P, M, err, s); });
-    if (e == cudaSuccess && P.chunk_bound > 0)
-        e = timed_launch(KDA_KERNEL_INTRA, s, [&] { return launch_intra(P, M, W, s); });
+        e = timed_launch(KDA_KERNEL_SEQMAP, s, [&] { return launch_seqmap(P, M, err, s); });
     if (e == cudaSuccess)
-        e = timed_launch(KDA_KERNEL_STATE, s, [&] { return launch_state(P, M, W, s); });
-    if (ws) cudaFreeAsync(ws, s);
+        e = timed_launch(KDA_KERNEL_FUSED, s, [&] { return launch_fused(P, M, err, s); });
+    if (scratch) cudaFreeAsync(scratch, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return KDA_ERR_LAUNCH;
@@ -413,9 +374,8 @@ int kda_profile_read(double* total_ms, long long* launches) {
 
 const char* kda_kernel_name(int kernel_id) {
     switch (kernel_id) {
-        case KDA_KERNEL_CHUNKMAP: return "chunkmap_kernel";
-        case KDA_KERNEL_INTRA: return "intra_kernel";
-        case KDA_KERNEL_STATE: return "state_kernel";
+        case KDA_KERNEL_SEQMAP: return "seqmap_kernel";
+        case KDA_KERNEL_FUSED: return "fused_kernel";
         default: return "unknown";
     }
 }

@@ -47,27 +47,12 @@ struct Problem {
     int N;                   // sequences
     int T;                   // tokens per sequence (fixed) or total tokens (varlen)
     int H;
-    int chunks_per_seq;      // fixed length: ceil(T/16)
-    int chunk_bound;         // number of chunk slots in the workspace
 };
 
-// Chunk table built on the device for varlen calls.
-struct ChunkMap {
-    int* chunk_first;   // [N+1] first global chunk of each sequence
-    int* chunk_seq;     // [chunk_bound] owning sequence of each chunk, -1 = unused
+// Scratch written by the varlen sequence map, read by the fused kernel.
+struct SeqMap {
     int* seq_order;     // [N] sequences, longest first
     int* valid;         // [1] 1 if cu_seqlens passed validation
-};
-
-// Per-(chunk, head) intermediates written by the intra-chunk kernel and read
-// by the state kernel.  Index jh = chunk * H + head.
-struct Workspace {
-    __half* qg;     // [jh][16][128]  Q * 2^G
-    __half* kd;     // [jh][16][128]  K * 2^(G_C - G)
-    __half* wneg;   // [jh][16][128]  -(T diag(b) (K * 2^G))
-    __half* u;      // [jh][16][128]  T diag(b) V
-    __half* aqk;    // [jh][16][16]   inclusive-lower Q.K decay products
-    float* gc;      // [jh][128]      2^G_C (decay over the whole chunk)
 };
 
 // Device error word helpers.
@@ -143,43 +128,9 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-// ---- chunk -> tokens ----------------------------------------------------------
-struct ChunkSpan {
-    int seq;     // owning sequence, -1 if the slot is unused
-    int tok0;    // first token row
-    int len;     // valid tokens (1..16)
-};
-
-__device__ __forceinline__ ChunkSpan chunk_span(const Problem& P, const ChunkMap& M, int j) {
-    ChunkSpan s;
-    if (P.cu_seqlens == nullptr) {
-        int n = j / P.chunks_per_seq;
-        int c = j - n * P.chunks_per_seq;
-        s.seq = n < P.N ? n : -1;
-        s.tok0 = n * P.T + c * kChunk;
-        s.len = min(kChunk, P.T - c * kChunk);
-    } else {
-        int n = (*M.valid) ? M.chunk_seq[j] : -1;
-        s.seq = n;
-        if (n >= 0) {
-            int c = j - M.chunk_first[n];
-            int start = P.cu_seqlens[n];
-            int end = P.cu_seqlens[n + 1];
-            s.tok0 = start + c * kChunk;
-            s.len = min(kChunk, end - s.tok0);
-        } else {
-            s.tok0 = 0;
-            s.len = 0;
-        }
-    }
-    return s;
-}
-
 // Host-side launchers (defined in the kernel translation units).
-cudaError_t launch_chunkmap(const Problem& P, const ChunkMap& M, int* err, cudaStream_t s);
-cudaError_t launch_intra(const Problem& P, const ChunkMap& M, const Workspace& W,
-                         cudaStream_t s);
-cudaError_t launch_state(const Problem& P, const ChunkMap& M, const Workspace& W,
-                         cudaStream_t s);
+cudaError_t launch_seqmap(const Problem& P, const SeqMap& M, int* err, cudaStream_t s);
+cudaError_t launch_fused(const Problem& P, const SeqMap& M, int* err, cudaStream_t s);
+size_t fused_smem_bytes();
 
 }  // namespace kda

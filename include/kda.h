@@ -71,7 +71,7 @@ typedef enum {
  *   beta        bf16 [B, T, H]           logits; sigmoid is applied inside
  *   scale       multiplies the output    (finite)
  *   A_log       fp32 [H]                 dt_bias  fp32 [H, K]
- *   lower_bound fp32 scalar, in [-5.45, 0]: the per-token log-decay lies in
+ *   lower_bound fp32 scalar, in [-5.5, 0]: the per-token log-decay lies in
  *               [lower_bound, 0]; with 16-token chunks this keeps every
  *               decay ratio inside the fp32 exponent range
  *   initial_state  NULL (zero state) or [N, H, K, V] of initial_state_dtype
@@ -92,9 +92,10 @@ typedef enum {
  *   stream      cudaStream_t to run on
  *
  * q, k, v, g and out must be 16-byte aligned; out must not overlap any input.
- * Scratch memory is taken from the stream-ordered allocator
- * (cudaMallocAsync / cudaFreeAsync on `stream`) and returned before the call's
- * work completes; the call does not synchronise.
+ * Fixed-length calls use no scratch memory.  Varlen calls take
+ * kda_fwd_workspace_bytes() of scratch (the longest-first sequence order)
+ * from the stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on
+ * `stream`); the call does not synchronise.
  */
 int kda_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
             float scale, void* out, const float* A_log, const float* dt_bias,
@@ -143,7 +144,7 @@ size_t kda_fwd_workspace_bytes(int B, int T, int H, int num_seqs, int varlen);
  * (KDA_KERNEL_*), the summed device time in milliseconds and the number of
  * launches since the last enable.  Arrays must hold KDA_NUM_KERNELS entries.
  * Returns KDA_OK, or KDA_ERR_CUDA. */
-enum { KDA_KERNEL_CHUNKMAP = 0, KDA_KERNEL_INTRA = 1, KDA_KERNEL_STATE = 2, KDA_NUM_KERNELS = 3 };
+enum { KDA_KERNEL_SEQMAP = 0, KDA_KERNEL_FUSED = 1, KDA_NUM_KERNELS = 2 };
 int kda_profile_enable(int on);
 int kda_profile_read(double* total_ms, long long* launches);
 const char* kda_kernel_name(int kernel_id);

@@ -109,9 +109,8 @@ def test_rejects_aliasing(lib):
 def test_workspace_size(lib):
     import gated_delta_rule_39_gb300 as kda
     assert kda.kda_fwd_workspace_bytes(1, 0, 4) == 0
-    b = kda.kda_fwd_workspace_bytes(1, 8192, 96)
-    assert b >= 8192 * 96 * (4 * 256 + 32 + 32)
-    assert kda.kda_fwd_workspace_bytes(1, 8192, 96, 12, True) >= b
+    assert kda.kda_fwd_workspace_bytes(1, 8192, 96) == 0          # fixed length: none
+    assert kda.kda_fwd_workspace_bytes(1, 8192, 96, 12, True) >= 4 * 13
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -212,6 +212,5 @@ def test_profile_counts_launches():
     run_gpu(d)
     prof = kda.kda_profile_read()
     kda.kda_profile_enable(False)
-    assert prof["chunkmap_kernel"][1] == 2
-    assert prof["intra_kernel"][1] == 2 and prof["state_kernel"][1] == 2
+    assert prof["seqmap_kernel"][1] == 2 and prof["fused_kernel"][1] == 2
     assert all(ms > 0 for ms, n in prof.values() if n)
