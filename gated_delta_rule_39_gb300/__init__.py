@@ -13,7 +13,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["KdaError", "kda_fwd", "kda_fwd_host", "kda_fwd_get_error", "kda_status_string",
+__all__ = ["KdaError", "kda_fwd", "kda_fwd_host", "kda_fwd_noalloc", "kda_fwd_get_error", "kda_status_string",
            "kda_fwd_workspace_bytes", "kda_profile_enable", "kda_profile_read",
            "kda_kernel_name", "lib_path", "load_library", "KDA_BF16", "KDA_F32",
            "KERNEL_NAMES"]
@@ -56,6 +56,8 @@ def load_library():
     lib.kda_fwd.restype = ctypes.c_int
     lib.kda_fwd_host.argtypes = fwd_args
     lib.kda_fwd_host.restype = ctypes.c_int
+    lib.kda_fwd_noalloc.argtypes = fwd_args
+    lib.kda_fwd_noalloc.restype = ctypes.c_int
     lib.kda_fwd_get_error.argtypes = [_vp]
     lib.kda_fwd_get_error.restype = ctypes.c_int
     lib.kda_status_string.argtypes = [ctypes.c_int]
@@ -166,6 +168,33 @@ def kda_fwd(q, k, v, g, beta, scale: float, out, A_log, dt_bias, lower_bound: fl
             _ptr(cu_seqlens), N if cu_seqlens is not None else 0, B, T, H, K, V, s)
     if rc != 0:
         raise KdaError(rc)
+
+
+def kda_fwd_noalloc(q, k, v, g, beta, scale: float, out, A_log, dt_bias, lower_bound: float,
+                    initial_state=None, final_state=None, cu_seqlens=None, stream=None) -> None:
+    """kda_fwd without any device allocation, for callers that cannot allocate.
+
+    Same arguments and results as ``kda_fwd``.  Varlen calls keep their
+    scratch in a fixed array inside the library (at most KDA_NOALLOC_MAX_SEQS =
+    65536 sequences); calls that overlap on the GPU share that array and race.
+    """
+    import torch
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("kda_fwd_noalloc takes CUDA tensors")
+    B, T, H, K, V, N = _marshal(q, k, v, g, beta, out, A_log, dt_bias, initial_state,
+                                final_state, cu_seqlens, dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    s = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    with torch.cuda.device(dev):
+        rc = load_library().kda_fwd_noalloc(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
+            _ptr(A_log), _ptr(dt_bias), float(lower_bound), _ptr(initial_state),
+            _state_dtype(initial_state), _ptr(final_state), _state_dtype(final_state),
+            _ptr(cu_seqlens), N if cu_seqlens is not None else 0, B, T, H, K, V, s)
+    if rc != 0:
+        raise KdaError(rc, "kda_fwd_noalloc")
 
 
 def kda_fwd_host(q, k, v, g, beta, scale: float, out, A_log, dt_bias, lower_bound: float,

@@ -158,6 +158,32 @@ int validate(const void* q, const void* k, const void* v, const void* g, const v
 }  // namespace
 }  // namespace kda
 
+// ---- scratch of kda_fwd_noalloc -------------------------------------------------
+// The varlen sequence map of kda_fwd_noalloc lives in this fixed device array
+// instead of memory from the allocator.  In host code the name only stands in
+// for the device copy: its device address comes from cudaGetSymbolAddress,
+// looked up once per device (with that device current) and cached.
+static __device__ __align__(256) int g_noalloc_scratch[KDA_NOALLOC_MAX_SEQS + 1];
+
+namespace {
+int* g_noalloc_addr[kda::kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+int noalloc_scratch(int dev, int** addr) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return KDA_ERR_CUDA;
+        }
+        g_noalloc_addr[dev] = static_cast<int*>(p);
+    }
+    *addr = g_noalloc_addr[dev];
+    return KDA_OK;
+}
+}  // namespace
+
 using namespace kda;
 
 extern "C" {
@@ -178,6 +204,9 @@ const char* kda_status_string(int status) {
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
         case KDA_ERR_ARG: return "KDA_ERR_ARG: scale must be finite, lower_bound in [-5.5, 0]";
         case KDA_ERR_ALIAS: return "KDA_ERR_ALIAS: out overlaps an input or states alias unsafely";
+        case KDA_ERR_SCRATCH_LIMIT:
+            return "KDA_ERR_SCRATCH_LIMIT: kda_fwd_noalloc takes at most KDA_NOALLOC_MAX_SEQS "
+                   "(65536) sequences";
         default: return "unknown kda_status";
     }
 }
@@ -326,6 +355,63 @@ int kda_fwd_host(const void* q, const void* k, const void* v, const void* g, con
     if (e != cudaSuccess) {
         cudaGetLastError();
         return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+int kda_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
+                    const void* beta, float scale, void* out, const float* A_log,
+                    const float* dt_bias, float lower_bound, const void* initial_state,
+                    int initial_state_dtype, void* final_state, int final_state_dtype,
+                    const int32_t* cu_seqlens, int num_seqs, int B, int T, int H, int K, int V,
+                    void* stream) {
+    int rc = validate(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
+                      initial_state_dtype, final_state, final_state_dtype, cu_seqlens, num_seqs,
+                      B, T, H, K, V, true);
+    if (rc != KDA_OK) return rc;
+    const bool varlen = cu_seqlens != nullptr;
+    if (varlen && num_seqs > KDA_NOALLOC_MAX_SEQS) return KDA_ERR_SCRATCH_LIMIT;
+    int dev = 0;
+    int* err = nullptr;
+    rc = device_setup(&dev, &err);
+    if (rc != KDA_OK) return rc;
+    int* scratch = nullptr;
+    if (varlen) {
+        rc = noalloc_scratch(dev, &scratch);
+        if (rc != KDA_OK) return rc;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int N = varlen ? num_seqs : B;
+    Problem P;
+    P.q = static_cast<const __nv_bfloat16*>(q);
+    P.k = static_cast<const __nv_bfloat16*>(k);
+    P.v = static_cast<const __nv_bfloat16*>(v);
+    P.g = static_cast<const __nv_bfloat16*>(g);
+    P.beta = static_cast<const __nv_bfloat16*>(beta);
+    P.out = static_cast<__nv_bfloat16*>(out);
+    P.A_log = A_log;
+    P.dt_bias = dt_bias;
+    P.scale = scale;
+    P.lower_bound = lower_bound;
+    P.init_state = initial_state;
+    P.init_dtype = initial_state_dtype;
+    P.final_state = final_state;
+    P.final_dtype = final_state_dtype;
+    P.cu_seqlens = cu_seqlens;
+    P.N = N;
+    P.T = T;
+    P.H = H;
+    SeqMap M{};
+    if (varlen) {
+        M.seq_order = scratch;       // every entry rewritten by the sequence map
+        M.valid = scratch + N;       // set to 0 or 1 by the sequence map
+    }
+    cudaError_t e = cudaSuccess;
+    if (varlen) e = launch_seqmap(P, M, err, s);
+    if (e == cudaSuccess) e = launch_fused(P, M, err, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_LAUNCH;
     }
     return KDA_OK;
 }

@@ -61,7 +61,8 @@ typedef enum {
     KDA_ERR_ALLOC = -10,          /* workspace allocation failed                       */
     KDA_ERR_CUDA = -11,           /* another CUDA runtime error                        */
     KDA_ERR_ARG = -12,            /* scale or lower_bound outside the supported range  */
-    KDA_ERR_ALIAS = -13           /* out overlaps an input, or states alias unsafely   */
+    KDA_ERR_ALIAS = -13,          /* out overlaps an input, or states alias unsafely   */
+    KDA_ERR_SCRATCH_LIMIT = -14   /* kda_fwd_noalloc: num_seqs > KDA_NOALLOC_MAX_SEQS   */
 } kda_status;
 
 /*
@@ -134,6 +135,42 @@ const char* kda_status_string(int status);
 /* Bytes of scratch memory kda_fwd takes from the stream-ordered allocator for
  * the given problem (0 for an empty problem).  Host-only, no CUDA call. */
 size_t kda_fwd_workspace_bytes(int B, int T, int H, int num_seqs, int varlen);
+
+/*
+ * kda_fwd_noalloc -- kda_fwd for callers that cannot allocate device memory.
+ *
+ * No counterpart on the pages: this entry point exists for users of the
+ * library whose device memory is not theirs to allocate from -- a serving
+ * runtime or framework that reserves its whole memory budget up front and
+ * owns every byte through its own allocator, or a hot loop that must not
+ * pay for (or synchronise on) an allocation.  kda_fwd takes a small scratch
+ * buffer from cudaMallocAsync on varlen calls; this variant takes it from a
+ * fixed array in the library's own device memory instead, and calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Same arguments, layouts, checks and results as kda_fwd (the caller still
+ * passes every input and output buffer), plus:
+ *   - The scratch is a static device array sized for KDA_NOALLOC_MAX_SEQS
+ *     sequences (about 256 KB).  Every GPU that loads this library holds one
+ *     copy of it until the process exits.  Varlen calls with
+ *     num_seqs > KDA_NOALLOC_MAX_SEQS return KDA_ERR_SCRATCH_LIMIT and launch
+ *     nothing.  Fixed-length calls use no scratch.
+ *   - The first varlen call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the one array.  Each call rewrites the part
+ *     it uses before reading it (nothing needs to start at zero), but calls
+ *     whose work overlaps on the GPU -- on different streams, or from
+ *     different host threads -- race on it: order them on one stream or
+ *     synchronise between them.
+ */
+#define KDA_NOALLOC_MAX_SEQS 65536
+int kda_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
+                    const void* beta, float scale, void* out, const float* A_log,
+                    const float* dt_bias, float lower_bound, const void* initial_state,
+                    int initial_state_dtype, void* final_state, int final_state_dtype,
+                    const int32_t* cu_seqlens, int num_seqs, int B, int T, int H, int K, int V,
+                    void* stream);
 
 /* ---- launch accounting (for measurement; off by default) ------------------
  *
