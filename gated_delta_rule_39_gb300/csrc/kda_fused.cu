@@ -2,20 +2,22 @@
 // the chunkwise algorithm, so q, k, v, g and beta are read from HBM once and
 // only the output and the states are written.
 //
-//   producer warps (4)  token-parallel stage, one 16-token chunk per warp at a
-//                       time, running ahead of the recurrence: gates, in-chunk
-//                       cumulative base-2 log-decay G, decay-ratio products
-//                       A_kk / A_qk (tf32 MMA), (I + A_kk)^-1 by forward
-//                       substitution, WY factors u = T diag(b) V and
+//   producer teams (2 x 4 warps)  the token-parallel stage.  Team t handles
+//                       chunks t, t+2, t+4, ... with its four warps working
+//                       together on one chunk while the next chunk's rows are
+//                       already in flight (double-buffered cp.async): gates,
+//                       in-chunk cumulative base-2 log-decay G, decay-ratio
+//                       products A_kk / A_qk (tf32 MMA), (I + A_kk)^-1 by
+//                       forward substitution, WY factors u = T diag(b) V and
 //                       w = T diag(b)(K * 2^G) (fp16 MMA), Q * 2^G,
 //                       K * 2^(G_last - G), 2^G_last
-//   chain warps (8)     sequential stage over the chunks: the fp32 state lives
-//                       in registers as S^T fragments, 16 value rows per warp;
-//                       per chunk U^T = u^T - S^T w^T, O^T = S^T (Q 2^G)^T +
-//                       U^T A_qk^T, S^T <- S^T Diag(2^G_last) + U^T (K 2^(G_last-G))
+//   chain warps (8)     the sequential stage over the chunks: the fp32 state
+//                       lives in registers as S^T fragments, 16 value rows per
+//                       warp; per chunk U^T = u^T - S^T w^T, O^T = S^T (Q 2^G)^T
+//                       + U^T A_qk^T, S^T <- S^T Diag(2^G_last) + U^T (K 2^(G_last-G))
 //
 // The stages hand chunk factors over through a 4-slot shared-memory ring
-// guarded by mbarriers (full: producer -> chain, empty: chain -> producer);
+// guarded by mbarriers (full: producers -> chain, empty: chain -> producers);
 // every wait is bounded and gives up with KDA_ERR_DEVICE_TIMEOUT.
 //
 // Chunkwise DPLR-variant (WY) algorithm with 16-token chunks, a 16 x 16
@@ -25,53 +27,75 @@
 // SMs idle; here the split stays, but inside one CTA, so the intermediate
 // factors never leave shared memory.
 #include "kda_internal.cuh"
+#include "kda_tcgen05.cuh"
 
 namespace kda {
 
 namespace {
 
-constexpr int kChainWarps = 8;              // 8 x 16 value rows = V
-constexpr int kProdWarps = 4;
-constexpr int kRing = 4;                    // chunk-factor slots
-constexpr int kThreads = (kChainWarps + kProdWarps) * 32;
-static_assert(kRing == kProdWarps, "producer p always fills slot p");
+constexpr int kEpiWarps = 4;                // epilogue: one TMEM lane (value row) per thread
+constexpr int kMmaWarp = kEpiWarps;         // issues the tcgen05 MMAs, owns tensor memory
+constexpr int kTeams = 2;                   // producer teams
+constexpr int kTeamWarps = 4;
+constexpr int kTeamThreads = kTeamWarps * 32;
+constexpr int kProdWarp0 = kMmaWarp + 1;
+constexpr int kRing = 4;                    // chunk-operand slots
+constexpr int kThreads = (kProdWarp0 + kTeams * kTeamWarps) * 32;
 
 constexpr int RAW_LD = 136;   // bf16 / fp16 per padded 128-wide row (272 B)
-constexpr int G_LD = 132;     // fp32 per padded row of cumulative gates
+constexpr int F_LD = 132;     // fp32 per padded 128-wide row (528 B: ldmatrix conflict-free)
 constexpr int A_LD = 17;
 constexpr int TB_LD = 24;     // fp16 per row of T diag(b) (48 B)
-constexpr int LD = 136;       // fp16 per padded 128-wide row of a chunk factor
-constexpr int AQ_LD = 24;
-constexpr int O_LD = 24;
 
-struct ProdSmem {
+// tensor-memory columns (one allocation of 512)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t TM_S32 = 0;     // S^T, fp32, 128 columns
+constexpr uint32_t TM_S16 = 128;   // S^T as the fp16 A operand, 64 columns
+constexpr uint32_t TM_UO = 192;    // [U | O] accumulators, 2 buffers x 32 columns
+constexpr uint32_t TM_U16 = 256;   // U^T as the fp16 A operand, 8 columns
+
+// Raw rows of one chunk.  After the gate pass, g holds fp16 K * 2^G in place.
+struct RawChunk {
     __nv_bfloat16 q[kChunk * RAW_LD];
     __nv_bfloat16 k[kChunk * RAW_LD];
-    __nv_bfloat16 v[kChunk * RAW_LD];   // rewritten in place as fp16 V
-    __nv_bfloat16 g[kChunk * RAW_LD];   // rewritten in place as fp16 K * 2^G
-    float G[kChunk * G_LD];
+    __nv_bfloat16 v[kChunk * RAW_LD];
+    __nv_bfloat16 g[kChunk * RAW_LD];
+};
+struct TeamSmem {
+    RawChunk raw[2];                // double buffer: chunk being worked on / next chunk
+    float kg32[kChunk * F_LD];      // tf32 operands of the decay-ratio products
+    float ki32[kChunk * F_LD];
+    float qg32[kChunk * F_LD];
+    float part[kTeamWarps][2][kChunk * kChunk];   // per-warp partial A_kk, A_qk
     float A[kChunk * A_LD];
     __half tb[kChunk * TB_LD];
     float beta[kChunk];
 };
+// One chunk's operands for the tensor-core recurrence (canonical K-major layouts)
 struct Stage {
-    __half qg[kChunk * LD];
-    __half kd[kChunk * LD];
-    __half w[kChunk * LD];     // negated
-    __half u[kChunk * LD];
-    __half aqk[kChunk * AQ_LD];
-    float gc[kDim];
+    __half buo[2 * 32 * 64];   // B of [U|O] += S^T [-w; Q 2^G]^T: 32 x 128, 128B swizzle
+    __half vt[128 * 16];       // A of u^T = V^T (T diag b)^T: V^T 128 x 16, interleaved
+    __half kdt[128 * 16];      // B of the state update: (K 2^(G_last-G))^T 128 x 16
+    __half tbt[32 * 16];       // B of the u MMA: rows 0-15 T diag(b), rows 16-31 zero
+    __half aqk[16 * 16];       // B of O += U A_qk^T: A_qk 16 x 16
+    float gc[kDim];            // 2^G_last
 };
+static_assert(sizeof(Stage) % 1024 == 0, "stages keep the swizzled tiles 1024-byte aligned");
 struct Smem {
-    ProdSmem prod[kProdWarps];
     Stage st[kRing];
-    __nv_bfloat16 ostage[kChainWarps][kChunk * O_LD];
-    unsigned long long full[kRing];
-    unsigned long long empty[kRing];
+    TeamSmem team[kTeams];
+    unsigned long long full[kRing];    // producers -> MMA / epilogue
+    unsigned long long empty[kRing];   // MMA commit -> producers
+    unsigned long long uo_done;        // U|O MMAs complete
+    unsigned long long s_done;         // state update + O MMAs complete
+    unsigned long long s16_ready;      // epilogue: S^T fp16 copy written, S^T rescaled
+    unsigned long long u16_ready;      // epilogue: U^T fp16 copy written
+    unsigned long long epi_done;       // epilogue finished with tensor memory
+    uint32_t tmem_base;
 };
-static_assert(sizeof(ProdSmem) % 16 == 0 && sizeof(Stage) % 16 == 0, "16-byte alignment");
+static_assert(sizeof(RawChunk) % 16 == 0 && sizeof(TeamSmem) % 16 == 0, "16-byte alignment");
 
-// ---- mbarrier helpers ---------------------------------------------------------
+// ---- small helpers ------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(unsigned long long* b, int count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(b)), "r"(count));
 }
@@ -101,339 +125,464 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* b, unsigned parity
     }
     return true;
 }
-
-__device__ __forceinline__ void unpack4(uint2 raw, float (&f)[4]) {
-    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&raw.x);
-    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
-    f[0] = __low2float(a);
-    f[1] = __high2float(a);
-    f[2] = __low2float(b);
-    f[3] = __high2float(b);
+// named barrier over the 128 threads of one producer team (ids 1, 2)
+__device__ __forceinline__ void team_sync(int team) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(team + 1), "n"(kTeamThreads) : "memory");
 }
+// team barrier that also returns the AND of every thread's flag
+__device__ __forceinline__ bool team_sync_and(int team, bool flag) {
+    unsigned r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n"
+        " setp.ne.u32 p, %1, 0;\n"
+        " bar.red.and.pred q, %2, %3, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((unsigned)flag), "r"(team + 1), "n"(kTeamThreads)
+        : "memory");
+    return r != 0;
+}
+// packed fp32 pair multiply (one instruction on sm_100 and later)
+__device__ __forceinline__ void mul2(float& a, float& b, float2 s) {
+    unsigned long long x, y, z;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(s.x), "f"(s.y));
+    asm("mul.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(y));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(z));
+}
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t raw) {
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&raw);
+    return __bfloat1622float2(v);
+}
+__device__ __forceinline__ float tf32_round(float x) { return __uint_as_float(to_tf32(x)); }
 
 struct Unit {
     int n, h, tok_start, L, nch;
 };
 
-// ---- token-parallel stage for one chunk (one warp) -------------------------------
-__device__ __forceinline__ bool produce_chunk(const Problem& P, const Unit& U, int c,
-                                              ProdSmem& S, Stage& st,
-                                              unsigned long long* empty_bar, int lane,
-                                              float expA, const float (&dtb)[4], int* err) {
-    const int h = U.h;
+// Issue the copies of chunk c's rows into one raw buffer (rows past the end are zeroed).
+__device__ __forceinline__ void load_chunk(const Problem& P, const Unit& U, int c, RawChunk& R,
+                                           int tt) {
     const int tok0 = U.tok_start + c * kChunk;
     const int len = min(kChunk, U.L - c * kChunk);
-    for (int i = lane; i < kChunk * 16; i += 32) {
+    for (int i = tt; i < kChunk * 16; i += kTeamThreads) {
         const int r = i >> 4, p = i & 15;
         const int so = r * RAW_LD + p * 8;
         if (r < len) {
-            const size_t go = ((size_t)(tok0 + r) * P.H + h) * kDim + p * 8;
-            cp_async16(&S.q[so], P.q + go);
-            cp_async16(&S.k[so], P.k + go);
-            cp_async16(&S.v[so], P.v + go);
-            cp_async16(&S.g[so], P.g + go);
+            const size_t go = ((size_t)(tok0 + r) * P.H + U.h) * kDim + p * 8;
+            cp_async16(&R.q[so], P.q + go);
+            cp_async16(&R.k[so], P.k + go);
+            cp_async16(&R.v[so], P.v + go);
+            cp_async16(&R.g[so], P.g + go);
         } else {
             const uint4 z = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(&S.q[so]) = z;
-            *reinterpret_cast<uint4*>(&S.k[so]) = z;
-            *reinterpret_cast<uint4*>(&S.v[so]) = z;
-            *reinterpret_cast<uint4*>(&S.g[so]) = z;
+            *reinterpret_cast<uint4*>(&R.q[so]) = z;
+            *reinterpret_cast<uint4*>(&R.k[so]) = z;
+            *reinterpret_cast<uint4*>(&R.v[so]) = z;
+            *reinterpret_cast<uint4*>(&R.g[so]) = z;
         }
     }
-    cp_async_commit();
-    if (lane < kChunk) {
-        float b = 0.0f;
-        if (lane < len) b = sigmoid_fast(__bfloat162float(P.beta[(size_t)(tok0 + lane) * P.H + h]));
-        S.beta[lane] = b;
-    }
-    const int c0 = 4 * lane;
-    const float lb2 = P.lower_bound * kLog2e;
-    cp_async_wait<0>();
-    __syncwarp();
-
-    // gates -> cumulative base-2 log-decay; K * 2^G later overwrites the raw g rows
-    {
-        float run[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int r = 0; r < kChunk; ++r) {
-            float gv[4];
-            unpack4(*reinterpret_cast<const uint2*>(&S.g[r * RAW_LD + c0]), gv);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float g2 = lb2 * sigmoid_fast(expA * (gv[i] + dtb[i]));
-                run[i] += (r < len) ? g2 : 0.0f;
-            }
-            *reinterpret_cast<float4*>(&S.G[r * G_LD + c0]) =
-                make_float4(run[0], run[1], run[2], run[3]);
-        }
-    }
-    __syncwarp();
-
-    // decay-ratio products A_kk, A_qk (tf32 MMA over the 128 key channels)
-    const int fg = lane >> 2, ft = lane & 3;
-    float akk[2][4] = {}, aqk[2][4] = {};
-#pragma unroll 4
-    for (int kk = 0; kk < kDim / 8; ++kk) {
-        const int cl = kk * 8 + ft, ch = cl + 4;
-        const float G00 = S.G[fg * G_LD + cl], G01 = S.G[fg * G_LD + ch];
-        const float G10 = S.G[(fg + 8) * G_LD + cl], G11 = S.G[(fg + 8) * G_LD + ch];
-        const float k00 = __bfloat162float(S.k[fg * RAW_LD + cl]);
-        const float k01 = __bfloat162float(S.k[fg * RAW_LD + ch]);
-        const float k10 = __bfloat162float(S.k[(fg + 8) * RAW_LD + cl]);
-        const float k11 = __bfloat162float(S.k[(fg + 8) * RAW_LD + ch]);
-        const float q00 = __bfloat162float(S.q[fg * RAW_LD + cl]);
-        const float q01 = __bfloat162float(S.q[fg * RAW_LD + ch]);
-        const float q10 = __bfloat162float(S.q[(fg + 8) * RAW_LD + cl]);
-        const float q11 = __bfloat162float(S.q[(fg + 8) * RAW_LD + ch]);
-        const float e00 = ex2_approx(G00), e01 = ex2_approx(G01);
-        const float e10 = ex2_approx(G10), e11 = ex2_approx(G11);
-        const float i00 = ex2_approx(-G00), i01 = ex2_approx(-G01);
-        const float i10 = ex2_approx(-G10), i11 = ex2_approx(-G11);
-        const uint32_t ak[4] = {to_tf32(k00 * e00), to_tf32(k10 * e10), to_tf32(k01 * e01),
-                                to_tf32(k11 * e11)};
-        const uint32_t aq[4] = {to_tf32(q00 * e00), to_tf32(q10 * e10), to_tf32(q01 * e01),
-                                to_tf32(q11 * e11)};
-        const uint32_t b00 = to_tf32(k00 * i00), b01 = to_tf32(k01 * i01);
-        const uint32_t b10 = to_tf32(k10 * i10), b11 = to_tf32(k11 * i11);
-        mma_tf32(akk[0], ak, b00, b01);
-        mma_tf32(akk[1], ak, b10, b11);
-        mma_tf32(aqk[0], aq, b00, b01);
-        mma_tf32(aqk[1], aq, b10, b11);
-    }
-
-    // the slot must be free before anything is written into it
-    const int k = c / kRing;
-    if (k >= 1 && !mbar_wait(empty_bar, (unsigned)((k - 1) & 1), err)) return false;
-
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int hi = 0; hi < 2; ++hi) {
-            const int r = fg + 8 * hi;
-            const int s = 8 * nt + 2 * ft;
-            const float br = S.beta[r];
-            S.A[r * A_LD + s] = (s < r) ? br * akk[nt][2 * hi] : 0.0f;
-            S.A[r * A_LD + s + 1] = (s + 1 < r) ? br * akk[nt][2 * hi + 1] : 0.0f;
-            const float x0 = (s <= r) ? aqk[nt][2 * hi] : 0.0f;
-            const float x1 = (s + 1 <= r) ? aqk[nt][2 * hi + 1] : 0.0f;
-            *reinterpret_cast<uint32_t*>(&st.aqk[r * AQ_LD + s]) = pack_half2(x0, x1);
-        }
-    __syncwarp();
-
-    // T = (I + A_kk)^-1 by forward substitution, one column per lane; T diag(b) in fp16
-    if (lane < kChunk) {
-        float Tc[kChunk];
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            float s = 0.0f;
-#pragma unroll
-            for (int m = 0; m < i; ++m) s = fmaf(S.A[i * A_LD + m], Tc[m], s);
-            Tc[i] = (i == lane) ? 1.0f : ((i < lane) ? 0.0f : -s);
-        }
-        const float bj = S.beta[lane];
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) S.tb[i * TB_LD + lane] = __float2half_rn(Tc[i] * bj);
-    }
-
-    // fp16 operands (column-owner layout): Q 2^G, K 2^(G_last - G) into the slot;
-    // K 2^G and V in place of the raw g and v rows
-    __half* kg16 = reinterpret_cast<__half*>(S.g);
-    __half* v16 = reinterpret_cast<__half*>(S.v);
-    {
-        const float4 gl4 = *reinterpret_cast<const float4*>(&S.G[(kChunk - 1) * G_LD + c0]);
-        const float gl[4] = {gl4.x, gl4.y, gl4.z, gl4.w};
-#pragma unroll 4
-        for (int r = 0; r < kChunk; ++r) {
-            const float4 G4 = *reinterpret_cast<const float4*>(&S.G[r * G_LD + c0]);
-            const float Gr[4] = {G4.x, G4.y, G4.z, G4.w};
-            float kv[4], qv[4], vv[4];
-            unpack4(*reinterpret_cast<const uint2*>(&S.k[r * RAW_LD + c0]), kv);
-            unpack4(*reinterpret_cast<const uint2*>(&S.q[r * RAW_LD + c0]), qv);
-            unpack4(*reinterpret_cast<const uint2*>(&S.v[r * RAW_LD + c0]), vv);
-            float e[4], d[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                e[i] = ex2_approx(Gr[i]);
-                d[i] = ex2_approx(gl[i] - Gr[i]);
-            }
-            *reinterpret_cast<uint2*>(&st.qg[r * LD + c0]) = make_uint2(
-                pack_half2(qv[0] * e[0], qv[1] * e[1]), pack_half2(qv[2] * e[2], qv[3] * e[3]));
-            *reinterpret_cast<uint2*>(&st.kd[r * LD + c0]) = make_uint2(
-                pack_half2(kv[0] * d[0], kv[1] * d[1]), pack_half2(kv[2] * d[2], kv[3] * d[3]));
-            *reinterpret_cast<uint2*>(&kg16[r * RAW_LD + c0]) = make_uint2(
-                pack_half2(kv[0] * e[0], kv[1] * e[1]), pack_half2(kv[2] * e[2], kv[3] * e[3]));
-            *reinterpret_cast<uint2*>(&v16[r * RAW_LD + c0]) =
-                make_uint2(pack_half2(vv[0], vv[1]), pack_half2(vv[2], vv[3]));
-        }
-        *reinterpret_cast<float4*>(&st.gc[c0]) =
-            make_float4(ex2_approx(gl[0]), ex2_approx(gl[1]), ex2_approx(gl[2]), ex2_approx(gl[3]));
-    }
-    __syncwarp();
-
-    // u = T diag(b) V and w = T diag(b) (K 2^G) (stored negated), fp16 MMA, N = 128
-    {
-        uint32_t ta[4];
-        ldsm_x4(ta, &S.tb[((lane & 7) + 8 * ((lane >> 3) & 1)) * TB_LD + 8 * (lane >> 4)]);
-        const int brow = (lane & 7) + 8 * ((lane >> 3) & 1);
-#pragma unroll 2
-        for (int np = 0; np < kDim / 16; ++np) {
-            const int bcol = 16 * np + 8 * (lane >> 4);
-            uint32_t bv[4], bk[4];
-            ldsm_x4_t(bv, &v16[brow * RAW_LD + bcol]);
-            ldsm_x4_t(bk, &kg16[brow * RAW_LD + bcol]);
-            float cu0[4] = {}, cu1[4] = {}, cw0[4] = {}, cw1[4] = {};
-            mma_f16(cu0, ta, bv[0], bv[1]);
-            mma_f16(cu1, ta, bv[2], bv[3]);
-            mma_f16(cw0, ta, bk[0], bk[1]);
-            mma_f16(cw1, ta, bk[2], bk[3]);
-            const int col0 = 16 * np + 2 * ft, col1 = col0 + 8;
-            *reinterpret_cast<uint32_t*>(&st.u[fg * LD + col0]) = pack_half2(cu0[0], cu0[1]);
-            *reinterpret_cast<uint32_t*>(&st.u[(fg + 8) * LD + col0]) = pack_half2(cu0[2], cu0[3]);
-            *reinterpret_cast<uint32_t*>(&st.u[fg * LD + col1]) = pack_half2(cu1[0], cu1[1]);
-            *reinterpret_cast<uint32_t*>(&st.u[(fg + 8) * LD + col1]) = pack_half2(cu1[2], cu1[3]);
-            *reinterpret_cast<uint32_t*>(&st.w[fg * LD + col0]) = pack_half2(-cw0[0], -cw0[1]);
-            *reinterpret_cast<uint32_t*>(&st.w[(fg + 8) * LD + col0]) = pack_half2(-cw0[2], -cw0[3]);
-            *reinterpret_cast<uint32_t*>(&st.w[fg * LD + col1]) = pack_half2(-cw1[0], -cw1[1]);
-            *reinterpret_cast<uint32_t*>(&st.w[(fg + 8) * LD + col1]) = pack_half2(-cw1[2], -cw1[3]);
-        }
-    }
-    __syncwarp();
-    return true;
 }
 
-// ---- sequential stage ------------------------------------------------------------
-__device__ __forceinline__ void chain(const Problem& P, const Unit& U, Smem& S, int warp,
-                                      int lane, int* err) {
+// ---- token-parallel stage: one producer team, all its chunks ----------------------
+__device__ void produce(const Problem& P, const Unit& U, Smem& S, int team, int tt, int* err) {
+    TeamSmem& T = S.team[team];
+    const int warp = tt >> 5, lane = tt & 31;
     const int fg = lane >> 2, ft = lane & 3;
-    const int vw = warp * 16;
-    const size_t state_base = ((size_t)U.n * P.H + U.h) * kDim * kDim;
+    // gate-pass ownership: channel pair (2j, 2j+1), rows 8 half .. 8 half + 7
+    const int j = warp * 16 + (lane & 15);
+    const int half = lane >> 4;
+    const int c2 = 2 * j;
+    const int r0 = 8 * half;
+    const float expA = expf(P.A_log[U.h]);
+    // sigmoid argument in base 2: -(exp(A_log) (g + dt_bias)) log2 e = g ga + gb
+    const float ga = -expA * kLog2e;
+    const float gb0 = ga * P.dt_bias[(size_t)U.h * kDim + c2];
+    const float gb1 = ga * P.dt_bias[(size_t)U.h * kDim + c2 + 1];
+    const float lb2 = P.lower_bound * kLog2e;
+    const size_t beta_base = (size_t)U.tok_start * P.H + U.h;
 
-    // Sacc[nt][i] = S[c][v], v = vw + g + 8 (i >> 1), c = 8 nt + 2 t + (i & 1)
-    float Sacc[16][4];
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int v = vw + fg + 8 * (i >> 1);
-            const int c = 8 * nt + 2 * ft + (i & 1);
-            float x = 0.0f;
-            if (P.init_state) {
-                const size_t idx = state_base + (size_t)c * kDim + v;
-                x = (P.init_dtype == KDA_F32)
-                        ? static_cast<const float*>(P.init_state)[idx]
-                        : __bfloat162float(static_cast<const __nv_bfloat16*>(P.init_state)[idx]);
-            }
-            Sacc[nt][i] = x;
+    int c = team;
+    if (c >= U.nch) return;
+    load_chunk(P, U, c, T.raw[0], tt);
+    cp_async_commit();
+    float blogit = 0.0f;
+    if (tt < kChunk && c * kChunk + tt < U.L)
+        blogit = __bfloat162float(P.beta[beta_base + (size_t)(c * kChunk + tt) * P.H]);
+
+    for (int it = 0; c < U.nch; c += kTeams, ++it) {
+        RawChunk& R = T.raw[it & 1];
+        const int len = min(kChunk, U.L - c * kChunk);
+        if (tt < kChunk) T.beta[tt] = (tt < len) ? sigmoid_fast(blogit) : 0.0f;
+        cp_async_wait<0>();  // this chunk's rows (issued one iteration earlier)
+        // the chunk's slot must be free before anything is written into it; the
+        // team votes so that a timed-out wait ends the whole team together
+        const int slot = c % kRing;
+        const int k = c / kRing;
+        bool ok = true;
+        if (k >= 1) ok = mbar_wait(&S.empty[slot], (unsigned)((k - 1) & 1), err);
+        if (!team_sync_and(team, ok)) return;
+        Stage& st = S.st[slot];
+        // every thread of the team is past the previous chunk: prefetch the team's
+        // next chunk into the other buffer
+        const int cn = c + kTeams;
+        if (cn < U.nch) {
+            load_chunk(P, U, cn, T.raw[(it + 1) & 1], tt);
+            if (tt < kChunk && cn * kChunk + tt < U.L)
+                blogit = __bfloat162float(P.beta[beta_base + (size_t)(cn * kChunk + tt) * P.H]);
         }
+        cp_async_commit();
 
-    const int brow_n = (lane & 7) + 8 * (lane >> 4);
-    const int bcol_n = 8 * ((lane >> 3) & 1);
-    const int brow_t = (lane & 7) + 8 * ((lane >> 3) & 1);
-    const int bcol_t = 8 * (lane >> 4);
-    __nv_bfloat16* os = S.ostage[warp];
+        // ---- gate pass: base-2 log-decay, cumulative over the chunk -------------
+        float G0[8], G1[8];
+        {
+            float run0 = 0.f, run1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = r0 + i;
+                const float2 gv = bf2_to_f2(*reinterpret_cast<const uint32_t*>(&R.g[r * RAW_LD + c2]));
+                const float s0 = rcp_approx(1.0f + ex2_approx(fmaf(gv.x, ga, gb0)));
+                const float s1 = rcp_approx(1.0f + ex2_approx(fmaf(gv.y, ga, gb1)));
+                if (r < len) {
+                    run0 = fmaf(lb2, s0, run0);
+                    run1 = fmaf(lb2, s1, run1);
+                }
+                G0[i] = run0;
+                G1[i] = run1;
+            }
+            // rows 8..15 continue from the total of rows 0..7 (held by lane ^ 16)
+            const float t0 = __shfl_xor_sync(0xffffffffu, run0, 16);
+            const float t1 = __shfl_xor_sync(0xffffffffu, run1, 16);
+            if (half) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    G0[i] += t0;
+                    G1[i] += t1;
+                }
+            }
+        }
+        const float gl0 = __shfl_sync(0xffffffffu, G0[7], lane | 16);
+        const float gl1 = __shfl_sync(0xffffffffu, G1[7], lane | 16);
+        const float gc0 = ex2_approx(gl0), gc1 = ex2_approx(gl1);
+        if (half == 0) *reinterpret_cast<float2*>(&st.gc[c2]) = make_float2(gc0, gc1);
+        __half* kg16 = reinterpret_cast<__half*>(R.g);
+        unsigned char* buo = reinterpret_cast<unsigned char*>(st.buo);
+        unsigned char* kdt = reinterpret_cast<unsigned char*>(st.kdt);
+        unsigned char* vt = reinterpret_cast<unsigned char*>(st.vt);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = r0 + i;
+            const float e0 = ex2_approx(G0[i]), e1 = ex2_approx(G1[i]);
+            const float d0 = ex2_approx(-G0[i]), d1 = ex2_approx(-G1[i]);
+            const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t*>(&R.k[r * RAW_LD + c2]));
+            const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t*>(&R.q[r * RAW_LD + c2]));
+            const float2 vv = bf2_to_f2(*reinterpret_cast<const uint32_t*>(&R.v[r * RAW_LD + c2]));
+            const float kg0 = kv.x * e0, kg1 = kv.y * e1;
+            const float ki0 = kv.x * d0, ki1 = kv.y * d1;
+            const float qg0 = qv.x * e0, qg1 = qv.y * e1;
+            *reinterpret_cast<float2*>(&T.kg32[r * F_LD + c2]) =
+                make_float2(tf32_round(kg0), tf32_round(kg1));
+            *reinterpret_cast<float2*>(&T.ki32[r * F_LD + c2]) =
+                make_float2(tf32_round(ki0), tf32_round(ki1));
+            *reinterpret_cast<float2*>(&T.qg32[r * F_LD + c2]) =
+                make_float2(tf32_round(qg0), tf32_round(qg1));
+            *reinterpret_cast<uint32_t*>(&kg16[r * RAW_LD + c2]) = pack_half2(kg0, kg1);
+            // Q 2^G: rows 16..31 of the [-w; Q 2^G] operand (K-major, 128B swizzle)
+            *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(16 + r, c2, 32)) =
+                pack_half2(qg0, qg1);
+            // transposed tiles: (K 2^(G_last - G))^T and V^T, row = channel, K = token
+            *reinterpret_cast<__half*>(kdt + tc::interleaved_offset(c2, r, kChunk)) =
+                __float2half_rn(ki0 * gc0);
+            *reinterpret_cast<__half*>(kdt + tc::interleaved_offset(c2 + 1, r, kChunk)) =
+                __float2half_rn(ki1 * gc1);
+            *reinterpret_cast<__half*>(vt + tc::interleaved_offset(c2, r, kChunk)) =
+                __float2half_rn(vv.x);
+            *reinterpret_cast<__half*>(vt + tc::interleaved_offset(c2 + 1, r, kChunk)) =
+                __float2half_rn(vv.y);
+        }
+        team_sync(team);
 
+        // ---- decay-ratio products, tf32 MMA: warp w covers key channels 32w .. 32w+31
+        {
+            float pk[2][4] = {}, pq[2][4] = {};
+            const int arow = (lane & 7) + 8 * ((lane >> 3) & 1);
+            const int acol = 4 * (lane >> 4);
+            const int brow = (lane & 7) + 8 * (lane >> 4);
+            const int bcol = 4 * ((lane >> 3) & 1);
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {
+                const int kc = 32 * warp + 8 * kq;
+                uint32_t ak[4], aq[4], b[4];
+                ldsm_x4(ak, &T.kg32[arow * F_LD + kc + acol]);
+                ldsm_x4(aq, &T.qg32[arow * F_LD + kc + acol]);
+                ldsm_x4(b, &T.ki32[brow * F_LD + kc + bcol]);
+                mma_tf32(pk[0], ak, b[0], b[1]);
+                mma_tf32(pk[1], ak, b[2], b[3]);
+                mma_tf32(pq[0], aq, b[0], b[1]);
+                mma_tf32(pq[1], aq, b[2], b[3]);
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hi = 0; hi < 2; ++hi) {
+                    const int r = fg + 8 * hi, s = 8 * nt + 2 * ft;
+                    *reinterpret_cast<float2*>(&T.part[warp][0][r * kChunk + s]) =
+                        make_float2(pk[nt][2 * hi], pk[nt][2 * hi + 1]);
+                    *reinterpret_cast<float2*>(&T.part[warp][1][r * kChunk + s]) =
+                        make_float2(pq[nt][2 * hi], pq[nt][2 * hi + 1]);
+                }
+        }
+        team_sync(team);
+
+        if (warp == 0) {
+            // A_kk = diag(b) (sum of partials), strictly lower; then T = (I + A_kk)^-1
+#pragma unroll
+            for (int e = lane; e < kChunk * kChunk; e += 32) {
+                const int r = e >> 4, s = e & 15;
+                const float x = T.part[0][0][e] + T.part[1][0][e] + T.part[2][0][e] + T.part[3][0][e];
+                T.A[r * A_LD + s] = (s < r) ? T.beta[r] * x : 0.0f;
+            }
+            __syncwarp();
+            if (lane < kChunk) {
+                float Tc[kChunk];
+#pragma unroll
+                for (int i = 0; i < kChunk; ++i) {
+                    float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+                    for (int m = 0; m + 1 < i; m += 2) {
+                        s0 = fmaf(T.A[i * A_LD + m], Tc[m], s0);
+                        s1 = fmaf(T.A[i * A_LD + m + 1], Tc[m + 1], s1);
+                    }
+                    if (i & 1) s0 = fmaf(T.A[i * A_LD + i - 1], Tc[i - 1], s0);
+                    Tc[i] = (i == lane) ? 1.0f : ((i < lane) ? 0.0f : -(s0 + s1));
+                }
+                const float bj = T.beta[lane];
+                unsigned char* tbt = reinterpret_cast<unsigned char*>(st.tbt);
+#pragma unroll
+                for (int i = 0; i < kChunk; ++i) {
+                    const __half x = __float2half_rn(Tc[i] * bj);
+                    T.tb[i * TB_LD + lane] = x;
+                    *reinterpret_cast<__half*>(tbt + tc::interleaved_offset(i, lane, kChunk)) = x;
+                }
+            }
+        } else if (warp == 1) {
+            // A_qk = sum of partials, inclusive lower, fp16 into the slot
+#pragma unroll
+            for (int e = 2 * lane; e < kChunk * kChunk; e += 64) {
+                const int r = e >> 4, s = e & 15;
+                float x0 = T.part[0][1][e] + T.part[1][1][e] + T.part[2][1][e] + T.part[3][1][e];
+                float x1 = T.part[0][1][e + 1] + T.part[1][1][e + 1] + T.part[2][1][e + 1] +
+                           T.part[3][1][e + 1];
+                x0 = (s <= r) ? x0 : 0.0f;
+                x1 = (s + 1 <= r) ? x1 : 0.0f;
+                *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(st.aqk) +
+                                             tc::interleaved_offset(r, s, kChunk)) =
+                    pack_half2(x0, x1);
+            }
+        }
+        team_sync(team);
+
+        // ---- w = T diag(b)(K 2^G), stored negated as rows 0..15 of [-w; Q 2^G]:
+        //      warp w covers key channels 32w .. 32w+31
+        {
+            uint32_t ta[4];
+            ldsm_x4(ta, &T.tb[((lane & 7) + 8 * ((lane >> 3) & 1)) * TB_LD + 8 * (lane >> 4)]);
+            const int brow = (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                const int np = 2 * warp + q2;
+                const int bcol = 16 * np + 8 * (lane >> 4);
+                uint32_t bk[4];
+                ldsm_x4_t(bk, &kg16[brow * RAW_LD + bcol]);
+                float cw0[4] = {}, cw1[4] = {};
+                mma_f16(cw0, ta, bk[0], bk[1]);
+                mma_f16(cw1, ta, bk[2], bk[3]);
+                const int col0 = 16 * np + 2 * ft, col1 = col0 + 8;
+                *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(fg, col0, 32)) =
+                    pack_half2(-cw0[0], -cw0[1]);
+                *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(fg + 8, col0, 32)) =
+                    pack_half2(-cw0[2], -cw0[3]);
+                *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(fg, col1, 32)) =
+                    pack_half2(-cw1[0], -cw1[1]);
+                *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(fg + 8, col1, 32)) =
+                    pack_half2(-cw1[2], -cw1[3]);
+            }
+        }
+        // generic-proxy writes of this thread -> visible to the tensor core
+        tc::fence_proxy_async_smem();
+        // every thread publishes its own writes to the slot
+        mbar_arrive(&S.full[slot]);
+    }
+}
+
+// ---- sequential stage: tensor-core issue (one thread) -------------------------------
+// Per chunk c (slot s), in the transposed orientation (TMEM lane = value row v):
+//   [U|O] = V^T [T diag(b) ; 0]^T             (u^T into the U half, zeros into O)
+//   [U|O] += S^T [-w ; Q 2^G]^T               (8 MMAs over the 128 key channels)
+//   S^T  += U^T (K 2^(G_last-G))              (S^T was rescaled by 2^G_last beforehand)
+//   O    += U^T A_qk^T
+__device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
+    constexpr uint32_t id32 = tc::idesc_f16_f32(128, 32);
+    constexpr uint32_t id16 = tc::idesc_f16_f32(128, 16);
+    constexpr uint32_t id128 = tc::idesc_f16_f32(128, 128);
     for (int c = 0; c < U.nch; ++c) {
         const int slot = c % kRing;
-        if (!mbar_wait(&S.full[slot], (unsigned)((c / kRing) & 1), err)) return;
         const Stage& st = S.st[slot];
-
-        uint32_t sa[8][4];
+        const uint32_t uo = tmem + TM_UO + 32u * (c & 1);
+        if (!mbar_wait(&S.full[slot], (unsigned)((c / kRing) & 1), err)) return;
+        if (!mbar_wait(&S.s16_ready, (unsigned)(c & 1), err)) return;
+        tc::fence_after_sync();
+        tc::mma_ss(uo, tc::smem_desc(smem_u32(st.vt), 128, 256, tc::kSwizzleNone),
+                   tc::smem_desc(smem_u32(st.tbt), 128, 256, tc::kSwizzleNone), id32, 0);
+        const uint32_t buo = smem_u32(st.buo);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            sa[kk][0] = pack_half2(Sacc[2 * kk][0], Sacc[2 * kk][1]);
-            sa[kk][1] = pack_half2(Sacc[2 * kk][2], Sacc[2 * kk][3]);
-            sa[kk][2] = pack_half2(Sacc[2 * kk + 1][0], Sacc[2 * kk + 1][1]);
-            sa[kk][3] = pack_half2(Sacc[2 * kk + 1][2], Sacc[2 * kk + 1][3]);
+            const uint32_t b = buo + (kk >> 2) * (32 * 128) + (kk & 3) * 32;
+            tc::mma_ts(uo, tmem + TM_S16 + 8 * kk, tc::smem_desc(b, 16, 1024, tc::kSwizzle128B),
+                       id32, 1);
         }
-        float Uacc[2][4], Oacc[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = 8 * nt + 2 * ft + (i & 1);
-                const int v = vw + fg + 8 * (i >> 1);
-                Uacc[nt][i] = __half2float(st.u[t * LD + v]);
-                Oacc[nt][i] = 0.0f;
-            }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            uint32_t bw[4], bq[4];
-            ldsm_x4(bw, &st.w[brow_n * LD + 16 * kk + bcol_n]);
-            ldsm_x4(bq, &st.qg[brow_n * LD + 16 * kk + bcol_n]);
-            mma_f16(Uacc[0], sa[kk], bw[0], bw[1]);
-            mma_f16(Uacc[1], sa[kk], bw[2], bw[3]);
-            mma_f16(Oacc[0], sa[kk], bq[0], bq[1]);
-            mma_f16(Oacc[1], sa[kk], bq[2], bq[3]);
-        }
-        const uint32_t ua[4] = {pack_half2(Uacc[0][0], Uacc[0][1]),
-                                pack_half2(Uacc[0][2], Uacc[0][3]),
-                                pack_half2(Uacc[1][0], Uacc[1][1]),
-                                pack_half2(Uacc[1][2], Uacc[1][3])};
-        {
-            uint32_t ba[4];
-            ldsm_x4(ba, &st.aqk[brow_n * AQ_LD + bcol_n]);
-            mma_f16(Oacc[0], ua, ba[0], ba[1]);
-            mma_f16(Oacc[1], ua, ba[2], ba[3]);
-        }
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            const float2 gc2 = *reinterpret_cast<const float2*>(&st.gc[8 * nt + 2 * ft]);
-            Sacc[nt][0] *= gc2.x;
-            Sacc[nt][1] *= gc2.y;
-            Sacc[nt][2] *= gc2.x;
-            Sacc[nt][3] *= gc2.y;
-        }
-#pragma unroll
-        for (int np = 0; np < 8; ++np) {
-            uint32_t bk[4];
-            ldsm_x4_t(bk, &st.kd[brow_t * LD + 16 * np + bcol_t]);
-            mma_f16(Sacc[2 * np], ua, bk[0], bk[1]);
-            mma_f16(Sacc[2 * np + 1], ua, bk[2], bk[3]);
-        }
-        // the slot's factors are all read: hand it back to its producer
-        mbar_arrive(&S.empty[slot]);
-
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = 8 * nt + 2 * ft + (i & 1);
-                const int v = fg + 8 * (i >> 1);
-                os[t * O_LD + v] = __float2bfloat16_rn(P.scale * Oacc[nt][i]);
-            }
-        __syncwarp();
-        {
-            const int r = lane >> 1, half = lane & 1;
-            const int tl = c * kChunk + r;
-            if (tl < U.L) {
-                const size_t o = ((size_t)(U.tok_start + tl) * P.H + U.h) * kDim + vw + 8 * half;
-                *reinterpret_cast<uint4*>(P.out + o) =
-                    *reinterpret_cast<const uint4*>(&os[r * O_LD + 8 * half]);
-            }
-        }
-        __syncwarp();
+        tc::commit(smem_u32(&S.uo_done));
+        if (!mbar_wait(&S.u16_ready, (unsigned)(c & 1), err)) return;
+        tc::fence_after_sync();
+        tc::mma_ts(tmem + TM_S32, tmem + TM_U16,
+                   tc::smem_desc(smem_u32(st.kdt), 128, 256, tc::kSwizzleNone), id128, 1);
+        tc::mma_ts(uo + 16, tmem + TM_U16,
+                   tc::smem_desc(smem_u32(st.aqk), 128, 256, tc::kSwizzleNone), id16, 1);
+        tc::commit(smem_u32(&S.s_done));
+        tc::commit(smem_u32(&S.empty[slot]));
     }
+}
 
-    if (P.final_state) {
+__device__ __forceinline__ float state_in(const Problem& P, size_t idx) {
+    return (P.init_dtype == KDA_F32)
+               ? static_cast<const float*>(P.init_state)[idx]
+               : __bfloat162float(static_cast<const __nv_bfloat16*>(P.init_state)[idx]);
+}
+__device__ __forceinline__ void state_out(const Problem& P, size_t idx, float x) {
+    if (P.final_dtype == KDA_F32)
+        static_cast<float*>(P.final_state)[idx] = x;
+    else
+        static_cast<__nv_bfloat16*>(P.final_state)[idx] = __float2bfloat16_rn(x);
+}
+
+// ---- sequential stage: epilogue (thread v owns TMEM lane v = value channel v) --------
+// Keeps the fp32 state S^T in tensor memory: after each state update it writes
+// the fp16 copy that the next chunk's MMAs read and pre-scales the fp32 state
+// by the next chunk's 2^G_last; converts U^T to fp16 for the update MMA; and
+// writes the chunk's outputs.
+__device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem, int ew,
+                         int lane, int* err) {
+    const int v = 32 * ew + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * ew) << 16);   // this warp's lane quarter
+    const size_t sbase = ((size_t)U.n * P.H + U.h) * kDim * kDim + v;   // + c * kDim
+    bool ok = true;
+
+    if (U.nch == 0) {   // no tokens: the final state is the initial state
+        if (P.final_state)
+            for (int c = 0; c < kDim; ++c)
+                state_out(P, sbase + (size_t)c * kDim, P.init_state ? state_in(P, sbase + (size_t)c * kDim) : 0.0f);
+        return;
+    }
+    // initial state: S16 = fp16(S0), S32 = S0 Diag(2^G_last of chunk 0)
+    ok = mbar_wait(&S.full[0], 0u, err);
+    if (!__all_sync(0xffffffffu, ok)) return;
+#pragma unroll 1
+    for (int piece = 0; piece < 4; ++piece) {
+        uint32_t x[32], h[16];
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt)
+        for (int i = 0; i < 32; ++i) {
+            const int c = 32 * piece + i;
+            x[i] = __float_as_uint(P.init_state ? state_in(P, sbase + (size_t)c * kDim) : 0.0f);
+        }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int v = vw + fg + 8 * (i >> 1);
-                const int c = 8 * nt + 2 * ft + (i & 1);
-                const size_t idx = state_base + (size_t)c * kDim + v;
-                if (P.final_dtype == KDA_F32)
-                    static_cast<float*>(P.final_state)[idx] = Sacc[nt][i];
-                else
-                    static_cast<__nv_bfloat16*>(P.final_state)[idx] =
-                        __float2bfloat16_rn(Sacc[nt][i]);
+        for (int i = 0; i < 16; ++i)
+            h[i] = pack_half2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+        const float* gc = S.st[0].gc + 32 * piece;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * gc[i]);
+        tc::st16(tl + TM_S16 + 16 * piece, h);
+        tc::st32(tl + TM_S32 + 32 * piece, x);
+    }
+    tc::wait_st();
+    tc::fence_before_sync();
+    mbar_arrive(&S.s16_ready);
+
+    for (int c = 0; c < U.nch; ++c) {
+        const uint32_t uo = tl + TM_UO + 32u * (c & 1);
+        // U^T -> fp16 A operand of the update
+        ok = mbar_wait(&S.uo_done, (unsigned)(c & 1), err);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc::fence_after_sync();
+        {
+            uint32_t u[16], h[8];
+            tc::ld16(uo, u);
+            tc::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                h[i] = pack_half2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+            tc::st8(tl + TM_U16, h);
+            tc::wait_st();
+        }
+        tc::fence_before_sync();
+        mbar_arrive(&S.u16_ready);
+
+        // state update done: fp16 copy + rescale for the next chunk (or the final state)
+        ok = mbar_wait(&S.s_done, (unsigned)(c & 1), err);
+        const bool more = c + 1 < U.nch;
+        const int nslot = (c + 1) % kRing;
+        if (more) ok = ok && mbar_wait(&S.full[nslot], (unsigned)(((c + 1) / kRing) & 1), err);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc::fence_after_sync();
+#pragma unroll 1
+        for (int piece = 0; piece < 4; ++piece) {
+            uint32_t x[32];
+            tc::ld32(tl + TM_S32 + 32 * piece, x);
+            tc::wait_ld();
+            if (more) {
+                uint32_t h[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    h[i] = pack_half2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+                tc::st16(tl + TM_S16 + 16 * piece, h);
+                const float* gc = S.st[nslot].gc + 32 * piece;
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float a = __uint_as_float(x[i]), b = __uint_as_float(x[i + 1]);
+                    mul2(a, b, make_float2(gc[i], gc[i + 1]));
+                    x[i] = __float_as_uint(a);
+                    x[i + 1] = __float_as_uint(b);
+                }
+                tc::st32(tl + TM_S32 + 32 * piece, x);
+            } else if (P.final_state) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    state_out(P, sbase + (size_t)(32 * piece + i) * kDim, __uint_as_float(x[i]));
             }
+        }
+        if (more) {
+            tc::wait_st();
+            tc::fence_before_sync();
+            mbar_arrive(&S.s16_ready);
+        }
+        // outputs of chunk c: O^T lane v, column t
+        {
+            uint32_t o[16];
+            tc::ld16(uo + 16, o);
+            tc::wait_ld();
+            const int len = min(kChunk, U.L - c * kChunk);
+            __nv_bfloat16* out = P.out + ((size_t)(U.tok_start + c * kChunk) * P.H + U.h) * kDim + v;
+#pragma unroll
+            for (int t = 0; t < kChunk; ++t)
+                if (t < len) out[(size_t)t * P.H * kDim] = __float2bfloat16_rn(P.scale * __uint_as_float(o[t]));
+        }
     }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Problem P, SeqMap M, int* err) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // the 128-byte swizzle acts on absolute shared addresses: align the stages to 1024 B
+    unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    Smem& S = *reinterpret_cast<Smem*>(base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     Unit U;
@@ -453,25 +602,47 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Problem P, SeqMap M,
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRing; ++s) {
-            mbar_init(&S.full[s], 32);                 // all lanes of the producer warp
-            mbar_init(&S.empty[s], kChainWarps * 32);  // every chain thread
+            mbar_init(&S.full[s], kTeamThreads);   // every thread of the producing team
+            mbar_init(&S.empty[s], 1);             // one tensor-core commit
         }
+        mbar_init(&S.uo_done, 1);
+        mbar_init(&S.s_done, 1);
+        mbar_init(&S.s16_ready, kEpiWarps * 32);
+        mbar_init(&S.u16_ready, kEpiWarps * 32);
+        mbar_init(&S.epi_done, kEpiWarps * 32);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
+    // rows 16..31 of every slot's T diag(b) operand stay zero
+    for (int i = threadIdx.x; i < kRing * 16 * 16 / 2; i += kThreads) {
+        const int slot = i / 128, e = i % 128;
+        reinterpret_cast<uint32_t*>(S.st[slot].tbt + 16 * 16)[e] = 0u;
+    }
+    tc::fence_proxy_async_smem();
+    if (warp == kMmaWarp) {
+        tc::tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
     __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = S.tmem_base;
 
-    if (warp < kChainWarps) {
-        chain(P, U, S, warp, lane, err);
+    if (warp < kEpiWarps) {
+        epilogue(P, U, S, tmem, warp, lane, err);
+        tc::fence_before_sync();
+        mbar_arrive(&S.epi_done);
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) mma_issuer(U, S, tmem, err);
+        __syncwarp();
+        // free tensor memory once the epilogue is done with it
+        const bool ok = mbar_wait(&S.epi_done, 0u, err);
+        __syncwarp();
+        (void)ok;
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
     } else {
-        const int pw = warp - kChainWarps;
-        const float expA = expf(P.A_log[U.h]);
-        const float* dtb_h = P.dt_bias + (size_t)U.h * kDim + 4 * lane;
-        const float dtb[4] = {dtb_h[0], dtb_h[1], dtb_h[2], dtb_h[3]};
-        for (int c = pw; c < U.nch; c += kProdWarps) {
-            if (!produce_chunk(P, U, c, S.prod[pw], S.st[pw], &S.empty[pw], lane, expA, dtb, err))
-                return;
-            mbar_arrive(&S.full[pw]);
-        }
+        const int pt = threadIdx.x - kProdWarp0 * 32;
+        produce(P, U, S, pt / kTeamThreads, pt % kTeamThreads, err);
     }
 }
 
@@ -479,10 +650,10 @@ bool g_attr_set[64] = {};
 
 }  // namespace
 
-size_t fused_smem_bytes() { return sizeof(Smem); }
+size_t fused_smem_bytes() { return sizeof(Smem) + 1024; }
 
 cudaError_t launch_fused(const Problem& P, const SeqMap& M, int* err, cudaStream_t s) {
-    const size_t smem = sizeof(Smem);
+    const size_t smem = fused_smem_bytes();
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
