@@ -46,6 +46,9 @@ constexpr int RAW_LD = 136;   // bf16 / fp16 per padded 128-wide row (272 B)
 constexpr int F_LD = 132;     // fp32 per padded 128-wide row (528 B: ldmatrix conflict-free)
 constexpr int A_LD = 17;
 constexpr int TB_LD = 24;     // fp16 per row of T diag(b) (48 B)
+constexpr int T_SBO = 272;    // byte step between 8-row groups of the transposed 128 x 16
+                              // tiles: 16 bytes past 256 makes the 16-byte row stores
+                              // of a quarter warp hit all 32 banks once
 
 // tensor-memory columns (one allocation of 512)
 constexpr uint32_t kTmemCols = 512;
@@ -66,19 +69,21 @@ struct TeamSmem {
     float kg32[kChunk * F_LD];      // tf32 operands of the decay-ratio products
     float ki32[kChunk * F_LD];
     float qg32[kChunk * F_LD];
-    float part[kTeamWarps][2][kChunk * kChunk];   // per-warp partial A_kk, A_qk
+    float part[kTeamWarps][kChunk * kChunk];   // warps 0,1: A_kk halves; 2,3: A_qk halves
     float A[kChunk * A_LD];
     __half tb[kChunk * TB_LD];
     float beta[kChunk];
+    unsigned long long raw_full[2];            // bulk copies of a raw buffer landed
 };
 // One chunk's operands for the tensor-core recurrence (canonical K-major layouts)
 struct Stage {
     __half buo[2 * 32 * 64];   // B of [U|O] += S^T [-w; Q 2^G]^T: 32 x 128, 128B swizzle
-    __half vt[128 * 16];       // A of u^T = V^T (T diag b)^T: V^T 128 x 16, interleaved
-    __half kdt[128 * 16];      // B of the state update: (K 2^(G_last-G))^T 128 x 16
+    __half vt[16 * T_SBO / 2];     // A of u^T = V^T (T diag b)^T: V^T 128 x 16, interleaved
+    __half kdt[16 * T_SBO / 2];    // B of the state update: (K 2^(G_last-G))^T 128 x 16
     __half tbt[32 * 16];       // B of the u MMA: rows 0-15 T diag(b), rows 16-31 zero
     __half aqk[16 * 16];       // B of O += U A_qk^T: A_qk 16 x 16
     float gc[kDim];            // 2^G_last
+    unsigned char pad_[512];   // keep sizeof(Stage) a multiple of 1024
 };
 static_assert(sizeof(Stage) % 1024 == 0, "stages keep the swizzled tiles 1024-byte aligned");
 struct Smem {
@@ -160,27 +165,35 @@ struct Unit {
     int n, h, tok_start, L, nch;
 };
 
-// Issue the copies of chunk c's rows into one raw buffer (rows past the end are zeroed).
+// Start chunk c's rows landing in one raw buffer: 64 threads of the team each
+// issue one 256-byte bulk copy (one row of one tensor) on the TMA engine, all
+// completing on the buffer's mbarrier; rows past the end are zeroed with
+// ordinary stores.
 __device__ __forceinline__ void load_chunk(const Problem& P, const Unit& U, int c, RawChunk& R,
-                                           int tt) {
+                                           unsigned long long* mbar, int tt) {
     const int tok0 = U.tok_start + c * kChunk;
     const int len = min(kChunk, U.L - c * kChunk);
-    for (int i = tt; i < kChunk * 16; i += kTeamThreads) {
-        const int r = i >> 4, p = i & 15;
-        const int so = r * RAW_LD + p * 8;
+    const uint32_t mb = smem_u32(mbar);
+    if (tt == 0) tc::mbar_arrive_expect_tx(mb, (uint32_t)(4 * len * kDim * 2));
+    if (tt < 4 * kChunk) {
+        const int tensor = tt >> 4, r = tt & 15;
         if (r < len) {
-            const size_t go = ((size_t)(tok0 + r) * P.H + U.h) * kDim + p * 8;
-            cp_async16(&R.q[so], P.q + go);
-            cp_async16(&R.k[so], P.k + go);
-            cp_async16(&R.v[so], P.v + go);
-            cp_async16(&R.g[so], P.g + go);
-        } else {
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(&R.q[so]) = z;
-            *reinterpret_cast<uint4*>(&R.k[so]) = z;
-            *reinterpret_cast<uint4*>(&R.v[so]) = z;
-            *reinterpret_cast<uint4*>(&R.g[so]) = z;
+            // earlier generic-proxy reads of this buffer are ordered before the copy
+            tc::fence_proxy_async_smem();
+            const size_t go = ((size_t)(tok0 + r) * P.H + U.h) * kDim;
+            const __nv_bfloat16* src = tensor == 0 ? P.q : tensor == 1 ? P.k : tensor == 2 ? P.v : P.g;
+            __nv_bfloat16* dst = tensor == 0 ? R.q : tensor == 1 ? R.k : tensor == 2 ? R.v : R.g;
+            tc::bulk_g2s(smem_u32(&dst[r * RAW_LD]), src + go, kDim * 2, mb);
         }
+    }
+    for (int i = tt; i < (kChunk - len) * 16; i += kTeamThreads) {
+        const int r = len + (i >> 4), p = i & 15;
+        const int so = r * RAW_LD + p * 8;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(&R.q[so]) = z;
+        *reinterpret_cast<uint4*>(&R.k[so]) = z;
+        *reinterpret_cast<uint4*>(&R.v[so]) = z;
+        *reinterpret_cast<uint4*>(&R.g[so]) = z;
     }
 }
 
@@ -204,8 +217,7 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int team, int 
 
     int c = team;
     if (c >= U.nch) return;
-    load_chunk(P, U, c, T.raw[0], tt);
-    cp_async_commit();
+    load_chunk(P, U, c, T.raw[0], &T.raw_full[0], tt);
     float blogit = 0.0f;
     if (tt < kChunk && c * kChunk + tt < U.L)
         blogit = __bfloat162float(P.beta[beta_base + (size_t)(c * kChunk + tt) * P.H]);
@@ -214,7 +226,6 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int team, int 
         RawChunk& R = T.raw[it & 1];
         const int len = min(kChunk, U.L - c * kChunk);
         if (tt < kChunk) T.beta[tt] = (tt < len) ? sigmoid_fast(blogit) : 0.0f;
-        cp_async_wait<0>();  // this chunk's rows (issued one iteration earlier)
         // the chunk's slot must be free before anything is written into it; the
         // team votes so that a timed-out wait ends the whole team together
         const int slot = c % kRing;
@@ -227,11 +238,13 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int team, int 
         // next chunk into the other buffer
         const int cn = c + kTeams;
         if (cn < U.nch) {
-            load_chunk(P, U, cn, T.raw[(it + 1) & 1], tt);
+            load_chunk(P, U, cn, T.raw[(it + 1) & 1], &T.raw_full[(it + 1) & 1], tt);
             if (tt < kChunk && cn * kChunk + tt < U.L)
                 blogit = __bfloat162float(P.beta[beta_base + (size_t)(cn * kChunk + tt) * P.H]);
         }
-        cp_async_commit();
+        // this chunk's rows (copies issued one iteration earlier)
+        if (!mbar_wait(&T.raw_full[it & 1], (unsigned)((it >> 1) & 1), err)) ok = false;
+        if (!team_sync_and(team, ok)) return;
 
         // ---- gate pass: base-2 log-decay, cumulative over the chunk -------------
         float G0[8], G1[8];
@@ -269,6 +282,7 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int team, int 
         unsigned char* buo = reinterpret_cast<unsigned char*>(st.buo);
         unsigned char* kdt = reinterpret_cast<unsigned char*>(st.kdt);
         unsigned char* vt = reinterpret_cast<unsigned char*>(st.vt);
+        uint32_t kdp0[4], kdp1[4], vp0[4], vp1[4];   // 8 tokens of channels c2, c2+1
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = r0 + i;
@@ -291,45 +305,56 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int team, int 
             *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(16 + r, c2, 32)) =
                 pack_half2(qg0, qg1);
             // transposed tiles: (K 2^(G_last - G))^T and V^T, row = channel, K = token
-            *reinterpret_cast<__half*>(kdt + tc::interleaved_offset(c2, r, kChunk)) =
-                __float2half_rn(ki0 * gc0);
-            *reinterpret_cast<__half*>(kdt + tc::interleaved_offset(c2 + 1, r, kChunk)) =
-                __float2half_rn(ki1 * gc1);
-            *reinterpret_cast<__half*>(vt + tc::interleaved_offset(c2, r, kChunk)) =
-                __float2half_rn(vv.x);
-            *reinterpret_cast<__half*>(vt + tc::interleaved_offset(c2 + 1, r, kChunk)) =
-                __float2half_rn(vv.y);
+            const uint32_t kd2 = pack_half2(ki0 * gc0, ki1 * gc1);
+            const uint32_t v2 = pack_half2(vv.x, vv.y);
+            if (i & 1) {
+                kdp0[i >> 1] |= kd2 << 16;
+                kdp1[i >> 1] |= kd2 & 0xffff0000u;
+                vp0[i >> 1] |= v2 << 16;
+                vp1[i >> 1] |= v2 & 0xffff0000u;
+            } else {
+                kdp0[i >> 1] = kd2 & 0xffffu;
+                kdp1[i >> 1] = kd2 >> 16;
+                vp0[i >> 1] = v2 & 0xffffu;
+                vp1[i >> 1] = v2 >> 16;
+            }
         }
+        // one 16-byte core-matrix row per channel: tokens r0 .. r0 + 7
+        *reinterpret_cast<uint4*>(kdt + tc::interleaved16_offset(c2, r0, T_SBO)) =
+            make_uint4(kdp0[0], kdp0[1], kdp0[2], kdp0[3]);
+        *reinterpret_cast<uint4*>(kdt + tc::interleaved16_offset(c2 + 1, r0, T_SBO)) =
+            make_uint4(kdp1[0], kdp1[1], kdp1[2], kdp1[3]);
+        *reinterpret_cast<uint4*>(vt + tc::interleaved16_offset(c2, r0, T_SBO)) =
+            make_uint4(vp0[0], vp0[1], vp0[2], vp0[3]);
+        *reinterpret_cast<uint4*>(vt + tc::interleaved16_offset(c2 + 1, r0, T_SBO)) =
+            make_uint4(vp1[0], vp1[1], vp1[2], vp1[3]);
         team_sync(team);
 
-        // ---- decay-ratio products, tf32 MMA: warp w covers key channels 32w .. 32w+31
+        // ---- decay-ratio products, tf32 MMA: warps 0,1 form A_kk over key channels
+        //      0-63 / 64-127, warps 2,3 form A_qk likewise
         {
-            float pk[2][4] = {}, pq[2][4] = {};
+            float pa[2][4] = {};
+            const float* asrc = (warp < 2) ? T.kg32 : T.qg32;
             const int arow = (lane & 7) + 8 * ((lane >> 3) & 1);
             const int acol = 4 * (lane >> 4);
             const int brow = (lane & 7) + 8 * (lane >> 4);
             const int bcol = 4 * ((lane >> 3) & 1);
 #pragma unroll
-            for (int kq = 0; kq < 4; ++kq) {
-                const int kc = 32 * warp + 8 * kq;
-                uint32_t ak[4], aq[4], b[4];
-                ldsm_x4(ak, &T.kg32[arow * F_LD + kc + acol]);
-                ldsm_x4(aq, &T.qg32[arow * F_LD + kc + acol]);
+            for (int kq = 0; kq < 8; ++kq) {
+                const int kc = 64 * (warp & 1) + 8 * kq;
+                uint32_t a[4], b[4];
+                ldsm_x4(a, &asrc[arow * F_LD + kc + acol]);
                 ldsm_x4(b, &T.ki32[brow * F_LD + kc + bcol]);
-                mma_tf32(pk[0], ak, b[0], b[1]);
-                mma_tf32(pk[1], ak, b[2], b[3]);
-                mma_tf32(pq[0], aq, b[0], b[1]);
-                mma_tf32(pq[1], aq, b[2], b[3]);
+                mma_tf32(pa[0], a, b[0], b[1]);
+                mma_tf32(pa[1], a, b[2], b[3]);
             }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int hi = 0; hi < 2; ++hi) {
                     const int r = fg + 8 * hi, s = 8 * nt + 2 * ft;
-                    *reinterpret_cast<float2*>(&T.part[warp][0][r * kChunk + s]) =
-                        make_float2(pk[nt][2 * hi], pk[nt][2 * hi + 1]);
-                    *reinterpret_cast<float2*>(&T.part[warp][1][r * kChunk + s]) =
-                        make_float2(pq[nt][2 * hi], pq[nt][2 * hi + 1]);
+                    *reinterpret_cast<float2*>(&T.part[warp][r * kChunk + s]) =
+                        make_float2(pa[nt][2 * hi], pa[nt][2 * hi + 1]);
                 }
         }
         team_sync(team);
@@ -339,7 +364,7 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int team, int 
 #pragma unroll
             for (int e = lane; e < kChunk * kChunk; e += 32) {
                 const int r = e >> 4, s = e & 15;
-                const float x = T.part[0][0][e] + T.part[1][0][e] + T.part[2][0][e] + T.part[3][0][e];
+                const float x = T.part[0][e] + T.part[1][e];
                 T.A[r * A_LD + s] = (s < r) ? T.beta[r] * x : 0.0f;
             }
             __syncwarp();
@@ -370,9 +395,8 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int team, int 
 #pragma unroll
             for (int e = 2 * lane; e < kChunk * kChunk; e += 64) {
                 const int r = e >> 4, s = e & 15;
-                float x0 = T.part[0][1][e] + T.part[1][1][e] + T.part[2][1][e] + T.part[3][1][e];
-                float x1 = T.part[0][1][e + 1] + T.part[1][1][e + 1] + T.part[2][1][e + 1] +
-                           T.part[3][1][e + 1];
+                float x0 = T.part[2][e] + T.part[3][e];
+                float x1 = T.part[2][e + 1] + T.part[3][e + 1];
                 x0 = (s <= r) ? x0 : 0.0f;
                 x1 = (s + 1 <= r) ? x1 : 0.0f;
                 *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(st.aqk) +
@@ -432,7 +456,7 @@ __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
         if (!mbar_wait(&S.full[slot], (unsigned)((c / kRing) & 1), err)) return;
         if (!mbar_wait(&S.s16_ready, (unsigned)(c & 1), err)) return;
         tc::fence_after_sync();
-        tc::mma_ss(uo, tc::smem_desc(smem_u32(st.vt), 128, 256, tc::kSwizzleNone),
+        tc::mma_ss(uo, tc::smem_desc(smem_u32(st.vt), 128, T_SBO, tc::kSwizzleNone),
                    tc::smem_desc(smem_u32(st.tbt), 128, 256, tc::kSwizzleNone), id32, 0);
         const uint32_t buo = smem_u32(st.buo);
 #pragma unroll
@@ -445,7 +469,7 @@ __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
         if (!mbar_wait(&S.u16_ready, (unsigned)(c & 1), err)) return;
         tc::fence_after_sync();
         tc::mma_ts(tmem + TM_S32, tmem + TM_U16,
-                   tc::smem_desc(smem_u32(st.kdt), 128, 256, tc::kSwizzleNone), id128, 1);
+                   tc::smem_desc(smem_u32(st.kdt), 128, T_SBO, tc::kSwizzleNone), id128, 1);
         tc::mma_ts(uo + 16, tmem + TM_U16,
                    tc::smem_desc(smem_u32(st.aqk), 128, 256, tc::kSwizzleNone), id16, 1);
         tc::commit(smem_u32(&S.s_done));
@@ -610,6 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Problem P, SeqMap M,
         mbar_init(&S.s16_ready, kEpiWarps * 32);
         mbar_init(&S.u16_ready, kEpiWarps * 32);
         mbar_init(&S.epi_done, kEpiWarps * 32);
+        for (int t = 0; t < kTeams; ++t)
+            for (int b = 0; b < 2; ++b) mbar_init(&S.team[t].raw_full[b], 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     // rows 16..31 of every slot's T diag(b) operand stay zero

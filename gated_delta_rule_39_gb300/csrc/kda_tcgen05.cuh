@@ -40,6 +40,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 __host__ __device__ constexpr int interleaved_offset(int row, int k, int kdim) {
     return ((row >> 3) * (kdim >> 3) + (k >> 3)) * 128 + (row & 7) * 16 + (k & 7) * 2;
 }
+// same, with an explicit byte step `sbo` between 8-row groups (K = 16 elements,
+// two core matrices per row group, 128 bytes apart)
+__host__ __device__ constexpr int interleaved16_offset(int row, int k, int sbo) {
+    return (row >> 3) * sbo + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2;
+}
 // byte offset of element (row, k) in a 128B-swizzled K-major tile of `rows` rows
 // and K = 64 * kblocks 16-bit elements, stored as [kblock][row][128 bytes]
 __host__ __device__ constexpr int swizzled_offset(int row, int k, int rows) {
@@ -64,6 +69,17 @@ __device__ __forceinline__ void fence_before_sync() {
 }
 __device__ __forceinline__ void fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+// bulk copy global -> shared on the TMA engine, completing `bytes` on an mbarrier
+__device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uint32_t bytes,
+                                         uint32_t mbar_smem) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+        ::"r"(dst_smem), "l"(src), "r"(bytes), "r"(mbar_smem) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar_smem, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+                 ::"r"(mbar_smem), "r"(bytes) : "memory");
 }
 // generic-proxy shared-memory writes -> visible to the tensor core (async proxy)
 __device__ __forceinline__ void fence_proxy_async_smem() {
