@@ -2,30 +2,26 @@
 // the chunkwise algorithm, so q, k, v, g and beta are read from HBM once and
 // only the output and the states are written.
 //
-//   producer teams (2 x 4 warps)  the token-parallel stage.  Team t handles
-//                       chunks t, t+2, t+4, ... with its four warps working
-//                       together on one chunk while the next chunk's rows are
-//                       already in flight (double-buffered cp.async): gates,
-//                       in-chunk cumulative base-2 log-decay G, decay-ratio
-//                       products A_kk / A_qk (tf32 MMA), (I + A_kk)^-1 by
-//                       forward substitution, WY factors u = T diag(b) V and
-//                       w = T diag(b)(K * 2^G) (fp16 MMA), Q * 2^G,
-//                       K * 2^(G_last - G), 2^G_last
-//   chain warps (8)     the sequential stage over the chunks: the fp32 state
-//                       lives in registers as S^T fragments, 16 value rows per
-//                       warp; per chunk U^T = u^T - S^T w^T, O^T = S^T (Q 2^G)^T
-//                       + U^T A_qk^T, S^T <- S^T Diag(2^G_last) + U^T (K 2^(G_last-G))
-//
-// The stages hand chunk factors over through a 4-slot shared-memory ring
-// guarded by mbarriers (full: producers -> chain, empty: chain -> producers);
-// every wait is bounded and gives up with KDA_ERR_DEVICE_TIMEOUT.
+//   producer warps (8)  the token-parallel stage.  Warp w owns key / value
+//                       channels 16w .. 16w+15 of every 16-token chunk: it loads
+//                       its slice of q, k, v, g straight into registers (one chunk
+//                       ahead), computes the gates and their in-chunk cumulative
+//                       sum across rows with warp shuffles, the decay factors,
+//                       the operand tiles of the recurrence (Q 2^G, K 2^(G_last-G),
+//                       V, 2^G_last) and its share of the decay-ratio products
+//                       A_kk and A_qk (tf32 MMA fed from registers, summed across
+//                       warps in shared memory).  One chunk later it forms its
+//                       slice of w = T diag(b)(K 2^G).
+//   solver warp         (I + A_kk)^-1 by forward substitution, T diag(b), A_qk.
+//   MMA warp            issues the tcgen05 MMAs of the recurrence (one thread).
+//   epilogue warps (4)  own the tensor-memory state S^T (lane v = value channel v).
 //
 // Chunkwise DPLR-variant (WY) algorithm with 16-token chunks, a 16 x 16
 // inverse and base-2 gates: "Moonshot AI Open-Sources FlashKDA", sections
 // "Why KDA?" and "What makes the kernel fast".  The pages split the two
 // stages into two kernels on Hopper because the sequential stage alone left
 // SMs idle; here the split stays, but inside one CTA, so the intermediate
-// factors never leave shared memory.
+// factors never leave the SM.
 #include "kda_internal.cuh"
 #include "kda_tcgen05.cuh"
 
@@ -35,20 +31,18 @@ namespace {
 
 constexpr int kEpiWarps = 4;                // epilogue: one TMEM lane (value row) per thread
 constexpr int kMmaWarp = kEpiWarps;         // issues the tcgen05 MMAs, owns tensor memory
-constexpr int kTeams = 2;                   // producer teams
-constexpr int kTeamWarps = 4;
-constexpr int kTeamThreads = kTeamWarps * 32;
-constexpr int kProdWarp0 = kMmaWarp + 1;
-constexpr int kRing = 4;                    // chunk-operand slots
-constexpr int kThreads = (kProdWarp0 + kTeams * kTeamWarps) * 32;
+constexpr int kSolveWarp = kMmaWarp + 1;    // 16 x 16 inverse
+constexpr int kProdWarp0 = kSolveWarp + 1;
+constexpr int kProdWarps = 8;               // 16 key channels each
+constexpr int kProdThreads = kProdWarps * 32;
+constexpr int kRing = 6;                    // chunk-operand slots
+constexpr int kThreads = (kProdWarp0 + kProdWarps) * 32;
 
-constexpr int RAW_LD = 136;   // bf16 / fp16 per padded 128-wide row (272 B)
-constexpr int F_LD = 132;     // fp32 per padded 128-wide row (528 B: ldmatrix conflict-free)
 constexpr int A_LD = 17;
-constexpr int TB_LD = 24;     // fp16 per row of T diag(b) (48 B)
+constexpr int TB_LD = 24;     // fp16 per row of T diag(b) (48 B: ldmatrix conflict-free)
+constexpr int KG_LD = 24;     // fp16 per row of a warp's K 2^G tile (48 B)
 constexpr int T_SBO = 272;    // byte step between 8-row groups of the transposed 128 x 16
-                              // tiles: 16 bytes past 256 makes the 16-byte row stores
-                              // of a quarter warp hit all 32 banks once
+                              // tiles (16 bytes past 256 spreads row groups over banks)
 
 // tensor-memory columns (one allocation of 512)
 constexpr uint32_t kTmemCols = 512;
@@ -57,40 +51,30 @@ constexpr uint32_t TM_S16 = 128;   // S^T as the fp16 A operand, 64 columns
 constexpr uint32_t TM_UO = 192;    // [U | O] accumulators, 2 buffers x 32 columns
 constexpr uint32_t TM_U16 = 256;   // U^T as the fp16 A operand, 8 columns
 
-// Raw rows of one chunk.  After the gate pass, g holds fp16 K * 2^G in place.
-struct RawChunk {
-    __nv_bfloat16 q[kChunk * RAW_LD];
-    __nv_bfloat16 k[kChunk * RAW_LD];
-    __nv_bfloat16 v[kChunk * RAW_LD];
-    __nv_bfloat16 g[kChunk * RAW_LD];
-};
-struct TeamSmem {
-    RawChunk raw[2];                // double buffer: chunk being worked on / next chunk
-    float kg32[kChunk * F_LD];      // tf32 operands of the decay-ratio products
-    float ki32[kChunk * F_LD];
-    float qg32[kChunk * F_LD];
-    float part[kTeamWarps][kChunk * kChunk];   // warps 0,1: A_kk halves; 2,3: A_qk halves
-    float A[kChunk * A_LD];
-    __half tb[kChunk * TB_LD];
-    float beta[kChunk];
-    unsigned long long raw_full[2];            // bulk copies of a raw buffer landed
-};
 // One chunk's operands for the tensor-core recurrence (canonical K-major layouts)
 struct Stage {
-    __half buo[2 * 32 * 64];   // B of [U|O] += S^T [-w; Q 2^G]^T: 32 x 128, 128B swizzle
+    __half buo[2 * 32 * 64];       // B of [U|O] += S^T [-w; Q 2^G]^T: 32 x 128, 128B swizzle
     __half vt[16 * T_SBO / 2];     // A of u^T = V^T (T diag b)^T: V^T 128 x 16, interleaved
     __half kdt[16 * T_SBO / 2];    // B of the state update: (K 2^(G_last-G))^T 128 x 16
-    __half tbt[32 * 16];       // B of the u MMA: rows 0-15 T diag(b), rows 16-31 zero
-    __half aqk[16 * 16];       // B of O += U A_qk^T: A_qk 16 x 16
-    float gc[kDim];            // 2^G_last
-    unsigned char pad_[512];   // keep sizeof(Stage) a multiple of 1024
+    __half tbt[32 * 16];           // B of the u MMA: rows 0-15 T diag(b), rows 16-31 zero
+    __half aqk[16 * 16];           // B of O += U A_qk^T: A_qk 16 x 16
+    float gc[kDim];                // 2^G_last
+    unsigned char pad_[512];       // keep sizeof(Stage) a multiple of 1024
 };
 static_assert(sizeof(Stage) % 1024 == 0, "stages keep the swizzled tiles 1024-byte aligned");
+struct ProdShared {
+    float part[2][kProdWarps][2][kChunk * kChunk]; // [chunk parity][warp][A_kk, A_qk] partials
+    __half tb[2][kChunk * TB_LD];                  // T diag(b) per chunk parity
+    __half kg[kProdWarps][2][kChunk * KG_LD];      // each warp's K 2^G tile per chunk parity
+    float A[kChunk * A_LD];                        // solver scratch
+};
 struct Smem {
     Stage st[kRing];
-    TeamSmem team[kTeams];
+    ProdShared pr;
     unsigned long long full[kRing];    // producers -> MMA / epilogue
     unsigned long long empty[kRing];   // MMA commit -> producers
+    unsigned long long a_ready[2];     // producers' partial A_kk / A_qk summed
+    unsigned long long t_ready[2];     // solver: T diag(b), A_qk written
     unsigned long long uo_done;        // U|O MMAs complete
     unsigned long long s_done;         // state update + O MMAs complete
     unsigned long long s16_ready;      // epilogue: S^T fp16 copy written, S^T rescaled
@@ -98,7 +82,6 @@ struct Smem {
     unsigned long long epi_done;       // epilogue finished with tensor memory
     uint32_t tmem_base;
 };
-static_assert(sizeof(RawChunk) % 16 == 0 && sizeof(TeamSmem) % 16 == 0, "16-byte alignment");
 
 // ---- small helpers ------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(unsigned long long* b, int count) {
@@ -130,23 +113,6 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* b, unsigned parity
     }
     return true;
 }
-// named barrier over the 128 threads of one producer team (ids 1, 2)
-__device__ __forceinline__ void team_sync(int team) {
-    asm volatile("bar.sync %0, %1;\n" ::"r"(team + 1), "n"(kTeamThreads) : "memory");
-}
-// team barrier that also returns the AND of every thread's flag
-__device__ __forceinline__ bool team_sync_and(int team, bool flag) {
-    unsigned r;
-    asm volatile(
-        "{\n .reg .pred p, q;\n"
-        " setp.ne.u32 p, %1, 0;\n"
-        " bar.red.and.pred q, %2, %3, p;\n"
-        " selp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(r)
-        : "r"((unsigned)flag), "r"(team + 1), "n"(kTeamThreads)
-        : "memory");
-    return r != 0;
-}
 // packed fp32 pair multiply (one instruction on sm_100 and later)
 __device__ __forceinline__ void mul2(float& a, float& b, float2 s) {
     unsigned long long x, y, z;
@@ -165,277 +131,256 @@ struct Unit {
     int n, h, tok_start, L, nch;
 };
 
-// Start chunk c's rows landing in one raw buffer: 64 threads of the team each
-// issue one 256-byte bulk copy (one row of one tensor) on the TMA engine, all
-// completing on the buffer's mbarrier; rows past the end are zeroed with
-// ordinary stores.
-__device__ __forceinline__ void load_chunk(const Problem& P, const Unit& U, int c, RawChunk& R,
-                                           unsigned long long* mbar, int tt) {
-    const int tok0 = U.tok_start + c * kChunk;
+// ---- token-parallel stage: producer warp w, channels 16w .. 16w+15 ----------------
+// Lane (g, t) = (lane >> 2, lane & 3) holds rows g and g+8 of the chunk for the
+// channel pairs p = 16w + 8kk + 2t, p+1 (kk = 0, 1).  In the tf32 MMA fragments
+// of k-step kk the pair plays logical columns t and t+4; the decay-ratio
+// products sum over channels, so this relabelling leaves them unchanged.
+struct RawSlice {
+    uint32_t q[2][2], k[2][2], v[2][2], g[2][2];   // [row g / g+8][kk] bf16 pairs
+};
+
+__device__ __forceinline__ void load_slice(const Problem& P, const Unit& U, int c, int cbase,
+                                           int lg, int lt, RawSlice& X) {
     const int len = min(kChunk, U.L - c * kChunk);
-    const uint32_t mb = smem_u32(mbar);
-    if (tt == 0) tc::mbar_arrive_expect_tx(mb, (uint32_t)(4 * len * kDim * 2));
-    if (tt < 4 * kChunk) {
-        const int tensor = tt >> 4, r = tt & 15;
-        if (r < len) {
-            // earlier generic-proxy reads of this buffer are ordered before the copy
-            tc::fence_proxy_async_smem();
-            const size_t go = ((size_t)(tok0 + r) * P.H + U.h) * kDim;
-            const __nv_bfloat16* src = tensor == 0 ? P.q : tensor == 1 ? P.k : tensor == 2 ? P.v : P.g;
-            __nv_bfloat16* dst = tensor == 0 ? R.q : tensor == 1 ? R.k : tensor == 2 ? R.v : R.g;
-            tc::bulk_g2s(smem_u32(&dst[r * RAW_LD]), src + go, kDim * 2, mb);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int r = lg + 8 * i;
+        const bool ok = r < len;
+        const size_t row = ((size_t)(U.tok_start + c * kChunk + (ok ? r : 0)) * P.H + U.h) * kDim;
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            const size_t o = row + cbase + 8 * kk + 2 * lt;
+            X.q[i][kk] = ok ? __ldg(reinterpret_cast<const unsigned int*>(P.q + o)) : 0u;
+            X.k[i][kk] = ok ? __ldg(reinterpret_cast<const unsigned int*>(P.k + o)) : 0u;
+            X.v[i][kk] = ok ? __ldg(reinterpret_cast<const unsigned int*>(P.v + o)) : 0u;
+            X.g[i][kk] = ok ? __ldg(reinterpret_cast<const unsigned int*>(P.g + o)) : 0u;
         }
-    }
-    for (int i = tt; i < (kChunk - len) * 16; i += kTeamThreads) {
-        const int r = len + (i >> 4), p = i & 15;
-        const int so = r * RAW_LD + p * 8;
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(&R.q[so]) = z;
-        *reinterpret_cast<uint4*>(&R.k[so]) = z;
-        *reinterpret_cast<uint4*>(&R.v[so]) = z;
-        *reinterpret_cast<uint4*>(&R.g[so]) = z;
     }
 }
 
-// ---- token-parallel stage: one producer team, all its chunks ----------------------
-__device__ void produce(const Problem& P, const Unit& U, Smem& S, int team, int tt, int* err) {
-    TeamSmem& T = S.team[team];
-    const int warp = tt >> 5, lane = tt & 31;
-    const int fg = lane >> 2, ft = lane & 3;
-    // gate-pass ownership: channel pair (2j, 2j+1), rows 8 half .. 8 half + 7
-    const int j = warp * 16 + (lane & 15);
-    const int half = lane >> 4;
-    const int c2 = 2 * j;
-    const int r0 = 8 * half;
+__device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lane, int* err) {
+    const int lg = lane >> 2, lt = lane & 3;
+    const int cbase = 16 * w;
     const float expA = expf(P.A_log[U.h]);
-    // sigmoid argument in base 2: -(exp(A_log) (g + dt_bias)) log2 e = g ga + gb
-    const float ga = -expA * kLog2e;
-    const float gb0 = ga * P.dt_bias[(size_t)U.h * kDim + c2];
-    const float gb1 = ga * P.dt_bias[(size_t)U.h * kDim + c2 + 1];
+    const float ga = -expA * kLog2e;   // sigmoid argument in base 2: g ga + gb
+    float gb[2][2];
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) gb[kk][e] = ga * P.dt_bias[(size_t)U.h * kDim + cbase + 8 * kk + 2 * lt + e];
     const float lb2 = P.lower_bound * kLog2e;
-    const size_t beta_base = (size_t)U.tok_start * P.H + U.h;
+    ProdShared& PS = S.pr;
 
-    int c = team;
-    if (c >= U.nch) return;
-    load_chunk(P, U, c, T.raw[0], &T.raw_full[0], tt);
-    float blogit = 0.0f;
-    if (tt < kChunk && c * kChunk + tt < U.L)
-        blogit = __bfloat162float(P.beta[beta_base + (size_t)(c * kChunk + tt) * P.H]);
+    RawSlice nxt;
+    if (U.nch > 0) load_slice(P, U, 0, cbase, lg, lt, nxt);
 
-    for (int it = 0; c < U.nch; c += kTeams, ++it) {
-        RawChunk& R = T.raw[it & 1];
-        const int len = min(kChunk, U.L - c * kChunk);
-        if (tt < kChunk) T.beta[tt] = (tt < len) ? sigmoid_fast(blogit) : 0.0f;
-        // the chunk's slot must be free before anything is written into it; the
-        // team votes so that a timed-out wait ends the whole team together
-        const int slot = c % kRing;
-        const int k = c / kRing;
-        bool ok = true;
-        if (k >= 1) ok = mbar_wait(&S.empty[slot], (unsigned)((k - 1) & 1), err);
-        if (!team_sync_and(team, ok)) return;
-        Stage& st = S.st[slot];
-        // every thread of the team is past the previous chunk: prefetch the team's
-        // next chunk into the other buffer
-        const int cn = c + kTeams;
-        if (cn < U.nch) {
-            load_chunk(P, U, cn, T.raw[(it + 1) & 1], &T.raw_full[(it + 1) & 1], tt);
-            if (tt < kChunk && cn * kChunk + tt < U.L)
-                blogit = __bfloat162float(P.beta[beta_base + (size_t)(cn * kChunk + tt) * P.H]);
-        }
-        // this chunk's rows (copies issued one iteration earlier)
-        if (!mbar_wait(&T.raw_full[it & 1], (unsigned)((it >> 1) & 1), err)) ok = false;
-        if (!team_sync_and(team, ok)) return;
+    for (int c = 0; c <= U.nch; ++c) {
+        if (c < U.nch) {
+            const RawSlice X = nxt;
+            if (c + 1 < U.nch) load_slice(P, U, c + 1, cbase, lg, lt, nxt);
+            const int len = min(kChunk, U.L - c * kChunk);
+            const int slot = c % kRing;
+            Stage& st = S.st[slot];
+            const int par = c & 1;
+            bool ok = true;
+            if (c >= kRing) ok = mbar_wait(&S.empty[slot], (unsigned)(((c / kRing) - 1) & 1), err);
+            if (!__all_sync(0xffffffffu, ok)) return;
 
-        // ---- gate pass: base-2 log-decay, cumulative over the chunk -------------
-        float G0[8], G1[8];
-        {
-            float run0 = 0.f, run1 = 0.f;
+            // gates, cumulative over rows: Hillis-Steele scan across the 8 lanes of equal t
+            float G[2][2][2];   // [row g / g+8][kk][e]
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = r0 + i;
-                const float2 gv = bf2_to_f2(*reinterpret_cast<const uint32_t*>(&R.g[r * RAW_LD + c2]));
-                const float s0 = rcp_approx(1.0f + ex2_approx(fmaf(gv.x, ga, gb0)));
-                const float s1 = rcp_approx(1.0f + ex2_approx(fmaf(gv.y, ga, gb1)));
-                if (r < len) {
-                    run0 = fmaf(lb2, s0, run0);
-                    run1 = fmaf(lb2, s1, run1);
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const float2 gv = bf2_to_f2(X.g[i][kk]);
+                    const bool valid = lg + 8 * i < len;
+                    const float s0 = rcp_approx(1.0f + ex2_approx(fmaf(gv.x, ga, gb[kk][0])));
+                    const float s1 = rcp_approx(1.0f + ex2_approx(fmaf(gv.y, ga, gb[kk][1])));
+                    G[i][kk][0] = valid ? lb2 * s0 : 0.0f;
+                    G[i][kk][1] = valid ? lb2 * s1 : 0.0f;
                 }
-                G0[i] = run0;
-                G1[i] = run1;
-            }
-            // rows 8..15 continue from the total of rows 0..7 (held by lane ^ 16)
-            const float t0 = __shfl_xor_sync(0xffffffffu, run0, 16);
-            const float t1 = __shfl_xor_sync(0xffffffffu, run1, 16);
-            if (half) {
+            float glast[2][2];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    G0[i] += t0;
-                    G1[i] += t1;
+            for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float a = G[0][kk][e], b = G[1][kk][e];
+#pragma unroll
+                    for (int d = 4; d < 32; d <<= 1) {
+                        const float ya = __shfl_up_sync(0xffffffffu, a, d);
+                        const float yb = __shfl_up_sync(0xffffffffu, b, d);
+                        if (lane >= d) {
+                            a += ya;
+                            b += yb;
+                        }
+                    }
+                    const float tot = __shfl_sync(0xffffffffu, a, 28 + lt);   // rows 0..7
+                    G[0][kk][e] = a;
+                    G[1][kk][e] = tot + b;
+                    glast[kk][e] = __shfl_sync(0xffffffffu, tot + b, 28 + lt);   // row 15
+                }
+
+            // decay factors and operand tiles
+            unsigned char* buo = reinterpret_cast<unsigned char*>(st.buo);
+            unsigned char* kdt = reinterpret_cast<unsigned char*>(st.kdt);
+            unsigned char* vt = reinterpret_cast<unsigned char*>(st.vt);
+            __half* kgt = PS.kg[w][par];
+            uint32_t akf[2][4], aqf[2][4], bf0[2][2], bf1[2][2];
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                const int p = cbase + 8 * kk + 2 * lt;
+                const float gc0 = ex2_approx(glast[kk][0]), gc1 = ex2_approx(glast[kk][1]);
+                if (lg == 0) *reinterpret_cast<float2*>(&st.gc[p]) = make_float2(gc0, gc1);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int r = lg + 8 * i;
+                    const float e0 = ex2_approx(G[i][kk][0]), e1 = ex2_approx(G[i][kk][1]);
+                    const float d0 = ex2_approx(-G[i][kk][0]), d1 = ex2_approx(-G[i][kk][1]);
+                    const float2 kv = bf2_to_f2(X.k[i][kk]);
+                    const float2 qv = bf2_to_f2(X.q[i][kk]);
+                    const float2 vv = bf2_to_f2(X.v[i][kk]);
+                    const float kg0 = kv.x * e0, kg1 = kv.y * e1;
+                    const float ki0 = kv.x * d0, ki1 = kv.y * d1;
+                    const float qg0 = qv.x * e0, qg1 = qv.y * e1;
+                    // tf32 fragments: A rows g / g+8 -> a0,a2 / a1,a3; B n-tile i
+                    akf[kk][i] = to_tf32(kg0);
+                    akf[kk][i + 2] = to_tf32(kg1);
+                    aqf[kk][i] = to_tf32(qg0);
+                    aqf[kk][i + 2] = to_tf32(qg1);
+                    if (i == 0) {
+                        bf0[kk][0] = to_tf32(ki0);
+                        bf0[kk][1] = to_tf32(ki1);
+                    } else {
+                        bf1[kk][0] = to_tf32(ki0);
+                        bf1[kk][1] = to_tf32(ki1);
+                    }
+                    *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(16 + r, p, 32)) =
+                        pack_half2(qg0, qg1);
+                    *reinterpret_cast<uint32_t*>(&kgt[r * KG_LD + 8 * kk + 2 * lt]) =
+                        pack_half2(kg0, kg1);
+                    *reinterpret_cast<__half*>(kdt + tc::interleaved16_offset(p, r, T_SBO)) =
+                        __float2half_rn(ki0 * gc0);
+                    *reinterpret_cast<__half*>(kdt + tc::interleaved16_offset(p + 1, r, T_SBO)) =
+                        __float2half_rn(ki1 * gc1);
+                    *reinterpret_cast<__half*>(vt + tc::interleaved16_offset(p, r, T_SBO)) =
+                        __float2half_rn(vv.x);
+                    *reinterpret_cast<__half*>(vt + tc::interleaved16_offset(p + 1, r, T_SBO)) =
+                        __float2half_rn(vv.y);
                 }
             }
-        }
-        const float gl0 = __shfl_sync(0xffffffffu, G0[7], lane | 16);
-        const float gl1 = __shfl_sync(0xffffffffu, G1[7], lane | 16);
-        const float gc0 = ex2_approx(gl0), gc1 = ex2_approx(gl1);
-        if (half == 0) *reinterpret_cast<float2*>(&st.gc[c2]) = make_float2(gc0, gc1);
-        __half* kg16 = reinterpret_cast<__half*>(R.g);
-        unsigned char* buo = reinterpret_cast<unsigned char*>(st.buo);
-        unsigned char* kdt = reinterpret_cast<unsigned char*>(st.kdt);
-        unsigned char* vt = reinterpret_cast<unsigned char*>(st.vt);
-        uint32_t kdp0[4], kdp1[4], vp0[4], vp1[4];   // 8 tokens of channels c2, c2+1
+            // this warp's share of A_kk = (K 2^G)(K 2^-G)^T and A_qk = (Q 2^G)(K 2^-G)^T
+            float pk[2][4] = {}, pq[2][4] = {};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = r0 + i;
-            const float e0 = ex2_approx(G0[i]), e1 = ex2_approx(G1[i]);
-            const float d0 = ex2_approx(-G0[i]), d1 = ex2_approx(-G1[i]);
-            const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t*>(&R.k[r * RAW_LD + c2]));
-            const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t*>(&R.q[r * RAW_LD + c2]));
-            const float2 vv = bf2_to_f2(*reinterpret_cast<const uint32_t*>(&R.v[r * RAW_LD + c2]));
-            const float kg0 = kv.x * e0, kg1 = kv.y * e1;
-            const float ki0 = kv.x * d0, ki1 = kv.y * d1;
-            const float qg0 = qv.x * e0, qg1 = qv.y * e1;
-            *reinterpret_cast<float2*>(&T.kg32[r * F_LD + c2]) =
-                make_float2(tf32_round(kg0), tf32_round(kg1));
-            *reinterpret_cast<float2*>(&T.ki32[r * F_LD + c2]) =
-                make_float2(tf32_round(ki0), tf32_round(ki1));
-            *reinterpret_cast<float2*>(&T.qg32[r * F_LD + c2]) =
-                make_float2(tf32_round(qg0), tf32_round(qg1));
-            *reinterpret_cast<uint32_t*>(&kg16[r * RAW_LD + c2]) = pack_half2(kg0, kg1);
-            // Q 2^G: rows 16..31 of the [-w; Q 2^G] operand (K-major, 128B swizzle)
-            *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(16 + r, c2, 32)) =
-                pack_half2(qg0, qg1);
-            // transposed tiles: (K 2^(G_last - G))^T and V^T, row = channel, K = token
-            const uint32_t kd2 = pack_half2(ki0 * gc0, ki1 * gc1);
-            const uint32_t v2 = pack_half2(vv.x, vv.y);
-            if (i & 1) {
-                kdp0[i >> 1] |= kd2 << 16;
-                kdp1[i >> 1] |= kd2 & 0xffff0000u;
-                vp0[i >> 1] |= v2 << 16;
-                vp1[i >> 1] |= v2 & 0xffff0000u;
-            } else {
-                kdp0[i >> 1] = kd2 & 0xffffu;
-                kdp1[i >> 1] = kd2 >> 16;
-                vp0[i >> 1] = v2 & 0xffffu;
-                vp1[i >> 1] = v2 >> 16;
+            for (int kk = 0; kk < 2; ++kk) {
+                mma_tf32(pk[0], akf[kk], bf0[kk][0], bf0[kk][1]);
+                mma_tf32(pk[1], akf[kk], bf1[kk][0], bf1[kk][1]);
+                mma_tf32(pq[0], aqf[kk], bf0[kk][0], bf0[kk][1]);
+                mma_tf32(pq[1], aqf[kk], bf1[kk][0], bf1[kk][1]);
             }
-        }
-        // one 16-byte core-matrix row per channel: tokens r0 .. r0 + 7
-        *reinterpret_cast<uint4*>(kdt + tc::interleaved16_offset(c2, r0, T_SBO)) =
-            make_uint4(kdp0[0], kdp0[1], kdp0[2], kdp0[3]);
-        *reinterpret_cast<uint4*>(kdt + tc::interleaved16_offset(c2 + 1, r0, T_SBO)) =
-            make_uint4(kdp1[0], kdp1[1], kdp1[2], kdp1[3]);
-        *reinterpret_cast<uint4*>(vt + tc::interleaved16_offset(c2, r0, T_SBO)) =
-            make_uint4(vp0[0], vp0[1], vp0[2], vp0[3]);
-        *reinterpret_cast<uint4*>(vt + tc::interleaved16_offset(c2 + 1, r0, T_SBO)) =
-            make_uint4(vp1[0], vp1[1], vp1[2], vp1[3]);
-        team_sync(team);
-
-        // ---- decay-ratio products, tf32 MMA: warps 0,1 form A_kk over key channels
-        //      0-63 / 64-127, warps 2,3 form A_qk likewise
-        {
-            float pa[2][4] = {};
-            const float* asrc = (warp < 2) ? T.kg32 : T.qg32;
-            const int arow = (lane & 7) + 8 * ((lane >> 3) & 1);
-            const int acol = 4 * (lane >> 4);
-            const int brow = (lane & 7) + 8 * (lane >> 4);
-            const int bcol = 4 * ((lane >> 3) & 1);
-#pragma unroll
-            for (int kq = 0; kq < 8; ++kq) {
-                const int kc = 64 * (warp & 1) + 8 * kq;
-                uint32_t a[4], b[4];
-                ldsm_x4(a, &asrc[arow * F_LD + kc + acol]);
-                ldsm_x4(b, &T.ki32[brow * F_LD + kc + bcol]);
-                mma_tf32(pa[0], a, b[0], b[1]);
-                mma_tf32(pa[1], a, b[2], b[3]);
-            }
+            // partials go to this warp's own slots; the solver sums them in a fixed
+            // order, so results do not depend on warp timing
+            float* ak = PS.part[par][w][0];
+            float* aq = PS.part[par][w][1];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int hi = 0; hi < 2; ++hi) {
-                    const int r = fg + 8 * hi, s = 8 * nt + 2 * ft;
-                    *reinterpret_cast<float2*>(&T.part[warp][r * kChunk + s]) =
-                        make_float2(pa[nt][2 * hi], pa[nt][2 * hi + 1]);
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int e = (lg + 8 * hh) * kChunk + 8 * nt + 2 * lt;
+                    *reinterpret_cast<float2*>(&ak[e]) = make_float2(pk[nt][2 * hh], pk[nt][2 * hh + 1]);
+                    *reinterpret_cast<float2*>(&aq[e]) = make_float2(pq[nt][2 * hh], pq[nt][2 * hh + 1]);
                 }
+            mbar_arrive(&S.a_ready[par]);
         }
-        team_sync(team);
+        // ---- one chunk behind: w = T diag(b)(K 2^G) for this warp's channels -------
+        if (c >= 1) {
+            const int cp = c - 1;
+            const int par = cp & 1;
+            const bool ok = mbar_wait(&S.t_ready[par], (unsigned)((cp >> 1) & 1), err);
+            if (!__all_sync(0xffffffffu, ok)) return;
+            Stage& st = S.st[cp % kRing];
+            unsigned char* buo = reinterpret_cast<unsigned char*>(st.buo);
+            uint32_t ta[4], b[4];
+            ldsm_x4(ta, &PS.tb[par][((lane & 7) + 8 * ((lane >> 3) & 1)) * TB_LD + 8 * (lane >> 4)]);
+            ldsm_x4_t(b, &PS.kg[w][par][((lane & 7) + 8 * ((lane >> 3) & 1)) * KG_LD + 8 * (lane >> 4)]);
+            float cw0[4] = {}, cw1[4] = {};
+            mma_f16(cw0, ta, b[0], b[1]);
+            mma_f16(cw1, ta, b[2], b[3]);
+            const int col0 = cbase + 2 * lt, col1 = col0 + 8;
+            *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(lg, col0, 32)) = pack_half2(-cw0[0], -cw0[1]);
+            *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(lg + 8, col0, 32)) = pack_half2(-cw0[2], -cw0[3]);
+            *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(lg, col1, 32)) = pack_half2(-cw1[0], -cw1[1]);
+            *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(lg + 8, col1, 32)) = pack_half2(-cw1[2], -cw1[3]);
+            // generic-proxy writes of this thread -> visible to the tensor core
+            tc::fence_proxy_async_smem();
+            mbar_arrive(&S.full[cp % kRing]);
+        }
+    }
+}
 
-        if (warp == 0) {
-            // A_kk = diag(b) (sum of partials), strictly lower; then T = (I + A_kk)^-1
+// ---- solver warp: (I + A_kk)^-1, T diag(b), A_qk for every chunk ------------------
+__device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* err) {
+    ProdShared& PS = S.pr;
+    const size_t beta_base = (size_t)U.tok_start * P.H + U.h;
+    float logit = 0.0f;
+    if (U.nch > 0 && lane < kChunk && lane < U.L)
+        logit = __bfloat162float(P.beta[beta_base + (size_t)lane * P.H]);
+    for (int c = 0; c < U.nch; ++c) {
+        const int len = min(kChunk, U.L - c * kChunk);
+        const float bl = (lane < len) ? sigmoid_fast(logit) : 0.0f;   // b of row `lane`
+        if (c + 1 < U.nch && lane < kChunk && (c + 1) * kChunk + lane < U.L)
+            logit = __bfloat162float(P.beta[beta_base + (size_t)((c + 1) * kChunk + lane) * P.H]);
+        const int par = c & 1;
+        const bool ok = mbar_wait(&S.a_ready[par], (unsigned)((c >> 1) & 1), err);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        Stage& st = S.st[c % kRing];
+        // A_kk = diag(b) (sum of the warps' partials), strictly lower; A_qk inclusive
+        // lower (fp16, interleaved); partials summed in warp order
 #pragma unroll
-            for (int e = lane; e < kChunk * kChunk; e += 32) {
-                const int r = e >> 4, s = e & 15;
-                const float x = T.part[0][e] + T.part[1][e];
-                T.A[r * A_LD + s] = (s < r) ? T.beta[r] * x : 0.0f;
+        for (int e = 2 * lane; e < kChunk * kChunk; e += 64) {
+            const int r = e >> 4, s = e & 15;
+            float2 sk = make_float2(0.f, 0.f), sq = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < kProdWarps; ++w) {
+                const float2 pk2 = *reinterpret_cast<const float2*>(&PS.part[par][w][0][e]);
+                const float2 pq2 = *reinterpret_cast<const float2*>(&PS.part[par][w][1][e]);
+                sk.x += pk2.x;
+                sk.y += pk2.y;
+                sq.x += pq2.x;
+                sq.y += pq2.y;
             }
-            __syncwarp();
-            if (lane < kChunk) {
-                float Tc[kChunk];
+            const float br = __shfl_sync(0xffffffffu, bl, r);
+            PS.A[r * A_LD + s] = (s < r) ? br * sk.x : 0.0f;
+            PS.A[r * A_LD + s + 1] = (s + 1 < r) ? br * sk.y : 0.0f;
+            *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(st.aqk) +
+                                         tc::interleaved_offset(r, s, kChunk)) =
+                pack_half2((s <= r) ? sq.x : 0.0f, (s + 1 <= r) ? sq.y : 0.0f);
+        }
+        __syncwarp();
+        if (lane < kChunk) {
+            float Tc[kChunk];
 #pragma unroll
-                for (int i = 0; i < kChunk; ++i) {
-                    float s0 = 0.0f, s1 = 0.0f;
+            for (int i = 0; i < kChunk; ++i) {
+                float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-                    for (int m = 0; m + 1 < i; m += 2) {
-                        s0 = fmaf(T.A[i * A_LD + m], Tc[m], s0);
-                        s1 = fmaf(T.A[i * A_LD + m + 1], Tc[m + 1], s1);
-                    }
-                    if (i & 1) s0 = fmaf(T.A[i * A_LD + i - 1], Tc[i - 1], s0);
-                    Tc[i] = (i == lane) ? 1.0f : ((i < lane) ? 0.0f : -(s0 + s1));
+                for (int m = 0; m + 1 < i; m += 2) {
+                    s0 = fmaf(PS.A[i * A_LD + m], Tc[m], s0);
+                    s1 = fmaf(PS.A[i * A_LD + m + 1], Tc[m + 1], s1);
                 }
-                const float bj = T.beta[lane];
-                unsigned char* tbt = reinterpret_cast<unsigned char*>(st.tbt);
-#pragma unroll
-                for (int i = 0; i < kChunk; ++i) {
-                    const __half x = __float2half_rn(Tc[i] * bj);
-                    T.tb[i * TB_LD + lane] = x;
-                    *reinterpret_cast<__half*>(tbt + tc::interleaved_offset(i, lane, kChunk)) = x;
-                }
+                if (i & 1) s0 = fmaf(PS.A[i * A_LD + i - 1], Tc[i - 1], s0);
+                Tc[i] = (i == lane) ? 1.0f : ((i < lane) ? 0.0f : -(s0 + s1));
             }
-        } else if (warp == 1) {
-            // A_qk = sum of partials, inclusive lower, fp16 into the slot
+            unsigned char* tbt = reinterpret_cast<unsigned char*>(st.tbt);
 #pragma unroll
-            for (int e = 2 * lane; e < kChunk * kChunk; e += 64) {
-                const int r = e >> 4, s = e & 15;
-                float x0 = T.part[2][e] + T.part[3][e];
-                float x1 = T.part[2][e + 1] + T.part[3][e + 1];
-                x0 = (s <= r) ? x0 : 0.0f;
-                x1 = (s + 1 <= r) ? x1 : 0.0f;
-                *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(st.aqk) +
-                                             tc::interleaved_offset(r, s, kChunk)) =
-                    pack_half2(x0, x1);
+            for (int i = 0; i < kChunk; ++i) {
+                const __half x = __float2half_rn(Tc[i] * bl);
+                PS.tb[par][i * TB_LD + lane] = x;
+                *reinterpret_cast<__half*>(tbt + tc::interleaved_offset(i, lane, kChunk)) = x;
             }
         }
-        team_sync(team);
-
-        // ---- w = T diag(b)(K 2^G), stored negated as rows 0..15 of [-w; Q 2^G]:
-        //      warp w covers key channels 32w .. 32w+31
-        {
-            uint32_t ta[4];
-            ldsm_x4(ta, &T.tb[((lane & 7) + 8 * ((lane >> 3) & 1)) * TB_LD + 8 * (lane >> 4)]);
-            const int brow = (lane & 7) + 8 * ((lane >> 3) & 1);
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                const int np = 2 * warp + q2;
-                const int bcol = 16 * np + 8 * (lane >> 4);
-                uint32_t bk[4];
-                ldsm_x4_t(bk, &kg16[brow * RAW_LD + bcol]);
-                float cw0[4] = {}, cw1[4] = {};
-                mma_f16(cw0, ta, bk[0], bk[1]);
-                mma_f16(cw1, ta, bk[2], bk[3]);
-                const int col0 = 16 * np + 2 * ft, col1 = col0 + 8;
-                *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(fg, col0, 32)) =
-                    pack_half2(-cw0[0], -cw0[1]);
-                *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(fg + 8, col0, 32)) =
-                    pack_half2(-cw0[2], -cw0[3]);
-                *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(fg, col1, 32)) =
-                    pack_half2(-cw1[0], -cw1[1]);
-                *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(fg + 8, col1, 32)) =
-                    pack_half2(-cw1[2], -cw1[3]);
-            }
-        }
-        // generic-proxy writes of this thread -> visible to the tensor core
         tc::fence_proxy_async_smem();
-        // every thread publishes its own writes to the slot
-        mbar_arrive(&S.full[slot]);
+        __syncwarp();
+        mbar_arrive(&S.t_ready[par]);
     }
 }
 
@@ -626,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Problem P, SeqMap M,
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRing; ++s) {
-            mbar_init(&S.full[s], kTeamThreads);   // every thread of the producing team
+            mbar_init(&S.full[s], kProdThreads);   // every producer thread
             mbar_init(&S.empty[s], 1);             // one tensor-core commit
         }
         mbar_init(&S.uo_done, 1);
@@ -634,8 +579,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Problem P, SeqMap M,
         mbar_init(&S.s16_ready, kEpiWarps * 32);
         mbar_init(&S.u16_ready, kEpiWarps * 32);
         mbar_init(&S.epi_done, kEpiWarps * 32);
-        for (int t = 0; t < kTeams; ++t)
-            for (int b = 0; b < 2; ++b) mbar_init(&S.team[t].raw_full[b], 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&S.a_ready[b], kProdThreads);
+            mbar_init(&S.t_ready[b], 32);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     // rows 16..31 of every slot's T diag(b) operand stay zero
@@ -666,9 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Problem P, SeqMap M,
         (void)ok;
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
+    } else if (warp == kSolveWarp) {
+        solve(P, U, S, lane, err);
     } else {
-        const int pt = threadIdx.x - kProdWarp0 * 32;
-        produce(P, U, S, pt / kTeamThreads, pt % kTeamThreads, err);
+        produce(P, U, S, warp - kProdWarp0, lane, err);
     }
 }
 
