@@ -29,7 +29,8 @@ namespace kda {
 
 namespace {
 
-constexpr int kEpiWarps = 4;                // epilogue: one TMEM lane (value row) per thread
+constexpr int kEpiWarps = 8;                // epilogue: two warps per TMEM lane quarter,
+                                            // each owning half of the state's columns
 constexpr int kMmaWarp = kEpiWarps;         // issues the tcgen05 MMAs, owns tensor memory
 constexpr int kSolveWarp = kMmaWarp + 1;    // 16 x 16 inverse
 constexpr int kProdWarp0 = kSolveWarp + 1;
@@ -94,10 +95,10 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* b, unsigned pa
     unsigned ok;
     asm volatile(
         "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
+        : "r"(smem_u32(b)), "r"(parity), "r"(1000000u)   // may sleep up to 1 ms per try
         : "memory");
     return ok != 0;
 }
@@ -112,6 +113,26 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* b, unsigned parity
         }
     }
     return true;
+}
+// packed fp32 pair arithmetic (one instruction each on sm_100 and later)
+__device__ __forceinline__ float2 f2mul(float2 a, float2 b) {
+    unsigned long long x, y, z;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("mul.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(y));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(z));
+    return r;
+}
+__device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) {
+    unsigned long long x, y, w, z;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(w) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(z) : "l"(x), "l"(y), "l"(w));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(z));
+    return r;
 }
 // packed fp32 pair multiply (one instruction on sm_100 and later)
 __device__ __forceinline__ void mul2(float& a, float& b, float2 s) {
@@ -195,10 +216,12 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
                 for (int kk = 0; kk < 2; ++kk) {
                     const float2 gv = bf2_to_f2(X.g[i][kk]);
                     const bool valid = lg + 8 * i < len;
-                    const float s0 = rcp_approx(1.0f + ex2_approx(fmaf(gv.x, ga, gb[kk][0])));
-                    const float s1 = rcp_approx(1.0f + ex2_approx(fmaf(gv.y, ga, gb[kk][1])));
-                    G[i][kk][0] = valid ? lb2 * s0 : 0.0f;
-                    G[i][kk][1] = valid ? lb2 * s1 : 0.0f;
+                    const float2 xa = f2fma(gv, make_float2(ga, ga), make_float2(gb[kk][0], gb[kk][1]));
+                    const float2 sg = f2mul(make_float2(rcp_approx(1.0f + ex2_approx(xa.x)),
+                                                        rcp_approx(1.0f + ex2_approx(xa.y))),
+                                            make_float2(lb2, lb2));
+                    G[i][kk][0] = valid ? sg.x : 0.0f;
+                    G[i][kk][1] = valid ? sg.y : 0.0f;
                 }
             float glast[2][2];
 #pragma unroll
@@ -240,9 +263,11 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
                     const float2 kv = bf2_to_f2(X.k[i][kk]);
                     const float2 qv = bf2_to_f2(X.q[i][kk]);
                     const float2 vv = bf2_to_f2(X.v[i][kk]);
-                    const float kg0 = kv.x * e0, kg1 = kv.y * e1;
-                    const float ki0 = kv.x * d0, ki1 = kv.y * d1;
-                    const float qg0 = qv.x * e0, qg1 = qv.y * e1;
+                    const float2 kg = f2mul(kv, make_float2(e0, e1));
+                    const float2 ki = f2mul(kv, make_float2(d0, d1));
+                    const float2 qg = f2mul(qv, make_float2(e0, e1));
+                    const float2 kd = f2mul(ki, make_float2(gc0, gc1));
+                    const float kg0 = kg.x, kg1 = kg.y, ki0 = ki.x, ki1 = ki.y, qg0 = qg.x, qg1 = qg.y;
                     // tf32 fragments: A rows g / g+8 -> a0,a2 / a1,a3; B n-tile i
                     akf[kk][i] = to_tf32(kg0);
                     akf[kk][i + 2] = to_tf32(kg1);
@@ -260,9 +285,9 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
                     *reinterpret_cast<uint32_t*>(&kgt[r * KG_LD + 8 * kk + 2 * lt]) =
                         pack_half2(kg0, kg1);
                     *reinterpret_cast<__half*>(kdt + tc::interleaved16_offset(p, r, T_SBO)) =
-                        __float2half_rn(ki0 * gc0);
+                        __float2half_rn(kd.x);
                     *reinterpret_cast<__half*>(kdt + tc::interleaved16_offset(p + 1, r, T_SBO)) =
-                        __float2half_rn(ki1 * gc1);
+                        __float2half_rn(kd.y);
                     *reinterpret_cast<__half*>(vt + tc::interleaved16_offset(p, r, T_SBO)) =
                         __float2half_rn(vv.x);
                     *reinterpret_cast<__half*>(vt + tc::interleaved16_offset(p + 1, r, T_SBO)) =
@@ -434,42 +459,62 @@ __device__ __forceinline__ void state_out(const Problem& P, size_t idx, float x)
         static_cast<__nv_bfloat16*>(P.final_state)[idx] = __float2bfloat16_rn(x);
 }
 
-// ---- sequential stage: epilogue (thread v owns TMEM lane v = value channel v) --------
-// Keeps the fp32 state S^T in tensor memory: after each state update it writes
-// the fp16 copy that the next chunk's MMAs read and pre-scales the fp32 state
-// by the next chunk's 2^G_last; converts U^T to fp16 for the update MMA; and
-// writes the chunk's outputs.
+// ---- sequential stage: epilogue ---------------------------------------------------
+// Warp ew reaches TMEM lanes 32 (ew % 4) .. + 31 (thread = value channel v) and
+// owns half of the state's columns: key channels 64 (ew / 4) .. + 63, U columns
+// (tokens) 8 (ew / 4) .. + 7 and the outputs of those tokens.  After each state
+// update it first writes the fp16 copy that the next chunk's MMAs read (the
+// critical path), then pre-scales the fp32 state by the next chunk's 2^G_last.
+__device__ __forceinline__ void scale32(uint32_t (&x)[32], const float* gc) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+        const float4 g4 = *reinterpret_cast<const float4*>(gc + i);
+        const float2 a = f2mul(make_float2(__uint_as_float(x[i]), __uint_as_float(x[i + 1])),
+                               make_float2(g4.x, g4.y));
+        const float2 b = f2mul(make_float2(__uint_as_float(x[i + 2]), __uint_as_float(x[i + 3])),
+                               make_float2(g4.z, g4.w));
+        x[i] = __float_as_uint(a.x);
+        x[i + 1] = __float_as_uint(a.y);
+        x[i + 2] = __float_as_uint(b.x);
+        x[i + 3] = __float_as_uint(b.y);
+    }
+}
+__device__ __forceinline__ void pack32(const uint32_t (&x)[32], uint32_t (&h)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        h[i] = pack_half2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+}
+
 __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem, int ew,
                          int lane, int* err) {
-    const int v = 32 * ew + lane;
-    const uint32_t tl = tmem + ((uint32_t)(32 * ew) << 16);   // this warp's lane quarter
+    const int quarter = ew & 3, colhalf = ew >> 2;
+    const int v = 32 * quarter + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);   // this warp's lane quarter
     const size_t sbase = ((size_t)U.n * P.H + U.h) * kDim * kDim + v;   // + c * kDim
+    const int p0 = 2 * colhalf;   // this warp's two 32-column pieces: p0, p0 + 1
     bool ok = true;
 
     if (U.nch == 0) {   // no tokens: the final state is the initial state
         if (P.final_state)
-            for (int c = 0; c < kDim; ++c)
-                state_out(P, sbase + (size_t)c * kDim, P.init_state ? state_in(P, sbase + (size_t)c * kDim) : 0.0f);
+            for (int c = 64 * colhalf; c < 64 * colhalf + 64; ++c)
+                state_out(P, sbase + (size_t)c * kDim,
+                          P.init_state ? state_in(P, sbase + (size_t)c * kDim) : 0.0f);
         return;
     }
     // initial state: S16 = fp16(S0), S32 = S0 Diag(2^G_last of chunk 0)
     ok = mbar_wait(&S.full[0], 0u, err);
     if (!__all_sync(0xffffffffu, ok)) return;
 #pragma unroll 1
-    for (int piece = 0; piece < 4; ++piece) {
+    for (int piece = p0; piece < p0 + 2; ++piece) {
         uint32_t x[32], h[16];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const int c = 32 * piece + i;
             x[i] = __float_as_uint(P.init_state ? state_in(P, sbase + (size_t)c * kDim) : 0.0f);
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            h[i] = pack_half2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
-        const float* gc = S.st[0].gc + 32 * piece;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * gc[i]);
+        pack32(x, h);
         tc::st16(tl + TM_S16 + 16 * piece, h);
+        scale32(x, S.st[0].gc + 32 * piece);
         tc::st32(tl + TM_S32 + 32 * piece, x);
     }
     tc::wait_st();
@@ -478,62 +523,64 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
 
     for (int c = 0; c < U.nch; ++c) {
         const uint32_t uo = tl + TM_UO + 32u * (c & 1);
-        // U^T -> fp16 A operand of the update
+        // U^T (this warp's 8 token columns) -> fp16 A operand of the update
         ok = mbar_wait(&S.uo_done, (unsigned)(c & 1), err);
         if (!__all_sync(0xffffffffu, ok)) return;
         tc::fence_after_sync();
         {
             uint32_t u[16], h[8];
-            tc::ld16(uo, u);
+            tc::ld16(uo, u);   // all 16 columns (one instruction); this warp converts its half
             tc::wait_ld();
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 h[i] = pack_half2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
-            tc::st8(tl + TM_U16, h);
+            if (colhalf == 0) tc::st8(tl + TM_U16, h);
             tc::wait_st();
         }
         tc::fence_before_sync();
         mbar_arrive(&S.u16_ready);
 
-        // state update done: fp16 copy + rescale for the next chunk (or the final state)
+        // state update done: fp16 copy first (next chunk's MMAs wait on it) ...
         ok = mbar_wait(&S.s_done, (unsigned)(c & 1), err);
         const bool more = c + 1 < U.nch;
         const int nslot = (c + 1) % kRing;
         if (more) ok = ok && mbar_wait(&S.full[nslot], (unsigned)(((c + 1) / kRing) & 1), err);
         if (!__all_sync(0xffffffffu, ok)) return;
         tc::fence_after_sync();
+        if (more) {
 #pragma unroll 1
-        for (int piece = 0; piece < 4; ++piece) {
-            uint32_t x[32];
-            tc::ld32(tl + TM_S32 + 32 * piece, x);
-            tc::wait_ld();
-            if (more) {
-                uint32_t h[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    h[i] = pack_half2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+            for (int piece = p0; piece < p0 + 2; ++piece) {
+                uint32_t x[32], h[16];
+                tc::ld32(tl + TM_S32 + 32 * piece, x);
+                tc::wait_ld();
+                pack32(x, h);
                 tc::st16(tl + TM_S16 + 16 * piece, h);
-                const float* gc = S.st[nslot].gc + 32 * piece;
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float a = __uint_as_float(x[i]), b = __uint_as_float(x[i + 1]);
-                    mul2(a, b, make_float2(gc[i], gc[i + 1]));
-                    x[i] = __float_as_uint(a);
-                    x[i + 1] = __float_as_uint(b);
-                }
+            }
+            tc::wait_st();
+            tc::fence_before_sync();
+            mbar_arrive(&S.s16_ready);
+            // ... then the rescale, finished before this warp's next U^T arrive (which
+            // the next state update waits for)
+#pragma unroll 1
+            for (int piece = p0; piece < p0 + 2; ++piece) {
+                uint32_t x[32];
+                tc::ld32(tl + TM_S32 + 32 * piece, x);
+                tc::wait_ld();
+                scale32(x, S.st[nslot].gc + 32 * piece);
                 tc::st32(tl + TM_S32 + 32 * piece, x);
-            } else if (P.final_state) {
+            }
+        } else if (P.final_state) {
+#pragma unroll 1
+            for (int piece = p0; piece < p0 + 2; ++piece) {
+                uint32_t x[32];
+                tc::ld32(tl + TM_S32 + 32 * piece, x);
+                tc::wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     state_out(P, sbase + (size_t)(32 * piece + i) * kDim, __uint_as_float(x[i]));
             }
         }
-        if (more) {
-            tc::wait_st();
-            tc::fence_before_sync();
-            mbar_arrive(&S.s16_ready);
-        }
-        // outputs of chunk c: O^T lane v, column t
+        // outputs of chunk c, tokens 8 colhalf .. + 7: O^T lane v, column t
         {
             uint32_t o[16];
             tc::ld16(uo + 16, o);
@@ -541,8 +588,12 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
             const int len = min(kChunk, U.L - c * kChunk);
             __nv_bfloat16* out = P.out + ((size_t)(U.tok_start + c * kChunk) * P.H + U.h) * kDim + v;
 #pragma unroll
-            for (int t = 0; t < kChunk; ++t)
-                if (t < len) out[(size_t)t * P.H * kDim] = __float2bfloat16_rn(P.scale * __uint_as_float(o[t]));
+            for (int j = 0; j < 8; ++j) {
+                const int t = 8 * colhalf + j;
+                const uint32_t ov = colhalf ? o[8 + j] : o[j];
+                if (t < len)
+                    out[(size_t)t * P.H * kDim] = __float2bfloat16_rn(P.scale * __uint_as_float(ov));
+            }
         }
     }
 }
