@@ -14,6 +14,7 @@ import ctypes
 import os
 
 __all__ = ["KdaError", "kda_fwd", "kda_fwd_host", "kda_fwd_noalloc", "kda_fwd_get_error", "kda_status_string",
+           "kda_last_cuda_error",
            "kda_fwd_workspace_bytes", "kda_profile_enable", "kda_profile_read",
            "kda_kernel_name", "lib_path", "load_library", "KDA_BF16", "KDA_F32",
            "KERNEL_NAMES"]
@@ -33,7 +34,12 @@ _vp = ctypes.c_void_p
 class KdaError(RuntimeError):
     def __init__(self, status: int, where: str = "kda_fwd"):
         self.status = status
-        super().__init__(f"{where} failed: {kda_status_string(status)} ({status})")
+        self.cuda_error = 0
+        msg = f"{where} failed: {kda_status_string(status)} ({status})"
+        if status in (-6, -10, -11):   # KDA_ERR_LAUNCH, KDA_ERR_ALLOC, KDA_ERR_CUDA
+            self.cuda_error = kda_last_cuda_error()
+            msg += f"; cudaError_t {self.cuda_error}"
+        super().__init__(msg)
 
 
 def lib_path() -> str:
@@ -60,6 +66,8 @@ def load_library():
     lib.kda_fwd_noalloc.restype = ctypes.c_int
     lib.kda_fwd_get_error.argtypes = [_vp]
     lib.kda_fwd_get_error.restype = ctypes.c_int
+    lib.kda_last_cuda_error.argtypes = []
+    lib.kda_last_cuda_error.restype = ctypes.c_int
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_fwd_workspace_bytes.argtypes = [ctypes.c_int] * 5
@@ -77,6 +85,11 @@ def load_library():
 
 def kda_status_string(status: int) -> str:
     return load_library().kda_status_string(int(status)).decode()
+
+
+def kda_last_cuda_error() -> int:
+    """cudaError_t value behind the calling thread's last LAUNCH / ALLOC / CUDA status."""
+    return int(load_library().kda_last_cuda_error())
 
 
 def kda_kernel_name(kernel_id: int) -> str:

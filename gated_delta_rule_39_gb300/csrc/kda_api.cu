@@ -11,6 +11,15 @@
 namespace kda {
 namespace {
 
+// cudaError_t behind the calling thread's most recent KDA_ERR_LAUNCH / ALLOC / CUDA
+thread_local int t_last_cuda_error = 0;
+// record a CUDA failure, clear the runtime's (non-sticky) last error, pass `status` on
+int cuda_fail(int status, cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    cudaGetLastError();
+    return status;
+}
+
 // Device-side error word (one per device: every device that loads the module
 // holds its own instance).  Kernels receive its address.
 __device__ int g_error_word;
@@ -28,18 +37,20 @@ std::mutex g_dev_mu;
 
 int device_setup(int* dev_out, int** err_out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(KDA_ERR_CUDA, e);
+    if (dev < 0 || dev >= kMaxDevices) return cuda_fail(KDA_ERR_CUDA, cudaErrorInvalidDevice);
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DeviceInfo& d = g_dev[dev];
     if (!d.ready) {
         int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-            return KDA_ERR_CUDA;
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return cuda_fail(KDA_ERR_CUDA, e);
         d.arch_ok = (major == 10 && minor == 3);
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return KDA_ERR_CUDA;
+        e = cudaGetSymbolAddress(&p, g_error_word);
+        if (e != cudaSuccess) return cuda_fail(KDA_ERR_CUDA, e);
         d.err = static_cast<int*>(p);
         // keep freed scratch in the device's default pool instead of returning
         // it to the driver at every synchronisation
@@ -173,10 +184,9 @@ int noalloc_scratch(int dev, int** addr) {
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (g_noalloc_addr[dev] == nullptr) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return KDA_ERR_CUDA;
-        }
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return kda::cuda_fail(KDA_ERR_CUDA, e != cudaSuccess ? e : cudaErrorInvalidSymbol);
         g_noalloc_addr[dev] = static_cast<int*>(p);
     }
     *addr = g_noalloc_addr[dev];
@@ -236,10 +246,8 @@ int kda_fwd(const void* q, const void* k, const void* v, const void* g, const vo
 
     int* scratch = nullptr;
     if (bytes > 0) {
-        if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), bytes, s) != cudaSuccess) {
-            cudaGetLastError();
-            return KDA_ERR_ALLOC;
-        }
+        const cudaError_t ea = cudaMallocAsync(reinterpret_cast<void**>(&scratch), bytes, s);
+        if (ea != cudaSuccess) return cuda_fail(KDA_ERR_ALLOC, ea);
     }
     Problem P;
     P.q = static_cast<const __nv_bfloat16*>(q);
@@ -272,10 +280,7 @@ int kda_fwd(const void* q, const void* k, const void* v, const void* g, const vo
     if (e == cudaSuccess)
         e = timed_launch(KDA_KERNEL_FUSED, s, [&] { return launch_fused(P, M, err, s); });
     if (scratch) cudaFreeAsync(scratch, s);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return KDA_ERR_LAUNCH;
-    }
+    if (e != cudaSuccess) return cuda_fail(KDA_ERR_LAUNCH, e);
     return KDA_OK;
 }
 
@@ -284,11 +289,14 @@ int kda_fwd_get_error(void* stream) {
     int* err = nullptr;
     int rc = device_setup(&dev, &err);
     if (rc == KDA_ERR_CUDA) return rc;
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(KDA_ERR_CUDA, e);
     int word = 0;
-    if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(KDA_ERR_CUDA, e);
     const int zero = 0;
-    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(KDA_ERR_CUDA, e);
     return word;
 }
 
@@ -326,10 +334,8 @@ int kda_fwd_host(const void* q, const void* k, const void* v, const void* g, con
         total += align_up(sizes[i]);
     }
     unsigned char* d = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void**>(&d), total, s) != cudaSuccess) {
-        cudaGetLastError();
-        return KDA_ERR_ALLOC;
-    }
+    const cudaError_t ea = cudaMallocAsync(reinterpret_cast<void**>(&d), total, s);
+    if (ea != cudaSuccess) return cuda_fail(KDA_ERR_ALLOC, ea);
     const void* hsrc[] = {q, k, v, g, beta, nullptr, A_log, dt_bias, initial_state, nullptr,
                           cu_seqlens};
     cudaError_t e = cudaSuccess;
@@ -350,12 +356,10 @@ int kda_fwd_host(const void* q, const void* k, const void* v, const void* g, con
             e = cudaMemcpyAsync(final_state, d + offs[9], b_s1, cudaMemcpyDeviceToHost, s);
     }
     cudaFreeAsync(d, s);
-    if (cudaStreamSynchronize(s) != cudaSuccess) e = cudaErrorUnknown;
+    const cudaError_t es = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = es;
     if (rc != KDA_OK) return rc;
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return KDA_ERR_CUDA;
-    }
+    if (e != cudaSuccess) return cuda_fail(KDA_ERR_CUDA, e);
     return KDA_OK;
 }
 
@@ -409,10 +413,7 @@ int kda_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
     cudaError_t e = cudaSuccess;
     if (varlen) e = launch_seqmap(P, M, err, s);
     if (e == cudaSuccess) e = launch_fused(P, M, err, s);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return KDA_ERR_LAUNCH;
-    }
+    if (e != cudaSuccess) return cuda_fail(KDA_ERR_LAUNCH, e);
     return KDA_OK;
 }
 
@@ -439,10 +440,10 @@ int kda_profile_read(double* total_ms, long long* launches) {
     int rc = KDA_OK;
     for (auto& r : g_prof.pending) {
         float ms = 0.0f;
-        if (cudaEventSynchronize(r.stop) != cudaSuccess ||
-            cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) {
-            cudaGetLastError();
-            rc = KDA_ERR_CUDA;
+        cudaError_t e = cudaEventSynchronize(r.stop);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
+        if (e != cudaSuccess) {
+            rc = cuda_fail(KDA_ERR_CUDA, e);
         } else {
             g_prof.total_ms[r.kernel] += ms;
             g_prof.launches[r.kernel] += 1;
@@ -457,6 +458,8 @@ int kda_profile_read(double* total_ms, long long* launches) {
     }
     return rc;
 }
+
+int kda_last_cuda_error(void) { return t_last_cuda_error; }
 
 const char* kda_kernel_name(int kernel_id) {
     switch (kernel_id) {

@@ -132,6 +132,12 @@ int kda_fwd_get_error(void* stream);
 /* Human-readable name of a kda_status value (static string, never NULL). */
 const char* kda_status_string(int status);
 
+/* The cudaError_t value (as an int) of the CUDA runtime failure behind the most
+ * recent KDA_ERR_LAUNCH, KDA_ERR_ALLOC or KDA_ERR_CUDA returned to the calling
+ * host thread (cudaGetErrorString gives its text); 0 if there was none.
+ * Successful calls leave it unchanged.  Host-only, no CUDA call. */
+int kda_last_cuda_error(void);
+
 /* Bytes of scratch memory kda_fwd takes from the stream-ordered allocator for
  * the given problem (0 for an empty problem).  Host-only, no CUDA call. */
 size_t kda_fwd_workspace_bytes(int B, int T, int H, int num_seqs, int varlen);

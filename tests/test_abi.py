@@ -119,3 +119,26 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(kda, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         kda.load_library()
+
+
+def test_last_cuda_error_reports_missing_device():
+    """With every GPU hidden, a well-formed call fails in the CUDA runtime before any
+    launch: KDA_ERR_CUDA, and kda_last_cuda_error names the runtime's error."""
+    code = (
+        "import ctypes, test_abi as t\n"
+        "import gated_delta_rule_39_gb300 as kda\n"
+        "lib = kda.load_library()\n"
+        "assert kda.kda_last_cuda_error() == 0\n"
+        "rc = t._call(lib)\n"
+        "print(rc, kda.kda_last_cuda_error())\n"
+    )
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="",
+               PYTHONPATH=os.pathsep.join([ROOT, os.path.join(ROOT, "tests")]))
+    from gated_delta_rule_39_gb300 import _build
+    _build.build()
+    r = subprocess.run(["python", "-c", code], capture_output=True, text=True, env=env,
+                       cwd=ROOT, timeout=120)
+    assert r.returncode == 0, r.stderr
+    rc, cuda_err = map(int, r.stdout.split())
+    assert rc == -11            # KDA_ERR_CUDA
+    assert cuda_err != 0        # cudaErrorNoDevice (or another "no device" code)
