@@ -22,6 +22,12 @@
 // stages into two kernels on Hopper because the sequential stage alone left
 // SMs idle; here the split stays, but inside one CTA, so the intermediate
 // factors never leave the SM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "kda_internal.cuh"
 #include "kda_tcgen05.cuh"
 
@@ -36,33 +42,44 @@ constexpr int kSolveWarp = kMmaWarp + 1;    // 16 x 16 inverse
 constexpr int kProdWarp0 = kSolveWarp + 1;
 constexpr int kProdWarps = 8;               // 16 key channels each
 constexpr int kProdThreads = kProdWarps * 32;
-constexpr int kRing = 6;                    // chunk-operand slots
-constexpr int kThreads = (kProdWarp0 + kProdWarps) * 32;
+constexpr int kLoadWarp = kProdWarp0 + kProdWarps;   // TMA loads of the raw rows (one lane)
+constexpr int kRing = 3;                    // chunk-operand slots
+constexpr int kRaw = 4;                     // raw-row slots: chunks in flight from HBM
+constexpr int kThreads = (kLoadWarp + 1) * 32;
 
 constexpr int A_LD = 17;
 constexpr int TB_LD = 24;     // fp16 per row of T diag(b) (48 B: ldmatrix conflict-free)
 constexpr int KG_LD = 24;     // fp16 per row of a warp's K 2^G tile (48 B)
-constexpr int T_SBO = 272;    // byte step between 8-row groups of the transposed 128 x 16
-                              // tiles (16 bytes past 256 spreads row groups over banks)
+constexpr int T_SBO = 272;    // byte step between 8-row groups of the transposed fp16
+                              // 128 x 16 tile (16 bytes past 256 spreads row groups over banks)
+constexpr int KD_SBO = 512;   // byte step between 8-row groups of the fp32 128 x 16 tile
+constexpr int AQ_SBO = 512;   // same for the fp32 16 x 16 A_qk tile
 
 // tensor-memory columns (one allocation of 512)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_S32 = 0;     // S^T, fp32, 128 columns
-constexpr uint32_t TM_S16 = 128;   // S^T as the fp16 A operand, 64 columns
-constexpr uint32_t TM_UO = 192;    // [U | O] accumulators, 2 buffers x 32 columns
-constexpr uint32_t TM_U16 = 256;   // U^T as the fp16 A operand, 8 columns
+constexpr uint32_t TM_S = 0;       // S^T, fp32: two buffers of 128 columns (chunk parity)
+constexpr uint32_t TM_UO = 256;    // [U | O] accumulators: three buffers of 32 columns
 
-// One chunk's operands for the tensor-core recurrence (canonical K-major layouts)
+// One chunk's operands for the tensor-core recurrence (canonical K-major layouts).
+// The operands multiplied by the fp32 state or by U are fp32 values rounded to
+// tf32 (kind::tf32 MMAs read the state and U straight from tensor memory).
 struct Stage {
-    __half buo[2 * 32 * 64];       // B of [U|O] += S^T [-w; Q 2^G]^T: 32 x 128, 128B swizzle
+    float buo[4 * 32 * 32];        // B of [U|O] += S^T [-w; Q 2^G]^T: 32 x 128, 128B swizzle
+    float kdt[16 * KD_SBO / 4];    // B of the state update: (K 2^(G_last-G))^T 128 x 16
+    float aqk[2 * AQ_SBO / 4];     // B of O += U A_qk^T: A_qk 16 x 16
     __half vt[16 * T_SBO / 2];     // A of u^T = V^T (T diag b)^T: V^T 128 x 16, interleaved
-    __half kdt[16 * T_SBO / 2];    // B of the state update: (K 2^(G_last-G))^T 128 x 16
     __half tbt[32 * 16];           // B of the u MMA: rows 0-15 T diag(b), rows 16-31 zero
-    __half aqk[16 * 16];           // B of O += U A_qk^T: A_qk 16 x 16
     float gc[kDim];                // 2^G_last
-    unsigned char pad_[512];       // keep sizeof(Stage) a multiple of 1024
+    unsigned char pad_[1280];      // keep sizeof(Stage) a multiple of 1024
 };
 static_assert(sizeof(Stage) % 1024 == 0, "stages keep the swizzled tiles 1024-byte aligned");
+// One chunk's raw rows of q, k, v, g as the TMA engine writes them: per tensor two
+// boxes of 16 rows x 64 channels (128 bytes per row, 128-byte swizzle).
+struct RawSlot {
+    __nv_bfloat16 x[4][2][kChunk * 64];
+};
+constexpr uint32_t kRawBytes = sizeof(RawSlot);
+static_assert(kRawBytes == 16384, "four tensors x 16 rows x 256 bytes");
 struct ProdShared {
     float part[2][kProdWarps][2][kChunk * kChunk]; // [chunk parity][warp][A_kk, A_qk] partials
     __half tb[2][kChunk * TB_LD];                  // T diag(b) per chunk parity
@@ -71,15 +88,18 @@ struct ProdShared {
 };
 struct Smem {
     Stage st[kRing];
+    RawSlot raw[kRaw];
     ProdShared pr;
+    unsigned long long raw_full[kRaw];   // TMA bytes landed
+    unsigned long long raw_empty[kRaw];  // producers have read the slot
     unsigned long long full[kRing];    // producers -> MMA / epilogue
     unsigned long long empty[kRing];   // MMA commit -> producers
     unsigned long long a_ready[2];     // producers' partial A_kk / A_qk summed
     unsigned long long t_ready[2];     // solver: T diag(b), A_qk written
     unsigned long long uo_done;        // U|O MMAs complete
     unsigned long long s_done;         // state update + O MMAs complete
-    unsigned long long s16_ready;      // epilogue: S^T fp16 copy written, S^T rescaled
-    unsigned long long u16_ready;      // epilogue: U^T fp16 copy written
+    unsigned long long init_ready;     // epilogue: initial state written
+    unsigned long long scaled;         // epilogue: 2^G_last S^T written to the other buffer
     unsigned long long epi_done;       // epilogue finished with tensor memory
     uint32_t tmem_base;
 };
@@ -134,14 +154,6 @@ __device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(z));
     return r;
 }
-// packed fp32 pair multiply (one instruction on sm_100 and later)
-__device__ __forceinline__ void mul2(float& a, float& b, float2 s) {
-    unsigned long long x, y, z;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(s.x), "f"(s.y));
-    asm("mul.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(y));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(z));
-}
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t raw) {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&raw);
     return __bfloat1622float2(v);
@@ -152,6 +164,40 @@ struct Unit {
     int n, h, tok_start, L, nch;
 };
 
+// ---- raw-row loads on the TMA engine (one thread) ----------------------------------
+// Tensor maps over q, k, v, g viewed as [rows][H][128] bf16 (rows = B*T tokens).
+// Rows past the end of the tensor are zero-filled; rows past the end of a
+// sequence belong to the next one and are masked by the producers.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];\n"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar)
+        : "memory");
+}
+
+__device__ void loader(const RawMaps& TM, const Unit& U, Smem& S, int* err) {
+    const CUtensorMap* maps[4] = {&TM.q, &TM.k, &TM.v, &TM.g};
+    for (int c = 0; c < U.nch; ++c) {
+        const int slot = c % kRaw;
+        if (c >= kRaw && !mbar_wait(&S.raw_empty[slot], (unsigned)(((c / kRaw) - 1) & 1), err))
+            break;
+        const uint32_t full = smem_u32(&S.raw_full[slot]);
+        tc::mbar_arrive_expect_tx(full, kRawBytes);
+        const int row = U.tok_start + c * kChunk;
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+                tma_load_3d(smem_u32(S.raw[slot].x[t][half]), maps[t], 64 * half, U.h, row, full);
+    }
+    // do not let the CTA exit while copies it issued are still landing
+    const int first = U.nch > kRaw ? U.nch - kRaw : 0;
+    for (int c = first; c < U.nch; ++c)
+        if (!mbar_wait(&S.raw_full[c % kRaw], (unsigned)((c / kRaw) & 1), err)) break;
+}
+
 // ---- token-parallel stage: producer warp w, channels 16w .. 16w+15 ----------------
 // Lane (g, t) = (lane >> 2, lane & 3) holds rows g and g+8 of the chunk for the
 // channel pairs p = 16w + 8kk + 2t, p+1 (kk = 0, 1).  In the tf32 MMA fragments
@@ -161,21 +207,26 @@ struct RawSlice {
     uint32_t q[2][2], k[2][2], v[2][2], g[2][2];   // [row g / g+8][kk] bf16 pairs
 };
 
-__device__ __forceinline__ void load_slice(const Problem& P, const Unit& U, int c, int cbase,
-                                           int lg, int lt, RawSlice& X) {
-    const int len = min(kChunk, U.L - c * kChunk);
+__device__ __forceinline__ void lds_slice(const RawSlot& R, int w, int lg, int lt, int len,
+                                          RawSlice& X) {
+    const int half = w >> 2;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int r = lg + 8 * i;
         const bool ok = r < len;
-        const size_t row = ((size_t)(U.tok_start + c * kChunk + (ok ? r : 0)) * P.H + U.h) * kDim;
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
-            const size_t o = row + cbase + 8 * kk + 2 * lt;
-            X.q[i][kk] = ok ? __ldg(reinterpret_cast<const unsigned int*>(P.q + o)) : 0u;
-            X.k[i][kk] = ok ? __ldg(reinterpret_cast<const unsigned int*>(P.k + o)) : 0u;
-            X.v[i][kk] = ok ? __ldg(reinterpret_cast<const unsigned int*>(P.v + o)) : 0u;
-            X.g[i][kk] = ok ? __ldg(reinterpret_cast<const unsigned int*>(P.g + o)) : 0u;
+            const int chunk16 = 2 * (w & 3) + kk;   // 16-byte chunk of the 128-byte row
+            const int off = r * 128 + ((chunk16 ^ (r & 7)) << 4) + 4 * lt;
+            const auto ld = [&](int t) {
+                return ok ? *reinterpret_cast<const uint32_t*>(
+                                reinterpret_cast<const unsigned char*>(R.x[t][half]) + off)
+                          : 0u;
+            };
+            X.q[i][kk] = ld(0);
+            X.k[i][kk] = ld(1);
+            X.v[i][kk] = ld(2);
+            X.g[i][kk] = ld(3);
         }
     }
 }
@@ -193,18 +244,18 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
     const float lb2 = P.lower_bound * kLog2e;
     ProdShared& PS = S.pr;
 
-    RawSlice nxt;
-    if (U.nch > 0) load_slice(P, U, 0, cbase, lg, lt, nxt);
-
     for (int c = 0; c <= U.nch; ++c) {
         if (c < U.nch) {
-            const RawSlice X = nxt;
-            if (c + 1 < U.nch) load_slice(P, U, c + 1, cbase, lg, lt, nxt);
             const int len = min(kChunk, U.L - c * kChunk);
+            const int rslot = c % kRaw;
+            bool ok = mbar_wait(&S.raw_full[rslot], (unsigned)((c / kRaw) & 1), err);
+            if (!__all_sync(0xffffffffu, ok)) return;
+            RawSlice X;
+            lds_slice(S.raw[rslot], w, lg, lt, len, X);
+            mbar_arrive(&S.raw_empty[rslot]);   // release: the reads above come first
             const int slot = c % kRing;
             Stage& st = S.st[slot];
             const int par = c & 1;
-            bool ok = true;
             if (c >= kRing) ok = mbar_wait(&S.empty[slot], (unsigned)(((c / kRing) - 1) & 1), err);
             if (!__all_sync(0xffffffffu, ok)) return;
 
@@ -280,14 +331,14 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
                         bf1[kk][0] = to_tf32(ki0);
                         bf1[kk][1] = to_tf32(ki1);
                     }
-                    *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(16 + r, p, 32)) =
-                        pack_half2(qg0, qg1);
+                    *reinterpret_cast<float2*>(buo + tc::swizzled32_offset(16 + r, p, 32)) =
+                        make_float2(__uint_as_float(aqf[kk][i]), __uint_as_float(aqf[kk][i + 2]));
                     *reinterpret_cast<uint32_t*>(&kgt[r * KG_LD + 8 * kk + 2 * lt]) =
                         pack_half2(kg0, kg1);
-                    *reinterpret_cast<__half*>(kdt + tc::interleaved16_offset(p, r, T_SBO)) =
-                        __float2half_rn(kd.x);
-                    *reinterpret_cast<__half*>(kdt + tc::interleaved16_offset(p + 1, r, T_SBO)) =
-                        __float2half_rn(kd.y);
+                    *reinterpret_cast<float*>(kdt + tc::interleaved32_offset(p, r, KD_SBO)) =
+                        tf32_round(kd.x);
+                    *reinterpret_cast<float*>(kdt + tc::interleaved32_offset(p + 1, r, KD_SBO)) =
+                        tf32_round(kd.y);
                     *reinterpret_cast<__half*>(vt + tc::interleaved16_offset(p, r, T_SBO)) =
                         __float2half_rn(vv.x);
                     *reinterpret_cast<__half*>(vt + tc::interleaved16_offset(p + 1, r, T_SBO)) =
@@ -332,10 +383,14 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
             mma_f16(cw0, ta, b[0], b[1]);
             mma_f16(cw1, ta, b[2], b[3]);
             const int col0 = cbase + 2 * lt, col1 = col0 + 8;
-            *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(lg, col0, 32)) = pack_half2(-cw0[0], -cw0[1]);
-            *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(lg + 8, col0, 32)) = pack_half2(-cw0[2], -cw0[3]);
-            *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(lg, col1, 32)) = pack_half2(-cw1[0], -cw1[1]);
-            *reinterpret_cast<uint32_t*>(buo + tc::swizzled_offset(lg + 8, col1, 32)) = pack_half2(-cw1[2], -cw1[3]);
+            *reinterpret_cast<float2*>(buo + tc::swizzled32_offset(lg, col0, 32)) =
+                make_float2(tf32_round(-cw0[0]), tf32_round(-cw0[1]));
+            *reinterpret_cast<float2*>(buo + tc::swizzled32_offset(lg + 8, col0, 32)) =
+                make_float2(tf32_round(-cw0[2]), tf32_round(-cw0[3]));
+            *reinterpret_cast<float2*>(buo + tc::swizzled32_offset(lg, col1, 32)) =
+                make_float2(tf32_round(-cw1[0]), tf32_round(-cw1[1]));
+            *reinterpret_cast<float2*>(buo + tc::swizzled32_offset(lg + 8, col1, 32)) =
+                make_float2(tf32_round(-cw1[2]), tf32_round(-cw1[3]));
             // generic-proxy writes of this thread -> visible to the tensor core
             tc::fence_proxy_async_smem();
             mbar_arrive(&S.full[cp % kRing]);
@@ -346,21 +401,31 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
 // ---- solver warp: (I + A_kk)^-1, T diag(b), A_qk for every chunk ------------------
 __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* err) {
     ProdShared& PS = S.pr;
-    const size_t beta_base = (size_t)U.tok_start * P.H + U.h;
-    float logit = 0.0f;
-    if (U.nch > 0 && lane < kChunk && lane < U.L)
-        logit = __bfloat162float(P.beta[beta_base + (size_t)lane * P.H]);
+    // beta logits in windows of 64 tokens (4 chunks), the next window loaded one
+    // window ahead: lane i holds tokens 64 j + i and 64 j + 32 + i of window j
+    const __nv_bfloat16* beta = P.beta + (size_t)U.tok_start * P.H + U.h;
+    const auto load_window = [&](int j, float& w0, float& w1) {
+        const int t0 = 64 * j + lane, t1 = t0 + 32;
+        w0 = (t0 < U.L) ? __bfloat162float(beta[(size_t)t0 * P.H]) : 0.0f;
+        w1 = (t1 < U.L) ? __bfloat162float(beta[(size_t)t1 * P.H]) : 0.0f;
+    };
+    float bw0 = 0.0f, bw1 = 0.0f, nb0 = 0.0f, nb1 = 0.0f;
+    if (U.nch > 0) load_window(0, nb0, nb1);
     for (int c = 0; c < U.nch; ++c) {
         const int len = min(kChunk, U.L - c * kChunk);
-        const float bl = (lane < len) ? sigmoid_fast(logit) : 0.0f;   // b of row `lane`
-        if (c + 1 < U.nch && lane < kChunk && (c + 1) * kChunk + lane < U.L)
-            logit = __bfloat162float(P.beta[beta_base + (size_t)((c + 1) * kChunk + lane) * P.H]);
+        if ((c & 3) == 0) {
+            bw0 = nb0;
+            bw1 = nb1;
+            if (64 * (c / 4 + 1) < U.L) load_window(c / 4 + 1, nb0, nb1);
+        }
+        const float lw = __shfl_sync(0xffffffffu, (c & 2) ? bw1 : bw0, 16 * (c & 1) + (lane & 15));
+        const float bl = (lane < len) ? sigmoid_fast(lw) : 0.0f;   // b of row `lane`
         const int par = c & 1;
         const bool ok = mbar_wait(&S.a_ready[par], (unsigned)((c >> 1) & 1), err);
         if (!__all_sync(0xffffffffu, ok)) return;
         Stage& st = S.st[c % kRing];
         // A_kk = diag(b) (sum of the warps' partials), strictly lower; A_qk inclusive
-        // lower (fp16, interleaved); partials summed in warp order
+        // lower (tf32, interleaved); partials summed in warp order
 #pragma unroll
         for (int e = 2 * lane; e < kChunk * kChunk; e += 64) {
             const int r = e >> 4, s = e & 15;
@@ -377,9 +442,9 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
             const float br = __shfl_sync(0xffffffffu, bl, r);
             PS.A[r * A_LD + s] = (s < r) ? br * sk.x : 0.0f;
             PS.A[r * A_LD + s + 1] = (s + 1 < r) ? br * sk.y : 0.0f;
-            *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(st.aqk) +
-                                         tc::interleaved_offset(r, s, kChunk)) =
-                pack_half2((s <= r) ? sq.x : 0.0f, (s + 1 <= r) ? sq.y : 0.0f);
+            *reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(st.aqk) +
+                                       tc::interleaved32_offset(r, s, AQ_SBO)) =
+                make_float2((s <= r) ? tf32_round(sq.x) : 0.0f, (s + 1 <= r) ? tf32_round(sq.y) : 0.0f);
         }
         __syncwarp();
         if (lane < kChunk) {
@@ -410,38 +475,52 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
 }
 
 // ---- sequential stage: tensor-core issue (one thread) -------------------------------
-// Per chunk c (slot s), in the transposed orientation (TMEM lane = value row v):
-//   [U|O] = V^T [T diag(b) ; 0]^T             (u^T into the U half, zeros into O)
-//   [U|O] += S^T [-w ; Q 2^G]^T               (8 MMAs over the 128 key channels)
-//   S^T  += U^T (K 2^(G_last-G))              (S^T was rescaled by 2^G_last beforehand)
+// Per chunk c (slot s), in the transposed orientation (TMEM lane = value row v), with
+// S^T of the chunk's start in state buffer c & 1:
+//   [U|O] = V^T [T diag(b) ; 0]^T             (u^T into the U half, zeros into O; fp16)
+//   [U|O] += S^T [-w ; Q 2^G]^T               (16 tf32 MMAs over the 128 key channels)
+//   S'^T += U^T (K 2^(G_last-G))              (S'^T = S^T 2^G_last, written by the
+//                                              epilogue into the other state buffer)
 //   O    += U^T A_qk^T
+// The state and U are read from tensor memory as fp32 A operands (kind::tf32).
 __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
-    constexpr uint32_t id32 = tc::idesc_f16_f32(128, 32);
-    constexpr uint32_t id16 = tc::idesc_f16_f32(128, 16);
-    constexpr uint32_t id128 = tc::idesc_f16_f32(128, 128);
+    constexpr uint32_t id_u = tc::idesc_f16_f32(128, 32);
+    constexpr uint32_t id_s = tc::idesc_tf32_f32(128, 32);
+    constexpr uint32_t id_k = tc::idesc_tf32_f32(128, 128);
+    constexpr uint32_t id_q = tc::idesc_tf32_f32(128, 16);
+    // descriptors of slot 0; slot s adds its byte offset >> 4 to the start field
+    const uint64_t d_vt = tc::smem_desc(smem_u32(S.st[0].vt), 128, T_SBO, tc::kSwizzleNone);
+    const uint64_t d_tbt = tc::smem_desc(smem_u32(S.st[0].tbt), 128, 256, tc::kSwizzleNone);
+    const uint64_t d_buo = tc::smem_desc(smem_u32(S.st[0].buo), 16, 1024, tc::kSwizzle128B);
+    const uint64_t d_kdt = tc::smem_desc(smem_u32(S.st[0].kdt), 128, KD_SBO, tc::kSwizzleNone);
+    const uint64_t d_aqk = tc::smem_desc(smem_u32(S.st[0].aqk), 128, AQ_SBO, tc::kSwizzleNone);
     for (int c = 0; c < U.nch; ++c) {
         const int slot = c % kRing;
-        const Stage& st = S.st[slot];
-        const uint32_t uo = tmem + TM_UO + 32u * (c & 1);
+        const uint64_t so = (uint64_t)((slot * sizeof(Stage)) >> 4);
+        const uint32_t sc = tmem + TM_S + 128u * (c & 1);
+        const uint32_t sn = tmem + TM_S + 128u * ((c + 1) & 1);
+        const uint32_t uo = tmem + TM_UO + 32u * (c % 3);
         if (!mbar_wait(&S.full[slot], (unsigned)((c / kRing) & 1), err)) return;
-        if (!mbar_wait(&S.s16_ready, (unsigned)(c & 1), err)) return;
-        tc::fence_after_sync();
-        tc::mma_ss(uo, tc::smem_desc(smem_u32(st.vt), 128, T_SBO, tc::kSwizzleNone),
-                   tc::smem_desc(smem_u32(st.tbt), 128, 256, tc::kSwizzleNone), id32, 0);
-        const uint32_t buo = smem_u32(st.buo);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t b = buo + (kk >> 2) * (32 * 128) + (kk & 3) * 32;
-            tc::mma_ts(uo, tmem + TM_S16 + 8 * kk, tc::smem_desc(b, 16, 1024, tc::kSwizzle128B),
-                       id32, 1);
+        if (c == 0) {
+            if (!mbar_wait(&S.init_ready, 0u, err)) return;
+        } else {
+            if (!mbar_wait(&S.s_done, (unsigned)((c - 1) & 1), err)) return;
         }
-        tc::commit(smem_u32(&S.uo_done));
-        if (!mbar_wait(&S.u16_ready, (unsigned)(c & 1), err)) return;
         tc::fence_after_sync();
-        tc::mma_ts(tmem + TM_S32, tmem + TM_U16,
-                   tc::smem_desc(smem_u32(st.kdt), 128, T_SBO, tc::kSwizzleNone), id128, 1);
-        tc::mma_ts(uo + 16, tmem + TM_U16,
-                   tc::smem_desc(smem_u32(st.aqk), 128, 256, tc::kSwizzleNone), id16, 1);
+        tc::mma_ss(uo, d_vt + so, d_tbt + so, id_u, 0);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+            tc::mma_ts_tf32(uo, sc + 8 * kk,
+                            d_buo + so + (uint64_t)(((kk >> 2) * 4096 + (kk & 3) * 32) >> 4), id_s, 1);
+        tc::commit(smem_u32(&S.uo_done));
+        if (!mbar_wait(&S.uo_done, (unsigned)(c & 1), err)) return;
+        if (!mbar_wait(&S.scaled, (unsigned)(c & 1), err)) return;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            tc::mma_ts_tf32(sn, uo + 8 * kk, d_kdt + so + (uint64_t)((kk * 256) >> 4), id_k, 1);
+            tc::mma_ts_tf32(uo + 16, uo + 8 * kk, d_aqk + so + (uint64_t)((kk * 256) >> 4), id_q, 1);
+        }
         tc::commit(smem_u32(&S.s_done));
         tc::commit(smem_u32(&S.empty[slot]));
     }
@@ -461,10 +540,10 @@ __device__ __forceinline__ void state_out(const Problem& P, size_t idx, float x)
 
 // ---- sequential stage: epilogue ---------------------------------------------------
 // Warp ew reaches TMEM lanes 32 (ew % 4) .. + 31 (thread = value channel v) and
-// owns half of the state's columns: key channels 64 (ew / 4) .. + 63, U columns
-// (tokens) 8 (ew / 4) .. + 7 and the outputs of those tokens.  After each state
-// update it first writes the fp16 copy that the next chunk's MMAs read (the
-// critical path), then pre-scales the fp32 state by the next chunk's 2^G_last.
+// owns half of the state's columns (key channels 64 (ew / 4) .. + 63) and the
+// outputs of tokens 8 (ew / 4) .. + 7.  Once the state of chunk c's start is
+// complete, it writes 2^G_last(c) times it into the other state buffer, which the
+// update MMAs of chunk c accumulate into while the U|O MMAs still read the first.
 __device__ __forceinline__ void scale32(uint32_t (&x)[32], const float* gc) {
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
@@ -478,11 +557,6 @@ __device__ __forceinline__ void scale32(uint32_t (&x)[32], const float* gc) {
         x[i + 2] = __float_as_uint(b.x);
         x[i + 3] = __float_as_uint(b.y);
     }
-}
-__device__ __forceinline__ void pack32(const uint32_t (&x)[32], uint32_t (&h)[16]) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        h[i] = pack_half2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
 }
 
 __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem, int ew,
@@ -501,92 +575,75 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
                           P.init_state ? state_in(P, sbase + (size_t)c * kDim) : 0.0f);
         return;
     }
-    // initial state: S16 = fp16(S0), S32 = S0 Diag(2^G_last of chunk 0)
-    ok = mbar_wait(&S.full[0], 0u, err);
-    if (!__all_sync(0xffffffffu, ok)) return;
+    // initial state S0 into buffer 0, then S0 Diag(2^G_last of chunk 0) into buffer 1
 #pragma unroll 1
     for (int piece = p0; piece < p0 + 2; ++piece) {
-        uint32_t x[32], h[16];
+        uint32_t x[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const int c = 32 * piece + i;
             x[i] = __float_as_uint(P.init_state ? state_in(P, sbase + (size_t)c * kDim) : 0.0f);
         }
-        pack32(x, h);
-        tc::st16(tl + TM_S16 + 16 * piece, h);
-        scale32(x, S.st[0].gc + 32 * piece);
-        tc::st32(tl + TM_S32 + 32 * piece, x);
+        tc::st32(tl + TM_S + 32 * piece, x);
     }
     tc::wait_st();
     tc::fence_before_sync();
-    mbar_arrive(&S.s16_ready);
-
-    for (int c = 0; c < U.nch; ++c) {
-        const uint32_t uo = tl + TM_UO + 32u * (c & 1);
-        // U^T (this warp's 8 token columns) -> fp16 A operand of the update
-        ok = mbar_wait(&S.uo_done, (unsigned)(c & 1), err);
-        if (!__all_sync(0xffffffffu, ok)) return;
-        tc::fence_after_sync();
-        {
-            uint32_t u[16], h[8];
-            tc::ld16(uo, u);   // all 16 columns (one instruction); this warp converts its half
-            tc::wait_ld();
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                h[i] = pack_half2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
-            if (colhalf == 0) tc::st8(tl + TM_U16, h);
-            tc::wait_st();
-        }
-        tc::fence_before_sync();
-        mbar_arrive(&S.u16_ready);
-
-        // state update done: fp16 copy first (next chunk's MMAs wait on it) ...
-        ok = mbar_wait(&S.s_done, (unsigned)(c & 1), err);
-        const bool more = c + 1 < U.nch;
-        const int nslot = (c + 1) % kRing;
-        if (more) ok = ok && mbar_wait(&S.full[nslot], (unsigned)(((c + 1) / kRing) & 1), err);
-        if (!__all_sync(0xffffffffu, ok)) return;
-        tc::fence_after_sync();
-        if (more) {
+    mbar_arrive(&S.init_ready);
+    ok = mbar_wait(&S.full[0], 0u, err);
+    if (!__all_sync(0xffffffffu, ok)) return;
 #pragma unroll 1
-            for (int piece = p0; piece < p0 + 2; ++piece) {
-                uint32_t x[32], h[16];
-                tc::ld32(tl + TM_S32 + 32 * piece, x);
-                tc::wait_ld();
-                pack32(x, h);
-                tc::st16(tl + TM_S16 + 16 * piece, h);
-            }
-            tc::wait_st();
-            tc::fence_before_sync();
-            mbar_arrive(&S.s16_ready);
-            // ... then the rescale, finished before this warp's next U^T arrive (which
-            // the next state update waits for)
+    for (int piece = p0; piece < p0 + 2; ++piece) {
+        uint32_t x[32];
+        tc::ld32(tl + TM_S + 32 * piece, x);
+        tc::wait_ld();
+        scale32(x, S.st[0].gc + 32 * piece);
+        tc::st32(tl + TM_S + 128 + 32 * piece, x);
+    }
+    tc::wait_st();
+    tc::fence_before_sync();
+    mbar_arrive(&S.scaled);
+
+    for (int c = 1; c <= U.nch; ++c) {
+        // chunk c - 1 finished: its end state is in buffer c & 1
+        ok = mbar_wait(&S.s_done, (unsigned)((c - 1) & 1), err);
+        const bool more = c < U.nch;
+        const int slot = c % kRing;
+        if (more) ok = ok && mbar_wait(&S.full[slot], (unsigned)((c / kRing) & 1), err);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc::fence_after_sync();
+        const uint32_t sc = tl + TM_S + 128u * (c & 1);
+        if (more) {
+            const uint32_t sn = tl + TM_S + 128u * ((c + 1) & 1);
 #pragma unroll 1
             for (int piece = p0; piece < p0 + 2; ++piece) {
                 uint32_t x[32];
-                tc::ld32(tl + TM_S32 + 32 * piece, x);
+                tc::ld32(sc + 32 * piece, x);
                 tc::wait_ld();
-                scale32(x, S.st[nslot].gc + 32 * piece);
-                tc::st32(tl + TM_S32 + 32 * piece, x);
+                scale32(x, S.st[slot].gc + 32 * piece);
+                tc::st32(sn + 32 * piece, x);
             }
+            tc::wait_st();
+            tc::fence_before_sync();
+            mbar_arrive(&S.scaled);
         } else if (P.final_state) {
 #pragma unroll 1
             for (int piece = p0; piece < p0 + 2; ++piece) {
                 uint32_t x[32];
-                tc::ld32(tl + TM_S32 + 32 * piece, x);
+                tc::ld32(sc + 32 * piece, x);
                 tc::wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     state_out(P, sbase + (size_t)(32 * piece + i) * kDim, __uint_as_float(x[i]));
             }
         }
-        // outputs of chunk c, tokens 8 colhalf .. + 7: O^T lane v, column t
+        // outputs of chunk c - 1, tokens 8 colhalf .. + 7: O^T lane v, column t
         {
+            const int cp = c - 1;
             uint32_t o[16];
-            tc::ld16(uo + 16, o);
+            tc::ld16(tl + TM_UO + 32u * (cp % 3) + 16, o);
             tc::wait_ld();
-            const int len = min(kChunk, U.L - c * kChunk);
-            __nv_bfloat16* out = P.out + ((size_t)(U.tok_start + c * kChunk) * P.H + U.h) * kDim + v;
+            const int len = min(kChunk, U.L - cp * kChunk);
+            __nv_bfloat16* out = P.out + ((size_t)(U.tok_start + cp * kChunk) * P.H + U.h) * kDim + v;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int t = 8 * colhalf + j;
@@ -598,7 +655,8 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) fused_kernel(Problem P, SeqMap M, int* err) {
+__global__ void __launch_bounds__(kThreads, 1)
+    fused_kernel(Problem P, SeqMap M, const __grid_constant__ RawMaps TM, int* err) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the 128-byte swizzle acts on absolute shared addresses: align the stages to 1024 B
     unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -627,12 +685,16 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Problem P, SeqMap M,
         }
         mbar_init(&S.uo_done, 1);
         mbar_init(&S.s_done, 1);
-        mbar_init(&S.s16_ready, kEpiWarps * 32);
-        mbar_init(&S.u16_ready, kEpiWarps * 32);
+        mbar_init(&S.init_ready, kEpiWarps * 32);
+        mbar_init(&S.scaled, kEpiWarps * 32);
         mbar_init(&S.epi_done, kEpiWarps * 32);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&S.a_ready[b], kProdThreads);
             mbar_init(&S.t_ready[b], 32);
+        }
+        for (int s = 0; s < kRaw; ++s) {
+            mbar_init(&S.raw_full[s], 1);                 // loader's arrive + TMA bytes
+            mbar_init(&S.raw_empty[s], kProdThreads);     // every producer thread
         }
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
@@ -666,12 +728,40 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Problem P, SeqMap M,
         tc::tmem_dealloc(tmem, kTmemCols);
     } else if (warp == kSolveWarp) {
         solve(P, U, S, lane, err);
+    } else if (warp == kLoadWarp) {
+        if (lane == 0) loader(TM, U, S, err);
     } else {
         produce(P, U, S, warp - kProdWarp0, lane, err);
     }
 }
 
 bool g_attr_set[64] = {};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// [rows][H][128] bf16 viewed as a 3-D tensor (channel, head, row); boxes of
+// 64 channels x 1 head x 16 rows, 128-byte swizzle (one 128-byte row per token)
+cudaError_t encode_rows(CUtensorMap* map, const void* base, int H, long long rows) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (g_encode == nullptr) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)H, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)kDim * 2, (cuuint64_t)H * kDim * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)kChunk};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 }  // namespace
 
@@ -689,7 +779,19 @@ cudaError_t launch_fused(const Problem& P, const SeqMap& M, int* err, cudaStream
     }
     const long long ctas = (long long)P.N * P.H;
     if (ctas == 0) return cudaSuccess;
-    fused_kernel<<<(unsigned)ctas, kThreads, smem, s>>>(P, M, err);
+    // total token rows: B*T (fixed length, N = B sequences of T) or T (varlen, B = 1)
+    const long long rows = (P.cu_seqlens == nullptr) ? (long long)P.N * P.T : (long long)P.T;
+    RawMaps TM;
+    if (rows > 0) {
+        cudaError_t e = encode_rows(&TM.q, P.q, P.H, rows);
+        if (e == cudaSuccess) e = encode_rows(&TM.k, P.k, P.H, rows);
+        if (e == cudaSuccess) e = encode_rows(&TM.v, P.v, P.H, rows);
+        if (e == cudaSuccess) e = encode_rows(&TM.g, P.g, P.H, rows);
+        if (e != cudaSuccess) return e;
+    } else {
+        memset(&TM, 0, sizeof(TM));   // no tokens: the loader issues nothing
+    }
+    fused_kernel<<<(unsigned)ctas, kThreads, smem, s>>>(P, M, TM, err);
     return cudaGetLastError();
 }
 

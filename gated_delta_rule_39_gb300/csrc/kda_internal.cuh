@@ -6,14 +6,17 @@
 //     A_qk = (Q*2^G)(K*2^-G)^T: tf32 tensor-core MMA with fp32 accumulate.
 //     2^-G reaches 2^115 inside a 16-token chunk, which needs an 8-bit
 //     exponent, and the 10-bit tf32 mantissa keeps these products accurate.
-//   - every operand of the sequential state recurrence (state copy, w, u, U,
-//     Q*2^G, K*2^(G_C-G), A_qk, the WY inverse): fp16 with fp32 accumulate.
-//     All of them are bounded by O(1) in magnitude (the inverse's inputs lie
-//     in [-1, 1], "Moonshot AI Open-Sources FlashKDA", "What makes the kernel
-//     fast": fp16 16x16 inversion), and fp16 carries 3 more mantissa bits
-//     than bf16; values that underflow fp16 are below 2^-24 of the state scale.
+//   - the sequential state recurrence runs on tcgen05 tensor cores with the
+//     state S and U = u - w S held in tensor memory as fp32 and read directly
+//     as the A operand of kind::tf32 MMAs; their partners (w, Q*2^G,
+//     K*2^(G_C-G), A_qk) are fp32 rounded to tf32 (round to nearest).
+//   - u = T diag(b) V: fp16 operands (V is bf16 data; the WY inverse's inputs
+//     lie in [-1, 1], "Moonshot AI Open-Sources FlashKDA", "What makes the
+//     kernel fast": fp16 16x16 inversion), fp32 accumulate.  w = T diag(b)
+//     (K*2^G) likewise, with fp32 accumulate and a tf32 result.
 //   - the recurrent state itself: fp32 accumulators.
 #pragma once
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -47,6 +50,11 @@ struct Problem {
     int N;                   // sequences
     int T;                   // tokens per sequence (fixed) or total tokens (varlen)
     int H;
+};
+
+// TMA tensor maps over the token rows of q, k, v, g (built on the host per call).
+struct RawMaps {
+    CUtensorMap q, k, v, g;
 };
 
 // Scratch written by the varlen sequence map, read by the fused kernel.

@@ -14,6 +14,11 @@ namespace tc {
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// kind::tf32 (A / B type 2 = tf32: fp32 storage, 10-bit mantissa), fp32 accumulator
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
 
 // ---- shared-memory matrix descriptor -------------------------------------------
 //   bits 0-13 start address >> 4, 16-29 leading-dimension byte offset >> 4,
@@ -49,6 +54,17 @@ __host__ __device__ constexpr int interleaved16_offset(int row, int k, int sbo) 
 // and K = 64 * kblocks 16-bit elements, stored as [kblock][row][128 bytes]
 __host__ __device__ constexpr int swizzled_offset(int row, int k, int rows) {
     return (k >> 6) * rows * 128 + row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) + (k & 7) * 2;
+}
+
+// 32-bit elements: a core matrix is 8 rows x 4 elements.  Interleaved K-major tile
+// with lbo = 128 (K-direction core step) and `sbo` bytes between 8-row groups
+__host__ __device__ constexpr int interleaved32_offset(int row, int k, int sbo) {
+    return (row >> 3) * sbo + (k >> 2) * 128 + (row & 7) * 16 + (k & 3) * 4;
+}
+// 128B-swizzled K-major tile of `rows` rows and K = 32 * kblocks 32-bit elements,
+// stored as [kblock][row][128 bytes]
+__host__ __device__ constexpr int swizzled32_offset(int row, int k, int rows) {
+    return (k >> 5) * rows * 128 + row * 128 + ((((k & 31) >> 2) ^ (row & 7)) << 4) + (k & 3) * 4;
 }
 
 // ---- tensor memory --------------------------------------------------------------
@@ -101,6 +117,14 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::tf32: A is M lanes x K fp32 columns
+__device__ __forceinline__ void mma_ts_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n"
         ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 // one arrive on the mbarrier once every MMA issued so far by this thread completes
