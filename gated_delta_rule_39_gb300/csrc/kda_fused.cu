@@ -2,19 +2,22 @@
 // the chunkwise algorithm, so q, k, v, g and beta are read from HBM once and
 // only the output and the states are written.
 //
-//   producer warps (8)  the token-parallel stage.  Warp w owns key / value
-//                       channels 16w .. 16w+15 of every 16-token chunk: it loads
-//                       its slice of q, k, v, g straight into registers (one chunk
-//                       ahead), computes the gates and their in-chunk cumulative
-//                       sum across rows with warp shuffles, the decay factors,
-//                       the operand tiles of the recurrence (Q 2^G, K 2^(G_last-G),
-//                       V, 2^G_last) and its share of the decay-ratio products
-//                       A_kk and A_qk (tf32 MMA fed from registers, summed across
-//                       warps in shared memory).  One chunk later it forms its
-//                       slice of w = T diag(b)(K 2^G).
-//   solver warp         (I + A_kk)^-1 by forward substitution, T diag(b), A_qk.
+//   loader warp         TMA tensor loads of each chunk's raw q, k, v, g rows into a
+//                       ring of shared-memory slots, several chunks ahead.
+//   producer warps (8)  the token-parallel stage.  Warp w owns key / value channels
+//                       16w .. 16w+15; each thread holds one channel pair over four
+//                       consecutive rows of the 16-token chunk.  They compute the
+//                       gates, the in-chunk cumulative base-2 log-decay G, the decay
+//                       factors and the operand tiles of the chunk (K 2^G, Q 2^G,
+//                       K 2^-G, K 2^(G_last-G), V), and one chunk later their slice
+//                       of w = T diag(b) (K 2^G).
+//   A-product warp      issues the tcgen05 MMAs of the decay-ratio products
+//                       A_kk = (K 2^G)(K 2^-G)^T and A_qk = (Q 2^G)(K 2^-G)^T and
+//                       writes A_qk (inclusive lower) as an operand tile.
+//   solver warp         (I + diag(b) A_kk)^-1 by forward substitution, T diag(b).
 //   MMA warp            issues the tcgen05 MMAs of the recurrence (one thread).
-//   epilogue warps (4)  own the tensor-memory state S^T (lane v = value channel v).
+//   epilogue warps (8)  own the tensor-memory state S^T (lane v = value channel v):
+//                       decay rescale, outputs, initial and final state.
 //
 // Chunkwise DPLR-variant (WY) algorithm with 16-token chunks, a 16 x 16
 // inverse and base-2 gates: "Moonshot AI Open-Sources FlashKDA", sections
@@ -37,40 +40,47 @@ namespace {
 
 constexpr int kEpiWarps = 8;                // epilogue: two warps per TMEM lane quarter,
                                             // each owning half of the state's columns
-constexpr int kMmaWarp = kEpiWarps;         // issues the tcgen05 MMAs, owns tensor memory
-constexpr int kSolveWarp = kMmaWarp + 1;    // 16 x 16 inverse
-constexpr int kProdWarp0 = kSolveWarp + 1;
+constexpr int kSolveWarp = kEpiWarps;       // lane quarter 0: reads A_kk rows 0-15
+constexpr int kAprodWarp = kSolveWarp + 1;  // lane quarter 1: reads A_qk rows (lanes 32-47)
+constexpr int kMmaWarp = kAprodWarp + 1;    // recurrence MMAs, owns tensor memory
+constexpr int kProdWarp0 = kMmaWarp + 1;
 constexpr int kProdWarps = 8;               // 16 key channels each
 constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kLoadWarp = kProdWarp0 + kProdWarps;   // TMA loads of the raw rows (one lane)
 constexpr int kRing = 3;                    // chunk-operand slots
 constexpr int kRaw = 4;                     // raw-row slots: chunks in flight from HBM
 constexpr int kThreads = (kLoadWarp + 1) * 32;
+static_assert(kSolveWarp % 4 == 0 && kAprodWarp % 4 == 1, "tensor-memory lane quarters");
 
-constexpr int A_LD = 17;
+constexpr int AH_LD = 24;     // fp16 per row of the solver's A tile (48 B: ldmatrix conflict-free)
 constexpr int TB_LD = 24;     // fp16 per row of T diag(b) (48 B: ldmatrix conflict-free)
 constexpr int KG_LD = 24;     // fp16 per row of a warp's K 2^G tile (48 B)
 constexpr int T_SBO = 272;    // byte step between 8-row groups of the transposed fp16
                               // 128 x 16 tile (16 bytes past 256 spreads row groups over banks)
-constexpr int KD_SBO = 512;   // byte step between 8-row groups of the fp32 128 x 16 tile
-constexpr int AQ_SBO = 512;   // same for the fp32 16 x 16 A_qk tile
+constexpr int KD_SBO = 528;   // same for the fp32 128 x 16 tile
+constexpr int AQ_SBO = 512;   // fp32 16 x 16 A_qk tile
+constexpr int X_ROWS = 48;    // rows of the [K 2^G ; Q 2^G ; -w] tile
 
 // tensor-memory columns (one allocation of 512)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_S = 0;       // S^T, fp32: two buffers of 128 columns (chunk parity)
-constexpr uint32_t TM_UO = 256;    // [U | O] accumulators: three buffers of 32 columns
+constexpr uint32_t TM_UO = 256;    // [O | U] accumulators: three buffers of 32 columns
+constexpr uint32_t TM_A = 352;     // A_kk / A_qk products (M = 64): two buffers of 16 columns
 
 // One chunk's operands for the tensor-core recurrence (canonical K-major layouts).
 // The operands multiplied by the fp32 state or by U are fp32 values rounded to
 // tf32 (kind::tf32 MMAs read the state and U straight from tensor memory).
 struct Stage {
-    float buo[4 * 32 * 32];        // B of [U|O] += S^T [-w; Q 2^G]^T: 32 x 128, 128B swizzle
+    // rows 0-15 K 2^G, rows 16-31 Q 2^G, rows 32-47 -w; 128 key channels; 128B swizzle,
+    // [K block of 32 channels][48 rows][128 bytes].  Rows 0-31 are the A operand of
+    // the decay-ratio products, rows 16-47 the B operand of [O|U] += S^T [Q 2^G ; -w]^T.
+    float x[4 * X_ROWS * 32];
     float kdt[16 * KD_SBO / 4];    // B of the state update: (K 2^(G_last-G))^T 128 x 16
     float aqk[2 * AQ_SBO / 4];     // B of O += U A_qk^T: A_qk 16 x 16
     __half vt[16 * T_SBO / 2];     // A of u^T = V^T (T diag b)^T: V^T 128 x 16, interleaved
-    __half tbt[32 * 16];           // B of the u MMA: rows 0-15 T diag(b), rows 16-31 zero
+    __half tbt[32 * 16];           // B of the u MMA: rows 0-15 zero, rows 16-31 T diag(b)
     float gc[kDim];                // 2^G_last
-    unsigned char pad_[1280];      // keep sizeof(Stage) a multiple of 1024
+    unsigned char pad_[1024];      // keep sizeof(Stage) a multiple of 1024
 };
 static_assert(sizeof(Stage) % 1024 == 0, "stages keep the swizzled tiles 1024-byte aligned");
 // One chunk's raw rows of q, k, v, g as the TMA engine writes them: per tensor two
@@ -81,26 +91,30 @@ struct RawSlot {
 constexpr uint32_t kRawBytes = sizeof(RawSlot);
 static_assert(kRawBytes == 16384, "four tensors x 16 rows x 256 bytes");
 struct ProdShared {
-    float part[2][kProdWarps][2][kChunk * kChunk]; // [chunk parity][warp][A_kk, A_qk] partials
     __half tb[2][kChunk * TB_LD];                  // T diag(b) per chunk parity
     __half kg[kProdWarps][2][kChunk * KG_LD];      // each warp's K 2^G tile per chunk parity
-    float A[kChunk * A_LD];                        // solver scratch
+    __half Ah[kChunk * AH_LD];                     // solver: diag(b) A_kk, strictly lower
 };
 struct Smem {
     Stage st[kRing];
+    // K 2^-G per chunk parity ([K block][16 rows][128 bytes], 128B swizzle): B operand of
+    // the decay-ratio products.  (Their M = 64 A operand, rows 0-63 of a stage's x tile,
+    // reads 2 KB past the tile's last block, into the same stage's kdt tile.)
+    float ki[2][4 * kChunk * 32];
     RawSlot raw[kRaw];
     ProdShared pr;
     unsigned long long raw_full[kRaw];   // TMA bytes landed
     unsigned long long raw_empty[kRaw];  // producers have read the slot
-    unsigned long long full[kRing];    // producers -> MMA / epilogue
-    unsigned long long empty[kRing];   // MMA commit -> producers
-    unsigned long long a_ready[2];     // producers' partial A_kk / A_qk summed
-    unsigned long long t_ready[2];     // solver: T diag(b), A_qk written
-    unsigned long long uo_done;        // U|O MMAs complete
-    unsigned long long s_done;         // state update + O MMAs complete
-    unsigned long long init_ready;     // epilogue: initial state written
-    unsigned long long scaled;         // epilogue: 2^G_last S^T written to the other buffer
-    unsigned long long epi_done;       // epilogue finished with tensor memory
+    unsigned long long full[kRing];      // producers -> MMA / epilogue
+    unsigned long long empty[kRing];     // MMA commit -> producers
+    unsigned long long kq_ready[2];      // producers: product operands written
+    unsigned long long a_done[2];        // decay-ratio MMAs complete
+    unsigned long long t_ready[2];       // solver (T diag b) and A-product warp (A_qk) done
+    unsigned long long uo_done;          // O|U MMAs complete
+    unsigned long long s_done;           // state update + O MMAs complete
+    unsigned long long init_ready;       // epilogue: initial state written
+    unsigned long long scaled;           // epilogue: 2^G_last S^T written to the other buffer
+    unsigned long long epi_done;         // epilogue finished with tensor memory
     uint32_t tmem_base;
 };
 
@@ -154,6 +168,27 @@ __device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(z));
     return r;
 }
+__device__ __forceinline__ float2 f2add(float2 a, float2 b) {
+    unsigned long long x, y, z;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("add.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(y));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(z));
+    return r;
+}
+__device__ __forceinline__ float2 f2sub(float2 a, float2 b) {
+    unsigned long long x, y, z;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("sub.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(y));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(z));
+    return r;
+}
+__device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
+    return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+}
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t raw) {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&raw);
     return __bfloat1622float2(v);
@@ -199,49 +234,21 @@ __device__ void loader(const RawMaps& TM, const Unit& U, Smem& S, int* err) {
 }
 
 // ---- token-parallel stage: producer warp w, channels 16w .. 16w+15 ----------------
-// Lane (g, t) = (lane >> 2, lane & 3) holds rows g and g+8 of the chunk for the
-// channel pairs p = 16w + 8kk + 2t, p+1 (kk = 0, 1).  In the tf32 MMA fragments
-// of k-step kk the pair plays logical columns t and t+4; the decay-ratio
-// products sum over channels, so this relabelling leaves them unchanged.
-struct RawSlice {
-    uint32_t q[2][2], k[2][2], v[2][2], g[2][2];   // [row g / g+8][kk] bf16 pairs
-};
-
-__device__ __forceinline__ void lds_slice(const RawSlot& R, int w, int lg, int lt, int len,
-                                          RawSlice& X) {
-    const int half = w >> 2;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int r = lg + 8 * i;
-        const bool ok = r < len;
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-            const int chunk16 = 2 * (w & 3) + kk;   // 16-byte chunk of the 128-byte row
-            const int off = r * 128 + ((chunk16 ^ (r & 7)) << 4) + 4 * lt;
-            const auto ld = [&](int t) {
-                return ok ? *reinterpret_cast<const uint32_t*>(
-                                reinterpret_cast<const unsigned char*>(R.x[t][half]) + off)
-                          : 0u;
-            };
-            X.q[i][kk] = ld(0);
-            X.k[i][kk] = ld(1);
-            X.v[i][kk] = ld(2);
-            X.g[i][kk] = ld(3);
-        }
-    }
-}
-
+// Lane (pi, j) = (lane & 7, lane >> 3) holds channels c0 = 16w + 2 pi, c0 + 1 over rows
+// 4j .. 4j+3 of the chunk.
 __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lane, int* err) {
-    const int lg = lane >> 2, lt = lane & 3;
-    const int cbase = 16 * w;
+    const int pi = lane & 7, j = lane >> 3;
+    const int c0 = 16 * w + 2 * pi;
+    const int r0 = 4 * j;
     const float expA = expf(P.A_log[U.h]);
     const float ga = -expA * kLog2e;   // sigmoid argument in base 2: g ga + gb
-    float gb[2][2];
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) gb[kk][e] = ga * P.dt_bias[(size_t)U.h * kDim + cbase + 8 * kk + 2 * lt + e];
+    const float2 gb = make_float2(ga * P.dt_bias[(size_t)U.h * kDim + c0],
+                                  ga * P.dt_bias[(size_t)U.h * kDim + c0 + 1]);
     const float lb2 = P.lower_bound * kLog2e;
+    // raw-slot addressing: box (channel half), 16-byte chunk of the 128-byte row, offset
+    const int half = w >> 2;
+    const int chunk16 = 2 * (w & 3) + (pi >> 2);
+    const int inoff = 4 * (pi & 3);
     ProdShared& PS = S.pr;
 
     for (int c = 0; c <= U.nch; ++c) {
@@ -250,123 +257,110 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
             const int rslot = c % kRaw;
             bool ok = mbar_wait(&S.raw_full[rslot], (unsigned)((c / kRaw) & 1), err);
             if (!__all_sync(0xffffffffu, ok)) return;
-            RawSlice X;
-            lds_slice(S.raw[rslot], w, lg, lt, len, X);
-            mbar_arrive(&S.raw_empty[rslot]);   // release: the reads above come first
+            uint32_t rq[4], rk[4], rv[4], rg[4];
+            {
+                const RawSlot& R = S.raw[rslot];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = r0 + i;
+                    const bool in = r < len;
+                    const int off = r * 128 + ((chunk16 ^ (r & 7)) << 4) + inoff;
+                    const auto ld = [&](int t) {
+                        return in ? *reinterpret_cast<const uint32_t*>(
+                                        reinterpret_cast<const unsigned char*>(R.x[t][half]) + off)
+                                  : 0u;
+                    };
+                    rq[i] = ld(0);
+                    rk[i] = ld(1);
+                    rv[i] = ld(2);
+                    rg[i] = ld(3);
+                }
+            }
+            // The slot's next writer is the TMA engine (async proxy): order this
+            // thread's generic-proxy reads before it, then release the slot.
+            tc::fence_proxy_async_smem();
+            mbar_arrive(&S.raw_empty[rslot]);
             const int slot = c % kRing;
             Stage& st = S.st[slot];
             const int par = c & 1;
             if (c >= kRing) ok = mbar_wait(&S.empty[slot], (unsigned)(((c / kRing) - 1) & 1), err);
             if (!__all_sync(0xffffffffu, ok)) return;
 
-            // gates, cumulative over rows: Hillis-Steele scan across the 8 lanes of equal t
-            float G[2][2][2];   // [row g / g+8][kk][e]
+            // gates lower_bound * sigmoid(exp(A_log) (g + dt_bias)), base 2; rows past the
+            // sequence end decay by nothing
+            float2 G[4];
 #pragma unroll
-            for (int i = 0; i < 2; ++i)
+            for (int i = 0; i < 4; ++i) {
+                const float2 xa = f2fma(bf2_to_f2(rg[i]), make_float2(ga, ga), gb);
+                const float2 sg = f2mul(make_float2(rcp_approx(1.0f + ex2_approx(xa.x)),
+                                                    rcp_approx(1.0f + ex2_approx(xa.y))),
+                                        make_float2(lb2, lb2));
+                G[i] = (r0 + i < len) ? sg : make_float2(0.0f, 0.0f);
+            }
+            // inclusive cumulative sum over the 16 rows: within the thread's four rows,
+            // then across the four row groups (lanes 8 apart)
+            G[1] = f2add(G[1], G[0]);
+            G[2] = f2add(G[2], G[1]);
+            G[3] = f2add(G[3], G[2]);
+            float2 incl = G[3];
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    const float2 gv = bf2_to_f2(X.g[i][kk]);
-                    const bool valid = lg + 8 * i < len;
-                    const float2 xa = f2fma(gv, make_float2(ga, ga), make_float2(gb[kk][0], gb[kk][1]));
-                    const float2 sg = f2mul(make_float2(rcp_approx(1.0f + ex2_approx(xa.x)),
-                                                        rcp_approx(1.0f + ex2_approx(xa.y))),
-                                            make_float2(lb2, lb2));
-                    G[i][kk][0] = valid ? sg.x : 0.0f;
-                    G[i][kk][1] = valid ? sg.y : 0.0f;
-                }
-            float glast[2][2];
+            for (int d = 8; d < 32; d <<= 1) {
+                const float2 y = make_float2(__shfl_up_sync(0xffffffffu, incl.x, d),
+                                             __shfl_up_sync(0xffffffffu, incl.y, d));
+                if (lane >= d) incl = f2add(incl, y);
+            }
+            const float2 excl = f2sub(incl, G[3]);
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float a = G[0][kk][e], b = G[1][kk][e];
-#pragma unroll
-                    for (int d = 4; d < 32; d <<= 1) {
-                        const float ya = __shfl_up_sync(0xffffffffu, a, d);
-                        const float yb = __shfl_up_sync(0xffffffffu, b, d);
-                        if (lane >= d) {
-                            a += ya;
-                            b += yb;
-                        }
-                    }
-                    const float tot = __shfl_sync(0xffffffffu, a, 28 + lt);   // rows 0..7
-                    G[0][kk][e] = a;
-                    G[1][kk][e] = tot + b;
-                    glast[kk][e] = __shfl_sync(0xffffffffu, tot + b, 28 + lt);   // row 15
-                }
+            for (int i = 0; i < 4; ++i) G[i] = f2add(G[i], excl);
+            const float2 glast = make_float2(__shfl_sync(0xffffffffu, incl.x, 24 + pi),
+                                             __shfl_sync(0xffffffffu, incl.y, 24 + pi));
+            const float2 gc = make_float2(ex2_approx(glast.x), ex2_approx(glast.y));
+            if (j == 0) *reinterpret_cast<float2*>(&st.gc[c0]) = gc;
 
             // decay factors and operand tiles
-            unsigned char* buo = reinterpret_cast<unsigned char*>(st.buo);
+            unsigned char* x = reinterpret_cast<unsigned char*>(st.x);
+            unsigned char* ki = reinterpret_cast<unsigned char*>(S.ki[par]);
+            __half* kgt = PS.kg[w][par];
+            float kd0[4], kd1[4];
+            __half v0[4], v1[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = r0 + i;
+                const float2 e = make_float2(ex2_approx(G[i].x), ex2_approx(G[i].y));
+                const float2 d = make_float2(ex2_approx(-G[i].x), ex2_approx(-G[i].y));
+                const float2 kv = bf2_to_f2(rk[i]);
+                const float2 kg = f2mul(kv, e);
+                const float2 kin = f2mul(kv, d);
+                const float2 qg = f2mul(bf2_to_f2(rq[i]), e);
+                const float2 kd = f2mul(kin, gc);
+                const float2 vv = bf2_to_f2(rv[i]);
+                *reinterpret_cast<float2*>(x + tc::swizzled32_offset(r, c0, X_ROWS)) =
+                    make_float2(tf32_round(kg.x), tf32_round(kg.y));
+                *reinterpret_cast<float2*>(x + tc::swizzled32_offset(16 + r, c0, X_ROWS)) =
+                    make_float2(tf32_round(qg.x), tf32_round(qg.y));
+                *reinterpret_cast<float2*>(ki + tc::swizzled32_offset(r, c0, kChunk)) =
+                    make_float2(tf32_round(kin.x), tf32_round(kin.y));
+                *reinterpret_cast<uint32_t*>(&kgt[r * KG_LD + 2 * pi]) = pack_half2(kg.x, kg.y);
+                kd0[i] = tf32_round(kd.x);
+                kd1[i] = tf32_round(kd.y);
+                v0[i] = __float2half_rn(vv.x);
+                v1[i] = __float2half_rn(vv.y);
+            }
+            // (K 2^(G_last-G))^T and V^T: four consecutive tokens of one channel are
+            // contiguous in the K-major core matrix
             unsigned char* kdt = reinterpret_cast<unsigned char*>(st.kdt);
             unsigned char* vt = reinterpret_cast<unsigned char*>(st.vt);
-            __half* kgt = PS.kg[w][par];
-            uint32_t akf[2][4], aqf[2][4], bf0[2][2], bf1[2][2];
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                const int p = cbase + 8 * kk + 2 * lt;
-                const float gc0 = ex2_approx(glast[kk][0]), gc1 = ex2_approx(glast[kk][1]);
-                if (lg == 0) *reinterpret_cast<float2*>(&st.gc[p]) = make_float2(gc0, gc1);
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int r = lg + 8 * i;
-                    const float e0 = ex2_approx(G[i][kk][0]), e1 = ex2_approx(G[i][kk][1]);
-                    const float d0 = ex2_approx(-G[i][kk][0]), d1 = ex2_approx(-G[i][kk][1]);
-                    const float2 kv = bf2_to_f2(X.k[i][kk]);
-                    const float2 qv = bf2_to_f2(X.q[i][kk]);
-                    const float2 vv = bf2_to_f2(X.v[i][kk]);
-                    const float2 kg = f2mul(kv, make_float2(e0, e1));
-                    const float2 ki = f2mul(kv, make_float2(d0, d1));
-                    const float2 qg = f2mul(qv, make_float2(e0, e1));
-                    const float2 kd = f2mul(ki, make_float2(gc0, gc1));
-                    const float kg0 = kg.x, kg1 = kg.y, ki0 = ki.x, ki1 = ki.y, qg0 = qg.x, qg1 = qg.y;
-                    // tf32 fragments: A rows g / g+8 -> a0,a2 / a1,a3; B n-tile i
-                    akf[kk][i] = to_tf32(kg0);
-                    akf[kk][i + 2] = to_tf32(kg1);
-                    aqf[kk][i] = to_tf32(qg0);
-                    aqf[kk][i + 2] = to_tf32(qg1);
-                    if (i == 0) {
-                        bf0[kk][0] = to_tf32(ki0);
-                        bf0[kk][1] = to_tf32(ki1);
-                    } else {
-                        bf1[kk][0] = to_tf32(ki0);
-                        bf1[kk][1] = to_tf32(ki1);
-                    }
-                    *reinterpret_cast<float2*>(buo + tc::swizzled32_offset(16 + r, p, 32)) =
-                        make_float2(__uint_as_float(aqf[kk][i]), __uint_as_float(aqf[kk][i + 2]));
-                    *reinterpret_cast<uint32_t*>(&kgt[r * KG_LD + 8 * kk + 2 * lt]) =
-                        pack_half2(kg0, kg1);
-                    *reinterpret_cast<float*>(kdt + tc::interleaved32_offset(p, r, KD_SBO)) =
-                        tf32_round(kd.x);
-                    *reinterpret_cast<float*>(kdt + tc::interleaved32_offset(p + 1, r, KD_SBO)) =
-                        tf32_round(kd.y);
-                    *reinterpret_cast<__half*>(vt + tc::interleaved16_offset(p, r, T_SBO)) =
-                        __float2half_rn(vv.x);
-                    *reinterpret_cast<__half*>(vt + tc::interleaved16_offset(p + 1, r, T_SBO)) =
-                        __float2half_rn(vv.y);
-                }
-            }
-            // this warp's share of A_kk = (K 2^G)(K 2^-G)^T and A_qk = (Q 2^G)(K 2^-G)^T
-            float pk[2][4] = {}, pq[2][4] = {};
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                mma_tf32(pk[0], akf[kk], bf0[kk][0], bf0[kk][1]);
-                mma_tf32(pk[1], akf[kk], bf1[kk][0], bf1[kk][1]);
-                mma_tf32(pq[0], aqf[kk], bf0[kk][0], bf0[kk][1]);
-                mma_tf32(pq[1], aqf[kk], bf1[kk][0], bf1[kk][1]);
-            }
-            // partials go to this warp's own slots; the solver sums them in a fixed
-            // order, so results do not depend on warp timing
-            float* ak = PS.part[par][w][0];
-            float* aq = PS.part[par][w][1];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int e = (lg + 8 * hh) * kChunk + 8 * nt + 2 * lt;
-                    *reinterpret_cast<float2*>(&ak[e]) = make_float2(pk[nt][2 * hh], pk[nt][2 * hh + 1]);
-                    *reinterpret_cast<float2*>(&aq[e]) = make_float2(pq[nt][2 * hh], pq[nt][2 * hh + 1]);
-                }
-            mbar_arrive(&S.a_ready[par]);
+            *reinterpret_cast<float4*>(kdt + tc::interleaved32_offset(c0, r0, KD_SBO)) =
+                make_float4(kd0[0], kd0[1], kd0[2], kd0[3]);
+            *reinterpret_cast<float4*>(kdt + tc::interleaved32_offset(c0 + 1, r0, KD_SBO)) =
+                make_float4(kd1[0], kd1[1], kd1[2], kd1[3]);
+            *reinterpret_cast<uint2*>(vt + tc::interleaved16_offset(c0, r0, T_SBO)) =
+                make_uint2(pack_halves(v0[0], v0[1]), pack_halves(v0[2], v0[3]));
+            *reinterpret_cast<uint2*>(vt + tc::interleaved16_offset(c0 + 1, r0, T_SBO)) =
+                make_uint2(pack_halves(v1[0], v1[1]), pack_halves(v1[2], v1[3]));
+            // generic-proxy writes of this thread -> visible to the tensor core
+            tc::fence_proxy_async_smem();
+            mbar_arrive(&S.kq_ready[par]);
         }
         // ---- one chunk behind: w = T diag(b)(K 2^G) for this warp's channels -------
         if (c >= 1) {
@@ -374,43 +368,126 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
             const int par = cp & 1;
             const bool ok = mbar_wait(&S.t_ready[par], (unsigned)((cp >> 1) & 1), err);
             if (!__all_sync(0xffffffffu, ok)) return;
+            __syncwarp();
             Stage& st = S.st[cp % kRing];
-            unsigned char* buo = reinterpret_cast<unsigned char*>(st.buo);
+            unsigned char* x = reinterpret_cast<unsigned char*>(st.x);
             uint32_t ta[4], b[4];
             ldsm_x4(ta, &PS.tb[par][((lane & 7) + 8 * ((lane >> 3) & 1)) * TB_LD + 8 * (lane >> 4)]);
             ldsm_x4_t(b, &PS.kg[w][par][((lane & 7) + 8 * ((lane >> 3) & 1)) * KG_LD + 8 * (lane >> 4)]);
             float cw0[4] = {}, cw1[4] = {};
             mma_f16(cw0, ta, b[0], b[1]);
             mma_f16(cw1, ta, b[2], b[3]);
-            const int col0 = cbase + 2 * lt, col1 = col0 + 8;
-            *reinterpret_cast<float2*>(buo + tc::swizzled32_offset(lg, col0, 32)) =
+            const int lg = lane >> 2, lt = lane & 3;
+            const int col0 = 16 * w + 2 * lt, col1 = col0 + 8;
+            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(32 + lg, col0, X_ROWS)) =
                 make_float2(tf32_round(-cw0[0]), tf32_round(-cw0[1]));
-            *reinterpret_cast<float2*>(buo + tc::swizzled32_offset(lg + 8, col0, 32)) =
+            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(40 + lg, col0, X_ROWS)) =
                 make_float2(tf32_round(-cw0[2]), tf32_round(-cw0[3]));
-            *reinterpret_cast<float2*>(buo + tc::swizzled32_offset(lg, col1, 32)) =
+            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(32 + lg, col1, X_ROWS)) =
                 make_float2(tf32_round(-cw1[0]), tf32_round(-cw1[1]));
-            *reinterpret_cast<float2*>(buo + tc::swizzled32_offset(lg + 8, col1, 32)) =
+            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(40 + lg, col1, X_ROWS)) =
                 make_float2(tf32_round(-cw1[2]), tf32_round(-cw1[3]));
-            // generic-proxy writes of this thread -> visible to the tensor core
             tc::fence_proxy_async_smem();
             mbar_arrive(&S.full[cp % kRing]);
         }
     }
 }
 
-// ---- solver warp: (I + A_kk)^-1, T diag(b), A_qk for every chunk ------------------
-__device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* err) {
+// ---- decay-ratio products on the tensor core (A-product warp) -----------------------
+// D (M = 64, N = 16) = [K 2^G ; Q 2^G ; ...] (K 2^-G)^T over the 128 key channels:
+// rows 0-15 = A_kk before diag(b) (TMEM lanes 0-15), rows 16-31 = A_qk (lanes 32-47).
+// This warp reads the A_qk rows and writes the inclusive-lower tf32 operand tile.
+__device__ void aprod(const Unit& U, Smem& S, uint32_t tmem, int lane, int* err) {
+    constexpr uint32_t id = tc::idesc_tf32_f32(64, 16);
+    const uint64_t d_x = tc::smem_desc(smem_u32(S.st[0].x), 16, 1024, tc::kSwizzle128B);
+    const uint32_t tl = tmem + (32u << 16);   // this warp's lane quarter (lanes 32-63)
+    for (int c = 0; c < U.nch; ++c) {
+        const int par = c & 1;
+        bool ok = true;
+        if (c >= 2) ok = mbar_wait(&S.t_ready[par], (unsigned)(((c - 2) >> 1) & 1), err);
+        ok = ok && mbar_wait(&S.kq_ready[par], (unsigned)((c >> 1) & 1), err);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        if (lane == 0) {
+            tc::fence_after_sync();
+            const uint64_t so = (uint64_t)(((c % kRing) * sizeof(Stage)) >> 4);
+            const uint64_t d_ki = tc::smem_desc(smem_u32(S.ki[par]), 16, 1024, tc::kSwizzle128B);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                tc::mma_ss_tf32(tmem + TM_A + 16u * par,
+                                d_x + so + (uint64_t)(((kk >> 2) * X_ROWS * 128 + (kk & 3) * 32) >> 4),
+                                d_ki + (uint64_t)(((kk >> 2) * kChunk * 128 + (kk & 3) * 32) >> 4),
+                                id, kk > 0 ? 1u : 0u);
+            tc::commit(smem_u32(&S.a_done[par]));
+        }
+        __syncwarp();
+        ok = mbar_wait(&S.a_done[par], (unsigned)((c >> 1) & 1), err);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc::fence_after_sync();
+        uint32_t a[16];
+        tc::ld16(tl + TM_A + 16u * par, a);
+        tc::wait_ld();
+        if (lane < kChunk) {   // row t = lane of A_qk
+            unsigned char* aqk = reinterpret_cast<unsigned char*>(S.st[c % kRing].aqk);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float4 f;
+                f.x = (4 * q + 0 <= lane) ? tf32_round(__uint_as_float(a[4 * q + 0])) : 0.0f;
+                f.y = (4 * q + 1 <= lane) ? tf32_round(__uint_as_float(a[4 * q + 1])) : 0.0f;
+                f.z = (4 * q + 2 <= lane) ? tf32_round(__uint_as_float(a[4 * q + 2])) : 0.0f;
+                f.w = (4 * q + 3 <= lane) ? tf32_round(__uint_as_float(a[4 * q + 3])) : 0.0f;
+                *reinterpret_cast<float4*>(aqk + tc::interleaved32_offset(lane, 4 * q, AQ_SBO)) = f;
+            }
+        }
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        mbar_arrive(&S.t_ready[par]);
+    }
+}
+
+// ---- solver warp: (I + diag(b) A_kk)^-1 and T diag(b) for every chunk -----------------
+// A = diag(b) A_kk is strictly lower triangular, so A^16 = 0 and
+//   T = (I + A)^-1 = (I - A)(I + A^2)(I + A^4)(I + A^8)
+// ("Moonshot AI Open-Sources FlashKDA", "What makes the kernel fast": the 16 x 16
+// inverse in fp16).  Twelve m16n8k16 MMAs in registers, fp16 operands, fp32 accumulate;
+// products feed the next MMA as A fragments directly and as B fragments through an
+// 8 x 8 register transpose.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+    return y;
+}
+// C fragments of a 16 x 16 product (two n-tiles) -> its A fragment and B fragments
+__device__ __forceinline__ void frag_a(const float (&c)[2][4], uint32_t (&a)[4]) {
+    a[0] = pack_half2(c[0][0], c[0][1]);
+    a[1] = pack_half2(c[0][2], c[0][3]);
+    a[2] = pack_half2(c[1][0], c[1][1]);
+    a[3] = pack_half2(c[1][2], c[1][3]);
+}
+__device__ __forceinline__ void frag_b(const uint32_t (&a)[4], uint32_t (&b)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) b[i] = movmatrix_t(a[i]);
+}
+// d = c + a * B (two n-tiles of 8 columns)
+__device__ __forceinline__ void mma16(float (&d)[2][4], const uint32_t (&a)[4], const uint32_t (&b)[4]) {
+    mma_f16(d[0], a, b[0], b[1]);
+    mma_f16(d[1], a, b[2], b[3]);
+}
+
+__device__ void solve(const Problem& P, const Unit& U, Smem& S, uint32_t tmem, int lane, int* err) {
     ProdShared& PS = S.pr;
+    const int g = lane >> 2, t = lane & 3;
     // beta logits in windows of 64 tokens (4 chunks), the next window loaded one
     // window ahead: lane i holds tokens 64 j + i and 64 j + 32 + i of window j
     const __nv_bfloat16* beta = P.beta + (size_t)U.tok_start * P.H + U.h;
-    const auto load_window = [&](int j, float& w0, float& w1) {
-        const int t0 = 64 * j + lane, t1 = t0 + 32;
+    const auto load_window = [&](int jw, float& w0, float& w1) {
+        const int t0 = 64 * jw + lane, t1 = t0 + 32;
         w0 = (t0 < U.L) ? __bfloat162float(beta[(size_t)t0 * P.H]) : 0.0f;
         w1 = (t1 < U.L) ? __bfloat162float(beta[(size_t)t1 * P.H]) : 0.0f;
     };
     float bw0 = 0.0f, bw1 = 0.0f, nb0 = 0.0f, nb1 = 0.0f;
     if (U.nch > 0) load_window(0, nb0, nb1);
+    // identity in A-fragment layout: rows g / g+8, columns 2t, 2t+1 / 8+2t, 9+2t
+    const uint32_t id0 = pack_half2(g == 2 * t ? 1.0f : 0.0f, g == 2 * t + 1 ? 1.0f : 0.0f);
     for (int c = 0; c < U.nch; ++c) {
         const int len = min(kChunk, U.L - c * kChunk);
         if ((c & 3) == 0) {
@@ -421,55 +498,77 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
         const float lw = __shfl_sync(0xffffffffu, (c & 2) ? bw1 : bw0, 16 * (c & 1) + (lane & 15));
         const float bl = (lane < len) ? sigmoid_fast(lw) : 0.0f;   // b of row `lane`
         const int par = c & 1;
-        const bool ok = mbar_wait(&S.a_ready[par], (unsigned)((c >> 1) & 1), err);
+        const bool ok = mbar_wait(&S.a_done[par], (unsigned)((c >> 1) & 1), err);
         if (!__all_sync(0xffffffffu, ok)) return;
+        tc::fence_after_sync();
+        uint32_t a[16];
+        tc::ld16(tmem + TM_A + 16u * par, a);   // lane r: row r of A_kk (lanes 0-15)
+        tc::wait_ld();
         Stage& st = S.st[c % kRing];
-        // A_kk = diag(b) (sum of the warps' partials), strictly lower; A_qk inclusive
-        // lower (tf32, interleaved); partials summed in warp order
+        if (lane < kChunk) {   // A = diag(b) A_kk, strictly lower, as an fp16 16 x 16 tile
+            uint32_t h[8];
 #pragma unroll
-        for (int e = 2 * lane; e < kChunk * kChunk; e += 64) {
-            const int r = e >> 4, s = e & 15;
-            float2 sk = make_float2(0.f, 0.f), sq = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int w = 0; w < kProdWarps; ++w) {
-                const float2 pk2 = *reinterpret_cast<const float2*>(&PS.part[par][w][0][e]);
-                const float2 pq2 = *reinterpret_cast<const float2*>(&PS.part[par][w][1][e]);
-                sk.x += pk2.x;
-                sk.y += pk2.y;
-                sq.x += pq2.x;
-                sq.y += pq2.y;
-            }
-            const float br = __shfl_sync(0xffffffffu, bl, r);
-            PS.A[r * A_LD + s] = (s < r) ? br * sk.x : 0.0f;
-            PS.A[r * A_LD + s + 1] = (s + 1 < r) ? br * sk.y : 0.0f;
-            *reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(st.aqk) +
-                                       tc::interleaved32_offset(r, s, AQ_SBO)) =
-                make_float2((s <= r) ? tf32_round(sq.x) : 0.0f, (s + 1 <= r) ? tf32_round(sq.y) : 0.0f);
+            for (int q = 0; q < 8; ++q)
+                h[q] = pack_half2((2 * q < lane) ? bl * __uint_as_float(a[2 * q]) : 0.0f,
+                                  (2 * q + 1 < lane) ? bl * __uint_as_float(a[2 * q + 1]) : 0.0f);
+            uint4* row = reinterpret_cast<uint4*>(&PS.Ah[lane * AH_LD]);
+            row[0] = make_uint4(h[0], h[1], h[2], h[3]);
+            row[1] = make_uint4(h[4], h[5], h[6], h[7]);
         }
         __syncwarp();
-        if (lane < kChunk) {
-            float Tc[kChunk];
+        uint32_t aA[4], bA[4];
+        ldsm_x4(aA, &PS.Ah[(lane & 15) * AH_LD + 8 * (lane >> 4)]);
+        ldsm_x4_t(bA, &PS.Ah[((lane & 7) + 8 * ((lane >> 3) & 1)) * AH_LD + 8 * (lane >> 4)]);
+        // I - A: fragment and fp32 accumulator
+        uint32_t aIA[4];
+        float cI[2][4];
+        {
+            const __half2 i2 = *reinterpret_cast<const __half2*>(&id0);
+            const __half2 z2 = __float2half2_rn(0.0f);
 #pragma unroll
-            for (int i = 0; i < kChunk; ++i) {
-                float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-                for (int m = 0; m + 1 < i; m += 2) {
-                    s0 = fmaf(PS.A[i * A_LD + m], Tc[m], s0);
-                    s1 = fmaf(PS.A[i * A_LD + m + 1], Tc[m + 1], s1);
-                }
-                if (i & 1) s0 = fmaf(PS.A[i * A_LD + i - 1], Tc[i - 1], s0);
-                Tc[i] = (i == lane) ? 1.0f : ((i < lane) ? 0.0f : -(s0 + s1));
+            for (int k = 0; k < 4; ++k) {
+                const __half2 x = *reinterpret_cast<const __half2*>(&aA[k]);
+                const __half2 y = __hsub2((k == 0 || k == 3) ? i2 : z2, x);
+                aIA[k] = *reinterpret_cast<const uint32_t*>(&y);
+                const float2 f = __half22float2(y);
+                cI[k >> 1][2 * (k & 1)] = f.x;
+                cI[k >> 1][2 * (k & 1) + 1] = f.y;
             }
-            unsigned char* tbt = reinterpret_cast<unsigned char*>(st.tbt);
+        }
+        float c2[2][4] = {}, c4[2][4] = {}, c8[2][4] = {};
+        uint32_t aP[4], bA2[4], bA4[4], bA8[4];
+        mma16(c2, aA, bA);                 // A^2
+        frag_a(c2, aP);
+        frag_b(aP, bA2);
+        mma16(c4, aP, bA2);                // A^4
+        mma16(cI, aIA, bA2);               // T1 = (I - A)(I + A^2)
+        frag_a(c4, aP);
+        frag_b(aP, bA4);
+        mma16(c8, aP, bA4);                // A^8
+        frag_a(cI, aP);
+        mma16(cI, aP, bA4);                // T2 = T1 (I + A^4)
+        frag_a(c8, aP);
+        frag_b(aP, bA8);
+        frag_a(cI, aP);
+        mma16(cI, aP, bA8);                // T = T2 (I + A^8)
+        // T diag(b): column n scaled by b_n; rows g, g+8, columns 8 nt + 2t, +1
+        const float b0 = __shfl_sync(0xffffffffu, bl, 2 * t), b1 = __shfl_sync(0xffffffffu, bl, 2 * t + 1);
+        const float b8 = __shfl_sync(0xffffffffu, bl, 8 + 2 * t), b9 = __shfl_sync(0xffffffffu, bl, 9 + 2 * t);
+        unsigned char* tbt = reinterpret_cast<unsigned char*>(st.tbt);
 #pragma unroll
-            for (int i = 0; i < kChunk; ++i) {
-                const __half x = __float2half_rn(Tc[i] * bl);
-                PS.tb[par][i * TB_LD + lane] = x;
-                *reinterpret_cast<__half*>(tbt + tc::interleaved_offset(i, lane, kChunk)) = x;
-            }
+        for (int nt = 0; nt < 2; ++nt) {
+            const float s0 = nt ? b8 : b0, s1 = nt ? b9 : b1;
+            const uint32_t lo = pack_half2(cI[nt][0] * s0, cI[nt][1] * s1);   // row g
+            const uint32_t hi = pack_half2(cI[nt][2] * s0, cI[nt][3] * s1);   // row g + 8
+            const int col = 8 * nt + 2 * t;
+            *reinterpret_cast<uint32_t*>(&PS.tb[par][g * TB_LD + col]) = lo;
+            *reinterpret_cast<uint32_t*>(&PS.tb[par][(g + 8) * TB_LD + col]) = hi;
+            *reinterpret_cast<uint32_t*>(tbt + tc::interleaved_offset(16 + g, col, kChunk)) = lo;
+            *reinterpret_cast<uint32_t*>(tbt + tc::interleaved_offset(24 + g, col, kChunk)) = hi;
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
+        tc::fence_before_sync();
         mbar_arrive(&S.t_ready[par]);
     }
 }
@@ -477,8 +576,8 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
 // ---- sequential stage: tensor-core issue (one thread) -------------------------------
 // Per chunk c (slot s), in the transposed orientation (TMEM lane = value row v), with
 // S^T of the chunk's start in state buffer c & 1:
-//   [U|O] = V^T [T diag(b) ; 0]^T             (u^T into the U half, zeros into O; fp16)
-//   [U|O] += S^T [-w ; Q 2^G]^T               (16 tf32 MMAs over the 128 key channels)
+//   [O|U] = V^T [0 ; T diag(b)]^T             (zeros into O, u^T into U; fp16)
+//   [O|U] += S^T [Q 2^G ; -w]^T               (16 tf32 MMAs over the 128 key channels)
 //   S'^T += U^T (K 2^(G_last-G))              (S'^T = S^T 2^G_last, written by the
 //                                              epilogue into the other state buffer)
 //   O    += U^T A_qk^T
@@ -491,7 +590,7 @@ __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
     // descriptors of slot 0; slot s adds its byte offset >> 4 to the start field
     const uint64_t d_vt = tc::smem_desc(smem_u32(S.st[0].vt), 128, T_SBO, tc::kSwizzleNone);
     const uint64_t d_tbt = tc::smem_desc(smem_u32(S.st[0].tbt), 128, 256, tc::kSwizzleNone);
-    const uint64_t d_buo = tc::smem_desc(smem_u32(S.st[0].buo), 16, 1024, tc::kSwizzle128B);
+    const uint64_t d_xb = tc::smem_desc(smem_u32(S.st[0].x) + 16 * 128, 16, 1024, tc::kSwizzle128B);
     const uint64_t d_kdt = tc::smem_desc(smem_u32(S.st[0].kdt), 128, KD_SBO, tc::kSwizzleNone);
     const uint64_t d_aqk = tc::smem_desc(smem_u32(S.st[0].aqk), 128, AQ_SBO, tc::kSwizzleNone);
     for (int c = 0; c < U.nch; ++c) {
@@ -511,19 +610,26 @@ __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk)
             tc::mma_ts_tf32(uo, sc + 8 * kk,
-                            d_buo + so + (uint64_t)(((kk >> 2) * 4096 + (kk & 3) * 32) >> 4), id_s, 1);
+                            d_xb + so + (uint64_t)(((kk >> 2) * X_ROWS * 128 + (kk & 3) * 32) >> 4),
+                            id_s, 1);
         tc::commit(smem_u32(&S.uo_done));
         if (!mbar_wait(&S.uo_done, (unsigned)(c & 1), err)) return;
         if (!mbar_wait(&S.scaled, (unsigned)(c & 1), err)) return;
         tc::fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
-            tc::mma_ts_tf32(sn, uo + 8 * kk, d_kdt + so + (uint64_t)((kk * 256) >> 4), id_k, 1);
-            tc::mma_ts_tf32(uo + 16, uo + 8 * kk, d_aqk + so + (uint64_t)((kk * 256) >> 4), id_q, 1);
+            tc::mma_ts_tf32(sn, uo + 16 + 8 * kk, d_kdt + so + (uint64_t)((kk * 256) >> 4), id_k, 1);
+            tc::mma_ts_tf32(uo, uo + 16 + 8 * kk, d_aqk + so + (uint64_t)((kk * 256) >> 4), id_q, 1);
         }
         tc::commit(smem_u32(&S.s_done));
         tc::commit(smem_u32(&S.empty[slot]));
     }
+    // Nobody else waits for the last kRing empty-slot commits.  Their arrivals must
+    // land before the CTA exits: a late one would hit the barrier that the next CTA
+    // on this SM initialises at the same shared-memory address.
+    const int first = U.nch > kRing ? U.nch - kRing : 0;
+    for (int c = first; c < U.nch; ++c)
+        if (!mbar_wait(&S.empty[c % kRing], (unsigned)((c / kRing) & 1), err)) return;
 }
 
 __device__ __forceinline__ float state_in(const Problem& P, size_t idx) {
@@ -640,7 +746,7 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
         {
             const int cp = c - 1;
             uint32_t o[16];
-            tc::ld16(tl + TM_UO + 32u * (cp % 3) + 16, o);
+            tc::ld16(tl + TM_UO + 32u * (cp % 3), o);
             tc::wait_ld();
             const int len = min(kChunk, U.L - cp * kChunk);
             __nv_bfloat16* out = P.out + ((size_t)(U.tok_start + cp * kChunk) * P.H + U.h) * kDim + v;
@@ -689,8 +795,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&S.scaled, kEpiWarps * 32);
         mbar_init(&S.epi_done, kEpiWarps * 32);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&S.a_ready[b], kProdThreads);
-            mbar_init(&S.t_ready[b], 32);
+            mbar_init(&S.kq_ready[b], kProdThreads);   // every producer thread
+            mbar_init(&S.a_done[b], 1);                // one tensor-core commit
+            mbar_init(&S.t_ready[b], 64);              // solver + A-product warps
         }
         for (int s = 0; s < kRaw; ++s) {
             mbar_init(&S.raw_full[s], 1);                 // loader's arrive + TMA bytes
@@ -698,10 +805,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
-    // rows 16..31 of every slot's T diag(b) operand stay zero
+    // rows 0..15 of every slot's T diag(b) operand stay zero
     for (int i = threadIdx.x; i < kRing * 16 * 16 / 2; i += kThreads) {
         const int slot = i / 128, e = i % 128;
-        reinterpret_cast<uint32_t*>(S.st[slot].tbt + 16 * 16)[e] = 0u;
+        reinterpret_cast<uint32_t*>(S.st[slot].tbt)[e] = 0u;
     }
     tc::fence_proxy_async_smem();
     if (warp == kMmaWarp) {
@@ -727,7 +834,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     } else if (warp == kSolveWarp) {
-        solve(P, U, S, lane, err);
+        solve(P, U, S, tmem, lane, err);
+    } else if (warp == kAprodWarp) {
+        aprod(U, S, tmem, lane, err);
     } else if (warp == kLoadWarp) {
         if (lane == 0) loader(TM, U, S, err);
     } else {

@@ -189,6 +189,18 @@ def test_deterministic():
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
 
 
+def test_deterministic_across_waves():
+    """Several waves of CTAs per SM (768 units on 152 SMs): repeated calls are bit-identical.
+    Catches state left behind by one CTA that a later CTA on the same SM could see."""
+    import torch
+    d = synth.make_workload("varlen_uniform_8x1024_h96")
+    x = upload(d)
+    o1, s1 = run_gpu(d, x=x)
+    for _ in range(4):
+        o2, s2 = run_gpu(d, x=x)
+        assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
 def test_host_entry_point_matches_device_entry_point():
     import torch
     import gated_delta_rule_39_gb300 as kda
