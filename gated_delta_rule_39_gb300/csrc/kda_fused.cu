@@ -11,9 +11,10 @@
 //                       factors and the operand tiles of the chunk (K 2^G, Q 2^G,
 //                       K 2^-G, K 2^(G_last-G), V), and one chunk later their slice
 //                       of w = T diag(b) (K 2^G).
-//   A-product warp      issues the tcgen05 MMAs of the decay-ratio products
-//                       A_kk = (K 2^G)(K 2^-G)^T and A_qk = (Q 2^G)(K 2^-G)^T and
-//                       writes A_qk (inclusive lower) as an operand tile.
+//   A-product warp      the decay-ratio products A_kk = (K 2^G)(K 2^-G)^T and
+//                       A_qk = (Q 2^G)(K 2^-G)^T (tf32 mma.sync from ldmatrix
+//                       fragments of the operand tiles); A_qk (inclusive lower)
+//                       goes to an operand tile, A_kk to the solver.
 //   solver warp         (I + diag(b) A_kk)^-1 by forward substitution, T diag(b).
 //   MMA warp            issues the tcgen05 MMAs of the recurrence (one thread).
 //   epilogue warps (8)  own the tensor-memory state S^T (lane v = value channel v):
@@ -40,8 +41,8 @@ namespace {
 
 constexpr int kEpiWarps = 8;                // epilogue: two warps per TMEM lane quarter,
                                             // each owning half of the state's columns
-constexpr int kSolveWarp = kEpiWarps;       // lane quarter 0: reads A_kk rows 0-15
-constexpr int kAprodWarp = kSolveWarp + 1;  // lane quarter 1: reads A_qk rows (lanes 32-47)
+constexpr int kSolveWarp = kEpiWarps;       // (I + diag(b) A_kk)^-1
+constexpr int kAprodWarp = kSolveWarp + 1;  // decay-ratio products
 constexpr int kMmaWarp = kAprodWarp + 1;    // recurrence MMAs, owns tensor memory
 constexpr int kProdWarp0 = kMmaWarp + 1;
 constexpr int kProdWarps = 8;               // 16 key channels each
@@ -50,9 +51,9 @@ constexpr int kLoadWarp = kProdWarp0 + kProdWarps;   // TMA loads of the raw row
 constexpr int kRing = 3;                    // chunk-operand slots
 constexpr int kRaw = 4;                     // raw-row slots: chunks in flight from HBM
 constexpr int kThreads = (kLoadWarp + 1) * 32;
-static_assert(kSolveWarp % 4 == 0 && kAprodWarp % 4 == 1, "tensor-memory lane quarters");
 
 constexpr int AH_LD = 24;     // fp16 per row of the solver's A tile (48 B: ldmatrix conflict-free)
+constexpr int AK_LD = 20;     // fp32 per row of A_kk handed to the solver (16-byte rows)
 constexpr int TB_LD = 24;     // fp16 per row of T diag(b) (48 B: ldmatrix conflict-free)
 constexpr int KG_LD = 24;     // fp16 per row of a warp's K 2^G tile (48 B)
 constexpr int T_SBO = 272;    // byte step between 8-row groups of the transposed fp16
@@ -65,15 +66,14 @@ constexpr int X_ROWS = 48;    // rows of the [K 2^G ; Q 2^G ; -w] tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_S = 0;       // S^T, fp32: two buffers of 128 columns (chunk parity)
 constexpr uint32_t TM_UO = 256;    // [O | U] accumulators: three buffers of 32 columns
-constexpr uint32_t TM_A = 352;     // A_kk / A_qk products (M = 64): two buffers of 16 columns
 
 // One chunk's operands for the tensor-core recurrence (canonical K-major layouts).
 // The operands multiplied by the fp32 state or by U are fp32 values rounded to
 // tf32 (kind::tf32 MMAs read the state and U straight from tensor memory).
 struct Stage {
     // rows 0-15 K 2^G, rows 16-31 Q 2^G, rows 32-47 -w; 128 key channels; 128B swizzle,
-    // [K block of 32 channels][48 rows][128 bytes].  Rows 0-31 are the A operand of
-    // the decay-ratio products, rows 16-47 the B operand of [O|U] += S^T [Q 2^G ; -w]^T.
+    // [K block of 32 channels][48 rows][128 bytes].  Rows 0-31 feed the decay-ratio
+    // products, rows 16-47 are the B operand of [O|U] += S^T [Q 2^G ; -w]^T.
     float x[4 * X_ROWS * 32];
     float kdt[16 * KD_SBO / 4];    // B of the state update: (K 2^(G_last-G))^T 128 x 16
     float aqk[2 * AQ_SBO / 4];     // B of O += U A_qk^T: A_qk 16 x 16
@@ -93,13 +93,12 @@ static_assert(kRawBytes == 16384, "four tensors x 16 rows x 256 bytes");
 struct ProdShared {
     __half tb[2][kChunk * TB_LD];                  // T diag(b) per chunk parity
     __half kg[kProdWarps][2][kChunk * KG_LD];      // each warp's K 2^G tile per chunk parity
+    float Akk[2][kChunk * AK_LD];                  // A_kk (before diag(b)) per chunk parity
     __half Ah[kChunk * AH_LD];                     // solver: diag(b) A_kk, strictly lower
 };
 struct Smem {
     Stage st[kRing];
-    // K 2^-G per chunk parity ([K block][16 rows][128 bytes], 128B swizzle): B operand of
-    // the decay-ratio products.  (Their M = 64 A operand, rows 0-63 of a stage's x tile,
-    // reads 2 KB past the tile's last block, into the same stage's kdt tile.)
+    // K 2^-G per chunk parity ([K block][16 rows][128 bytes], 128B swizzle)
     float ki[2][4 * kChunk * 32];
     RawSlot raw[kRaw];
     ProdShared pr;
@@ -108,8 +107,8 @@ struct Smem {
     unsigned long long full[kRing];      // producers -> MMA / epilogue
     unsigned long long empty[kRing];     // MMA commit -> producers
     unsigned long long kq_ready[2];      // producers: product operands written
-    unsigned long long a_done[2];        // decay-ratio MMAs complete
-    unsigned long long t_ready[2];       // solver (T diag b) and A-product warp (A_qk) done
+    unsigned long long a_ready[2];       // A-product warp: A_kk and A_qk written
+    unsigned long long t_ready[2];       // solver: T diag(b) written
     unsigned long long uo_done;          // O|U MMAs complete
     unsigned long long s_done;           // state update + O MMAs complete
     unsigned long long init_ready;       // epilogue: initial state written
@@ -193,7 +192,12 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t raw) {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&raw);
     return __bfloat1622float2(v);
 }
-__device__ __forceinline__ float tf32_round(float x) { return __uint_as_float(to_tf32(x)); }
+// fp32 -> tf32 (10 mantissa bits kept): add half a tf32 ulp to the bit pattern and
+// clear the 13 dropped bits, i.e. round half away from zero in two integer operations
+// (Inf and NaN stay Inf and NaN; the largest finite values round up to Inf).
+__device__ __forceinline__ float tf32_round(float x) {
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+}
 
 struct Unit {
     int n, h, tok_start, L, nch;
@@ -393,54 +397,54 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
     }
 }
 
-// ---- decay-ratio products on the tensor core (A-product warp) -----------------------
-// D (M = 64, N = 16) = [K 2^G ; Q 2^G ; ...] (K 2^-G)^T over the 128 key channels:
-// rows 0-15 = A_kk before diag(b) (TMEM lanes 0-15), rows 16-31 = A_qk (lanes 32-47).
-// This warp reads the A_qk rows and writes the inclusive-lower tf32 operand tile.
-__device__ void aprod(const Unit& U, Smem& S, uint32_t tmem, int lane, int* err) {
-    constexpr uint32_t id = tc::idesc_tf32_f32(64, 16);
-    const uint64_t d_x = tc::smem_desc(smem_u32(S.st[0].x), 16, 1024, tc::kSwizzle128B);
-    const uint32_t tl = tmem + (32u << 16);   // this warp's lane quarter (lanes 32-63)
+// ---- decay-ratio products (A-product warp) -----------------------------------------
+// A_kk = (K 2^G)(K 2^-G)^T and A_qk = (Q 2^G)(K 2^-G)^T over the 128 key channels:
+// 16 k-steps of m16n8k8 tf32 MMAs (two n-tiles each), fragments loaded with ldmatrix
+// from the swizzled operand tiles (an 8 x 8 b16 matrix = 8 rows x 4 fp32).
+__device__ void aprod(const Unit& U, Smem& S, int lane, int* err) {
+    ProdShared& PS = S.pr;
+    const int g = lane >> 2, t = lane & 3;
+    const int m = lane >> 3, i8 = lane & 7;   // ldmatrix: matrix and row this lane addresses
     for (int c = 0; c < U.nch; ++c) {
         const int par = c & 1;
         bool ok = true;
         if (c >= 2) ok = mbar_wait(&S.t_ready[par], (unsigned)(((c - 2) >> 1) & 1), err);
         ok = ok && mbar_wait(&S.kq_ready[par], (unsigned)((c >> 1) & 1), err);
         if (!__all_sync(0xffffffffu, ok)) return;
-        if (lane == 0) {
-            tc::fence_after_sync();
-            const uint64_t so = (uint64_t)(((c % kRing) * sizeof(Stage)) >> 4);
-            const uint64_t d_ki = tc::smem_desc(smem_u32(S.ki[par]), 16, 1024, tc::kSwizzle128B);
-#pragma unroll
-            for (int kk = 0; kk < 16; ++kk)
-                tc::mma_ss_tf32(tmem + TM_A + 16u * par,
-                                d_x + so + (uint64_t)(((kk >> 2) * X_ROWS * 128 + (kk & 3) * 32) >> 4),
-                                d_ki + (uint64_t)(((kk >> 2) * kChunk * 128 + (kk & 3) * 32) >> 4),
-                                id, kk > 0 ? 1u : 0u);
-            tc::commit(smem_u32(&S.a_done[par]));
+        const unsigned char* x = reinterpret_cast<const unsigned char*>(S.st[c % kRing].x);
+        const unsigned char* ki = reinterpret_cast<const unsigned char*>(S.ki[par]);
+        float ck[2][4] = {}, cq[2][4] = {};
+#pragma unroll 4
+        for (int kk = 0; kk < 16; ++kk) {
+            // A fragments: matrices (rows 0-7 | 8-15) x (channels 8kk .. +3 | +4 .. +7)
+            const int ar = (m & 1) * 8 + i8, af = 8 * kk + 4 * (m >> 1);
+            // B fragments: matrices (tokens 0-7 | 8-15) x (channels 8kk .. +3 | +4 .. +7)
+            const int br = (m >> 1) * 8 + i8, bf = 8 * kk + 4 * (m & 1);
+            uint32_t aK[4], aQ[4], bK[4];
+            ldsm_x4(aK, x + tc::swizzled32_offset(ar, af, X_ROWS));
+            ldsm_x4(aQ, x + tc::swizzled32_offset(16 + ar, af, X_ROWS));
+            ldsm_x4(bK, ki + tc::swizzled32_offset(br, bf, kChunk));
+            mma_tf32(ck[0], aK, bK[0], bK[1]);
+            mma_tf32(ck[1], aK, bK[2], bK[3]);
+            mma_tf32(cq[0], aQ, bK[0], bK[1]);
+            mma_tf32(cq[1], aQ, bK[2], bK[3]);
         }
-        __syncwarp();
-        ok = mbar_wait(&S.a_done[par], (unsigned)((c >> 1) & 1), err);
-        if (!__all_sync(0xffffffffu, ok)) return;
-        tc::fence_after_sync();
-        uint32_t a[16];
-        tc::ld16(tl + TM_A + 16u * par, a);
-        tc::wait_ld();
-        if (lane < kChunk) {   // row t = lane of A_qk
-            unsigned char* aqk = reinterpret_cast<unsigned char*>(S.st[c % kRing].aqk);
+        // rows g, g + 8; columns (tokens s) 8 nt + 2t, + 1
+        unsigned char* aqk = reinterpret_cast<unsigned char*>(S.st[c % kRing].aqk);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float4 f;
-                f.x = (4 * q + 0 <= lane) ? tf32_round(__uint_as_float(a[4 * q + 0])) : 0.0f;
-                f.y = (4 * q + 1 <= lane) ? tf32_round(__uint_as_float(a[4 * q + 1])) : 0.0f;
-                f.z = (4 * q + 2 <= lane) ? tf32_round(__uint_as_float(a[4 * q + 2])) : 0.0f;
-                f.w = (4 * q + 3 <= lane) ? tf32_round(__uint_as_float(a[4 * q + 3])) : 0.0f;
-                *reinterpret_cast<float4*>(aqk + tc::interleaved32_offset(lane, 4 * q, AQ_SBO)) = f;
-            }
+        for (int nt = 0; nt < 2; ++nt) {
+            const int s0 = 8 * nt + 2 * t;
+            *reinterpret_cast<float2*>(&PS.Akk[par][g * AK_LD + s0]) = make_float2(ck[nt][0], ck[nt][1]);
+            *reinterpret_cast<float2*>(&PS.Akk[par][(g + 8) * AK_LD + s0]) = make_float2(ck[nt][2], ck[nt][3]);
+            // A_qk inclusive lower (s <= row), tf32, K-major operand tile
+            *reinterpret_cast<float2*>(aqk + tc::interleaved32_offset(g, s0, AQ_SBO)) =
+                make_float2(s0 <= g ? tf32_round(cq[nt][0]) : 0.0f, s0 + 1 <= g ? tf32_round(cq[nt][1]) : 0.0f);
+            *reinterpret_cast<float2*>(aqk + tc::interleaved32_offset(g + 8, s0, AQ_SBO)) =
+                make_float2(s0 <= g + 8 ? tf32_round(cq[nt][2]) : 0.0f,
+                            s0 + 1 <= g + 8 ? tf32_round(cq[nt][3]) : 0.0f);
         }
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        mbar_arrive(&S.t_ready[par]);
+        tc::fence_proxy_async_smem();   // the A_qk tile is read by the chain's MMA
+        mbar_arrive(&S.a_ready[par]);
     }
 }
 
@@ -473,7 +477,7 @@ __device__ __forceinline__ void mma16(float (&d)[2][4], const uint32_t (&a)[4], 
     mma_f16(d[1], a, b[2], b[3]);
 }
 
-__device__ void solve(const Problem& P, const Unit& U, Smem& S, uint32_t tmem, int lane, int* err) {
+__device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* err) {
     ProdShared& PS = S.pr;
     const int g = lane >> 2, t = lane & 3;
     // beta logits in windows of 64 tokens (4 chunks), the next window loaded one
@@ -498,19 +502,24 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, uint32_t tmem, i
         const float lw = __shfl_sync(0xffffffffu, (c & 2) ? bw1 : bw0, 16 * (c & 1) + (lane & 15));
         const float bl = (lane < len) ? sigmoid_fast(lw) : 0.0f;   // b of row `lane`
         const int par = c & 1;
-        const bool ok = mbar_wait(&S.a_done[par], (unsigned)((c >> 1) & 1), err);
+        const bool ok = mbar_wait(&S.a_ready[par], (unsigned)((c >> 1) & 1), err);
         if (!__all_sync(0xffffffffu, ok)) return;
-        tc::fence_after_sync();
-        uint32_t a[16];
-        tc::ld16(tmem + TM_A + 16u * par, a);   // lane r: row r of A_kk (lanes 0-15)
-        tc::wait_ld();
         Stage& st = S.st[c % kRing];
         if (lane < kChunk) {   // A = diag(b) A_kk, strictly lower, as an fp16 16 x 16 tile
+            float a[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 f = *reinterpret_cast<const float4*>(&PS.Akk[par][lane * AK_LD + 4 * q]);
+                a[4 * q] = f.x;
+                a[4 * q + 1] = f.y;
+                a[4 * q + 2] = f.z;
+                a[4 * q + 3] = f.w;
+            }
             uint32_t h[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-                h[q] = pack_half2((2 * q < lane) ? bl * __uint_as_float(a[2 * q]) : 0.0f,
-                                  (2 * q + 1 < lane) ? bl * __uint_as_float(a[2 * q + 1]) : 0.0f);
+                h[q] = pack_half2((2 * q < lane) ? bl * a[2 * q] : 0.0f,
+                                  (2 * q + 1 < lane) ? bl * a[2 * q + 1] : 0.0f);
             uint4* row = reinterpret_cast<uint4*>(&PS.Ah[lane * AH_LD]);
             row[0] = make_uint4(h[0], h[1], h[2], h[3]);
             row[1] = make_uint4(h[4], h[5], h[6], h[7]);
@@ -568,7 +577,6 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, uint32_t tmem, i
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
-        tc::fence_before_sync();
         mbar_arrive(&S.t_ready[par]);
     }
 }
@@ -796,8 +804,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&S.epi_done, kEpiWarps * 32);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&S.kq_ready[b], kProdThreads);   // every producer thread
-            mbar_init(&S.a_done[b], 1);                // one tensor-core commit
-            mbar_init(&S.t_ready[b], 64);              // solver + A-product warps
+            mbar_init(&S.a_ready[b], 32);              // A-product warp
+            mbar_init(&S.t_ready[b], 32);              // solver warp
         }
         for (int s = 0; s < kRaw; ++s) {
             mbar_init(&S.raw_full[s], 1);                 // loader's arrive + TMA bytes
@@ -834,9 +842,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     } else if (warp == kSolveWarp) {
-        solve(P, U, S, tmem, lane, err);
+        solve(P, U, S, lane, err);
     } else if (warp == kAprodWarp) {
-        aprod(U, S, tmem, lane, err);
+        aprod(U, S, lane, err);
     } else if (warp == kLoadWarp) {
         if (lane == 0) loader(TM, U, S, err);
     } else {

@@ -9,7 +9,7 @@
 //   - the sequential state recurrence runs on tcgen05 tensor cores with the
 //     state S and U = u - w S held in tensor memory as fp32 and read directly
 //     as the A operand of kind::tf32 MMAs; their partners (w, Q*2^G,
-//     K*2^(G_C-G), A_qk) are fp32 rounded to tf32 (round to nearest).
+//     K*2^(G_C-G), A_qk) are fp32 rounded to tf32 (half away from zero).
 //   - u = T diag(b) V: fp16 operands (V is bf16 data; the WY inverse's inputs
 //     lie in [-1, 1], "Moonshot AI Open-Sources FlashKDA", "What makes the
 //     kernel fast": fp16 16x16 inversion), fp32 accumulate.  w = T diag(b)
@@ -82,11 +82,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // sigmoid(x) = 1 / (1 + 2^(-x log2 e))
 __device__ __forceinline__ float sigmoid_fast(float x) {
     return rcp_approx(1.0f + ex2_approx(-x * kLog2e));
-}
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
 }
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
