@@ -17,7 +17,7 @@
 //                       goes to an operand tile, A_kk to the solver.
 //   solver warp         (I + diag(b) A_kk)^-1 by forward substitution, T diag(b).
 //   MMA warp            issues the tcgen05 MMAs of the recurrence (one thread).
-//   epilogue warps (8)  own the tensor-memory state S^T (lane v = value channel v):
+//   epilogue warps (4)  own the tensor-memory state S^T (lane v = value channel v):
 //                       decay rescale, outputs, initial and final state.
 //
 // Chunkwise DPLR-variant (WY) algorithm with 16-token chunks, a 16 x 16
@@ -39,8 +39,7 @@ namespace kda {
 
 namespace {
 
-constexpr int kEpiWarps = 8;                // epilogue: two warps per TMEM lane quarter,
-                                            // each owning half of the state's columns
+constexpr int kEpiWarps = 4;                // epilogue: one warp per TMEM lane quarter
 constexpr int kSolveWarp = kEpiWarps;       // (I + diag(b) A_kk)^-1
 constexpr int kAprodWarp = kSolveWarp + 1;  // decay-ratio products
 constexpr int kMmaWarp = kAprodWarp + 1;    // recurrence MMAs, owns tensor memory
@@ -653,11 +652,11 @@ __device__ __forceinline__ void state_out(const Problem& P, size_t idx, float x)
 }
 
 // ---- sequential stage: epilogue ---------------------------------------------------
-// Warp ew reaches TMEM lanes 32 (ew % 4) .. + 31 (thread = value channel v) and
-// owns half of the state's columns (key channels 64 (ew / 4) .. + 63) and the
-// outputs of tokens 8 (ew / 4) .. + 7.  Once the state of chunk c's start is
-// complete, it writes 2^G_last(c) times it into the other state buffer, which the
-// update MMAs of chunk c accumulate into while the U|O MMAs still read the first.
+// Warp ew reaches TMEM lanes 32 ew .. + 31 (thread = value channel v) and owns all
+// 128 state columns and the 16 outputs of those lanes.  Once the state of chunk c's
+// start is complete, it writes 2^G_last(c) times it into the other state buffer,
+// which the update MMAs of chunk c accumulate into while the U|O MMAs still read
+// the first.
 __device__ __forceinline__ void scale32(uint32_t (&x)[32], const float* gc) {
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
@@ -675,23 +674,21 @@ __device__ __forceinline__ void scale32(uint32_t (&x)[32], const float* gc) {
 
 __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem, int ew,
                          int lane, int* err) {
-    const int quarter = ew & 3, colhalf = ew >> 2;
-    const int v = 32 * quarter + lane;
-    const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);   // this warp's lane quarter
+    const int v = 32 * ew + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * ew) << 16);   // this warp's lane quarter
     const size_t sbase = ((size_t)U.n * P.H + U.h) * kDim * kDim + v;   // + c * kDim
-    const int p0 = 2 * colhalf;   // this warp's two 32-column pieces: p0, p0 + 1
     bool ok = true;
 
     if (U.nch == 0) {   // no tokens: the final state is the initial state
         if (P.final_state)
-            for (int c = 64 * colhalf; c < 64 * colhalf + 64; ++c)
+            for (int c = 0; c < kDim; ++c)
                 state_out(P, sbase + (size_t)c * kDim,
                           P.init_state ? state_in(P, sbase + (size_t)c * kDim) : 0.0f);
         return;
     }
     // initial state S0 into buffer 0, then S0 Diag(2^G_last of chunk 0) into buffer 1
 #pragma unroll 1
-    for (int piece = p0; piece < p0 + 2; ++piece) {
+    for (int piece = 0; piece < 4; ++piece) {
         uint32_t x[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -706,7 +703,7 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
     ok = mbar_wait(&S.full[0], 0u, err);
     if (!__all_sync(0xffffffffu, ok)) return;
 #pragma unroll 1
-    for (int piece = p0; piece < p0 + 2; ++piece) {
+    for (int piece = 0; piece < 4; ++piece) {
         uint32_t x[32];
         tc::ld32(tl + TM_S + 32 * piece, x);
         tc::wait_ld();
@@ -717,23 +714,27 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
     tc::fence_before_sync();
     mbar_arrive(&S.scaled);
 
+    // slot / phase of chunk c in the operand ring, and the [O|U] buffer of chunk c - 1
+    int slot = 1 % kRing, phase = (1 / kRing) & 1, uob = 0;
+    __nv_bfloat16* out = P.out + ((size_t)U.tok_start * P.H + U.h) * kDim + v;
+    const size_t out_step = (size_t)P.H * kDim;   // elements between consecutive tokens
     for (int c = 1; c <= U.nch; ++c) {
         // chunk c - 1 finished: its end state is in buffer c & 1
         ok = mbar_wait(&S.s_done, (unsigned)((c - 1) & 1), err);
         const bool more = c < U.nch;
-        const int slot = c % kRing;
-        if (more) ok = ok && mbar_wait(&S.full[slot], (unsigned)((c / kRing) & 1), err);
+        if (more) ok = ok && mbar_wait(&S.full[slot], (unsigned)phase, err);
         if (!__all_sync(0xffffffffu, ok)) return;
         tc::fence_after_sync();
         const uint32_t sc = tl + TM_S + 128u * (c & 1);
         if (more) {
             const uint32_t sn = tl + TM_S + 128u * ((c + 1) & 1);
+            const float* gc = S.st[slot].gc;
 #pragma unroll 1
-            for (int piece = p0; piece < p0 + 2; ++piece) {
+            for (int piece = 0; piece < 4; ++piece) {
                 uint32_t x[32];
                 tc::ld32(sc + 32 * piece, x);
                 tc::wait_ld();
-                scale32(x, S.st[slot].gc + 32 * piece);
+                scale32(x, gc + 32 * piece);
                 tc::st32(sn + 32 * piece, x);
             }
             tc::wait_st();
@@ -741,7 +742,7 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
             mbar_arrive(&S.scaled);
         } else if (P.final_state) {
 #pragma unroll 1
-            for (int piece = p0; piece < p0 + 2; ++piece) {
+            for (int piece = 0; piece < 4; ++piece) {
                 uint32_t x[32];
                 tc::ld32(sc + 32 * piece, x);
                 tc::wait_ld();
@@ -750,22 +751,22 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
                     state_out(P, sbase + (size_t)(32 * piece + i) * kDim, __uint_as_float(x[i]));
             }
         }
-        // outputs of chunk c - 1, tokens 8 colhalf .. + 7: O^T lane v, column t
+        // outputs of chunk c - 1: O^T lane v, column t = token
         {
-            const int cp = c - 1;
             uint32_t o[16];
-            tc::ld16(tl + TM_UO + 32u * (cp % 3), o);
+            tc::ld16(tl + TM_UO + 32u * uob, o);
             tc::wait_ld();
-            const int len = min(kChunk, U.L - cp * kChunk);
-            __nv_bfloat16* out = P.out + ((size_t)(U.tok_start + cp * kChunk) * P.H + U.h) * kDim + v;
+            const int len = min(kChunk, U.L - (c - 1) * kChunk);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int t = 8 * colhalf + j;
-                const uint32_t ov = colhalf ? o[8 + j] : o[j];
-                if (t < len)
-                    out[(size_t)t * P.H * kDim] = __float2bfloat16_rn(P.scale * __uint_as_float(ov));
-            }
+            for (int t = 0; t < kChunk; ++t)
+                if (t < len) out[t * out_step] = __float2bfloat16_rn(P.scale * __uint_as_float(o[t]));
+            out += kChunk * out_step;
         }
+        if (++slot == kRing) {
+            slot = 0;
+            phase ^= 1;
+        }
+        if (++uob == 3) uob = 0;
     }
 }
 
