@@ -11,10 +11,9 @@
 //                       factors and the operand tiles of the chunk (K 2^G, Q 2^G,
 //                       K 2^-G, K 2^(G_last-G), V), and one chunk later their slice
 //                       of w = T diag(b) (K 2^G).
-//   A-product warp      the decay-ratio products A_kk = (K 2^G)(K 2^-G)^T and
-//                       A_qk = (Q 2^G)(K 2^-G)^T (tf32 mma.sync from ldmatrix
-//                       fragments of the operand tiles); A_qk (inclusive lower)
-//                       goes to an operand tile, A_kk to the solver.
+//   A-product warps (2) the decay-ratio products A_kk = (K 2^G)(K 2^-G)^T (to the
+//                       solver) and A_qk = (Q 2^G)(K 2^-G)^T (inclusive lower, to
+//                       an operand tile): tf32 mma.sync from ldmatrix fragments.
 //   solver warp         (I + diag(b) A_kk)^-1 by forward substitution, T diag(b).
 //   MMA warp            issues the tcgen05 MMAs of the recurrence (one thread).
 //   epilogue warps (4)  own the tensor-memory state S^T (lane v = value channel v):
@@ -41,8 +40,8 @@ namespace {
 
 constexpr int kEpiWarps = 4;                // epilogue: one warp per TMEM lane quarter
 constexpr int kSolveWarp = kEpiWarps;       // (I + diag(b) A_kk)^-1
-constexpr int kAprodWarp = kSolveWarp + 1;  // decay-ratio products
-constexpr int kMmaWarp = kAprodWarp + 1;    // recurrence MMAs, owns tensor memory
+constexpr int kAprodWarp = kSolveWarp + 1;  // decay-ratio products: A_kk, then A_qk
+constexpr int kMmaWarp = kAprodWarp + 2;    // recurrence MMAs, owns tensor memory
 constexpr int kProdWarp0 = kMmaWarp + 1;
 constexpr int kProdWarps = 8;               // 16 key channels each
 constexpr int kProdThreads = kProdWarps * 32;
@@ -106,8 +105,8 @@ struct Smem {
     unsigned long long full[kRing];      // producers -> MMA / epilogue
     unsigned long long empty[kRing];     // MMA commit -> producers
     unsigned long long kq_ready[2];      // producers: product operands written
-    unsigned long long a_ready[2];       // A-product warp: A_kk and A_qk written
-    unsigned long long t_ready[2];       // solver: T diag(b) written
+    unsigned long long a_ready[2];       // A_kk written
+    unsigned long long t_ready[2];       // solver (T diag(b)) and A_qk warp done
     unsigned long long uo_done;          // O|U MMAs complete
     unsigned long long s_done;           // state update + O MMAs complete
     unsigned long long init_ready;       // epilogue: initial state written
@@ -396,14 +395,17 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
     }
 }
 
-// ---- decay-ratio products (A-product warp) -----------------------------------------
-// A_kk = (K 2^G)(K 2^-G)^T and A_qk = (Q 2^G)(K 2^-G)^T over the 128 key channels:
-// 16 k-steps of m16n8k8 tf32 MMAs (two n-tiles each), fragments loaded with ldmatrix
-// from the swizzled operand tiles (an 8 x 8 b16 matrix = 8 rows x 4 fp32).
-__device__ void aprod(const Unit& U, Smem& S, int lane, int* err) {
+// ---- decay-ratio products (A-product warps) ----------------------------------------
+// Warp 0 computes A_kk = (K 2^G)(K 2^-G)^T, warp 1 A_qk = (Q 2^G)(K 2^-G)^T, over the
+// 128 key channels: m16n8k8 tf32 MMAs, fragments loaded with ldmatrix from the
+// swizzled operand tiles (an 8 x 8 b16 matrix = 8 rows x 4 fp32).  Four independent
+// accumulators per warp (two n-tiles x two channel halves) keep the MMA chains short;
+// the halves are added in a fixed order.
+__device__ void aprod(const Unit& U, Smem& S, int which, int lane, int* err) {
     ProdShared& PS = S.pr;
     const int g = lane >> 2, t = lane & 3;
     const int m = lane >> 3, i8 = lane & 7;   // ldmatrix: matrix and row this lane addresses
+    const int arow0 = 16 * which;            // rows of K 2^G (0) or Q 2^G (16) in the x tile
     for (int c = 0; c < U.nch; ++c) {
         const int par = c & 1;
         bool ok = true;
@@ -412,38 +414,46 @@ __device__ void aprod(const Unit& U, Smem& S, int lane, int* err) {
         if (!__all_sync(0xffffffffu, ok)) return;
         const unsigned char* x = reinterpret_cast<const unsigned char*>(S.st[c % kRing].x);
         const unsigned char* ki = reinterpret_cast<const unsigned char*>(S.ki[par]);
-        float ck[2][4] = {}, cq[2][4] = {};
+        float acc[2][2][4] = {};   // [channel half][n-tile][fragment]
 #pragma unroll 4
-        for (int kk = 0; kk < 16; ++kk) {
-            // A fragments: matrices (rows 0-7 | 8-15) x (channels 8kk .. +3 | +4 .. +7)
-            const int ar = (m & 1) * 8 + i8, af = 8 * kk + 4 * (m >> 1);
-            // B fragments: matrices (tokens 0-7 | 8-15) x (channels 8kk .. +3 | +4 .. +7)
-            const int br = (m >> 1) * 8 + i8, bf = 8 * kk + 4 * (m & 1);
-            uint32_t aK[4], aQ[4], bK[4];
-            ldsm_x4(aK, x + tc::swizzled32_offset(ar, af, X_ROWS));
-            ldsm_x4(aQ, x + tc::swizzled32_offset(16 + ar, af, X_ROWS));
-            ldsm_x4(bK, ki + tc::swizzled32_offset(br, bf, kChunk));
-            mma_tf32(ck[0], aK, bK[0], bK[1]);
-            mma_tf32(ck[1], aK, bK[2], bK[3]);
-            mma_tf32(cq[0], aQ, bK[0], bK[1]);
-            mma_tf32(cq[1], aQ, bK[2], bK[3]);
+        for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int k8 = kk + 8 * hh;
+                // A: matrices (rows 0-7 | 8-15) x (channels 8 k8 .. +3 | +4 .. +7)
+                // B: matrices (tokens 0-7 | 8-15) x (channels 8 k8 .. +3 | +4 .. +7)
+                uint32_t a4[4], b4[4];
+                ldsm_x4(a4, x + tc::swizzled32_offset(arow0 + (m & 1) * 8 + i8, 8 * k8 + 4 * (m >> 1), X_ROWS));
+                ldsm_x4(b4, ki + tc::swizzled32_offset((m >> 1) * 8 + i8, 8 * k8 + 4 * (m & 1), kChunk));
+                mma_tf32(acc[hh][0], a4, b4[0], b4[1]);
+                mma_tf32(acc[hh][1], a4, b4[2], b4[3]);
+            }
         }
         // rows g, g + 8; columns (tokens s) 8 nt + 2t, + 1
         unsigned char* aqk = reinterpret_cast<unsigned char*>(S.st[c % kRing].aqk);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             const int s0 = 8 * nt + 2 * t;
-            *reinterpret_cast<float2*>(&PS.Akk[par][g * AK_LD + s0]) = make_float2(ck[nt][0], ck[nt][1]);
-            *reinterpret_cast<float2*>(&PS.Akk[par][(g + 8) * AK_LD + s0]) = make_float2(ck[nt][2], ck[nt][3]);
-            // A_qk inclusive lower (s <= row), tf32, K-major operand tile
-            *reinterpret_cast<float2*>(aqk + tc::interleaved32_offset(g, s0, AQ_SBO)) =
-                make_float2(s0 <= g ? tf32_round(cq[nt][0]) : 0.0f, s0 + 1 <= g ? tf32_round(cq[nt][1]) : 0.0f);
-            *reinterpret_cast<float2*>(aqk + tc::interleaved32_offset(g + 8, s0, AQ_SBO)) =
-                make_float2(s0 <= g + 8 ? tf32_round(cq[nt][2]) : 0.0f,
-                            s0 + 1 <= g + 8 ? tf32_round(cq[nt][3]) : 0.0f);
+            float r[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) r[e] = acc[0][nt][e] + acc[1][nt][e];
+            if (which == 0) {
+                *reinterpret_cast<float2*>(&PS.Akk[par][g * AK_LD + s0]) = make_float2(r[0], r[1]);
+                *reinterpret_cast<float2*>(&PS.Akk[par][(g + 8) * AK_LD + s0]) = make_float2(r[2], r[3]);
+            } else {   // A_qk inclusive lower (s <= row), tf32, K-major operand tile
+                *reinterpret_cast<float2*>(aqk + tc::interleaved32_offset(g, s0, AQ_SBO)) =
+                    make_float2(s0 <= g ? tf32_round(r[0]) : 0.0f, s0 + 1 <= g ? tf32_round(r[1]) : 0.0f);
+                *reinterpret_cast<float2*>(aqk + tc::interleaved32_offset(g + 8, s0, AQ_SBO)) =
+                    make_float2(s0 <= g + 8 ? tf32_round(r[2]) : 0.0f,
+                                s0 + 1 <= g + 8 ? tf32_round(r[3]) : 0.0f);
+            }
         }
-        tc::fence_proxy_async_smem();   // the A_qk tile is read by the chain's MMA
-        mbar_arrive(&S.a_ready[par]);
+        if (which == 0) {
+            mbar_arrive(&S.a_ready[par]);
+        } else {
+            tc::fence_proxy_async_smem();   // the A_qk tile is read by the chain's MMA
+            mbar_arrive(&S.t_ready[par]);
+        }
     }
 }
 
@@ -806,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&S.kq_ready[b], kProdThreads);   // every producer thread
             mbar_init(&S.a_ready[b], 32);              // A-product warp
-            mbar_init(&S.t_ready[b], 32);              // solver warp
+            mbar_init(&S.t_ready[b], 64);              // solver + A_qk warp
         }
         for (int s = 0; s < kRaw; ++s) {
             mbar_init(&S.raw_full[s], 1);                 // loader's arrive + TMA bytes
@@ -844,8 +854,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_dealloc(tmem, kTmemCols);
     } else if (warp == kSolveWarp) {
         solve(P, U, S, lane, err);
-    } else if (warp == kAprodWarp) {
-        aprod(U, S, lane, err);
+    } else if (warp == kAprodWarp || warp == kAprodWarp + 1) {
+        aprod(U, S, warp - kAprodWarp, lane, err);
     } else if (warp == kLoadWarp) {
         if (lane == 0) loader(TM, U, S, err);
     } else {
