@@ -9,11 +9,12 @@
 //                       consecutive rows of the 16-token chunk.  They compute the
 //                       gates, the in-chunk cumulative base-2 log-decay G, the decay
 //                       factors and the operand tiles of the chunk (K 2^G, Q 2^G,
-//                       K 2^-G, K 2^(G_last-G), V), and one chunk later their slice
-//                       of w = T diag(b) (K 2^G).
+//                       K 2^-G, K 2^(G_last-G), V), up to kRing chunks ahead.
 //   A-product warps (2) the decay-ratio products A_kk = (K 2^G)(K 2^-G)^T (to the
 //                       solver) and A_qk = (Q 2^G)(K 2^-G)^T (inclusive lower, to
 //                       an operand tile): tf32 mma.sync from ldmatrix fragments.
+//   w warps (2)         once the solver has T: -w = -T diag(b)(K 2^G), 64 channels
+//                       each, which completes the chunk's operands.
 //   solver warp         (I + diag(b) A_kk)^-1 by forward substitution, T diag(b).
 //   MMA warp            issues the tcgen05 MMAs of the recurrence (one thread).
 //   epilogue warps (4)  own the tensor-memory state S^T (lane v = value channel v):
@@ -41,7 +42,8 @@ namespace {
 constexpr int kEpiWarps = 4;                // epilogue: one warp per TMEM lane quarter
 constexpr int kSolveWarp = kEpiWarps;       // (I + diag(b) A_kk)^-1
 constexpr int kAprodWarp = kSolveWarp + 1;  // decay-ratio products: A_kk, then A_qk
-constexpr int kMmaWarp = kAprodWarp + 2;    // recurrence MMAs, owns tensor memory
+constexpr int kWWarp = kAprodWarp + 2;      // -w, 64 channels each (two warps)
+constexpr int kMmaWarp = kWWarp + 2;        // recurrence MMAs, owns tensor memory
 constexpr int kProdWarp0 = kMmaWarp + 1;
 constexpr int kProdWarps = 8;               // 16 key channels each
 constexpr int kProdThreads = kProdWarps * 32;
@@ -53,7 +55,7 @@ constexpr int kThreads = (kLoadWarp + 1) * 32;
 constexpr int AH_LD = 24;     // fp16 per row of the solver's A tile (48 B: ldmatrix conflict-free)
 constexpr int AK_LD = 20;     // fp32 per row of A_kk handed to the solver (16-byte rows)
 constexpr int TB_LD = 24;     // fp16 per row of T diag(b) (48 B: ldmatrix conflict-free)
-constexpr int KG_LD = 24;     // fp16 per row of a warp's K 2^G tile (48 B)
+constexpr int KGH_LD = 136;   // fp16 per row of the K 2^G tile (272 B: ldmatrix conflict-free)
 constexpr int T_SBO = 272;    // byte step between 8-row groups of the transposed fp16
                               // 128 x 16 tile (16 bytes past 256 spreads row groups over banks)
 constexpr int KD_SBO = 528;   // same for the fp32 128 x 16 tile
@@ -73,12 +75,14 @@ struct Stage {
     // [K block of 32 channels][48 rows][128 bytes].  Rows 0-31 feed the decay-ratio
     // products, rows 16-47 are the B operand of [O|U] += S^T [Q 2^G ; -w]^T.
     float x[4 * X_ROWS * 32];
+    float ki[4 * kChunk * 32];     // K 2^-G, [K block][16 rows][128 bytes], 128B swizzle
     float kdt[16 * KD_SBO / 4];    // B of the state update: (K 2^(G_last-G))^T 128 x 16
     float aqk[2 * AQ_SBO / 4];     // B of O += U A_qk^T: A_qk 16 x 16
     __half vt[16 * T_SBO / 2];     // A of u^T = V^T (T diag b)^T: V^T 128 x 16, interleaved
     __half tbt[32 * 16];           // B of the u MMA: rows 0-15 zero, rows 16-31 T diag(b)
     float gc[kDim];                // 2^G_last
-    unsigned char pad_[1024];      // keep sizeof(Stage) a multiple of 1024
+    __half kgh[kChunk * KGH_LD];   // K 2^G in fp16, [token][channel]: B of w = T diag(b) K 2^G
+    __half tbr[kChunk * TB_LD];    // T diag(b) fp16 row-major: A of w (sizeof(Stage) % 1024 == 0)
 };
 static_assert(sizeof(Stage) % 1024 == 0, "stages keep the swizzled tiles 1024-byte aligned");
 // One chunk's raw rows of q, k, v, g as the TMA engine writes them: per tensor two
@@ -89,24 +93,20 @@ struct RawSlot {
 constexpr uint32_t kRawBytes = sizeof(RawSlot);
 static_assert(kRawBytes == 16384, "four tensors x 16 rows x 256 bytes");
 struct ProdShared {
-    __half tb[2][kChunk * TB_LD];                  // T diag(b) per chunk parity
-    __half kg[kProdWarps][2][kChunk * KG_LD];      // each warp's K 2^G tile per chunk parity
     float Akk[2][kChunk * AK_LD];                  // A_kk (before diag(b)) per chunk parity
     __half Ah[kChunk * AH_LD];                     // solver: diag(b) A_kk, strictly lower
 };
 struct Smem {
     Stage st[kRing];
-    // K 2^-G per chunk parity ([K block][16 rows][128 bytes], 128B swizzle)
-    float ki[2][4 * kChunk * 32];
     RawSlot raw[kRaw];
     ProdShared pr;
     unsigned long long raw_full[kRaw];   // TMA bytes landed
     unsigned long long raw_empty[kRaw];  // producers have read the slot
-    unsigned long long full[kRing];      // producers -> MMA / epilogue
+    unsigned long long full[kRing];      // operands complete (-w written) -> MMA / epilogue
     unsigned long long empty[kRing];     // MMA commit -> producers
-    unsigned long long kq_ready[2];      // producers: product operands written
-    unsigned long long a_ready[2];       // A_kk written
-    unsigned long long t_ready[2];       // solver (T diag(b)) and A_qk warp done
+    unsigned long long kq_ready[kRing];  // producers: the chunk's tiles written
+    unsigned long long a_ready[2];       // A-product warps: A_kk / A_qk written
+    unsigned long long t_ready[kRing];   // solver: T diag(b) written
     unsigned long long uo_done;          // O|U MMAs complete
     unsigned long long s_done;           // state update + O MMAs complete
     unsigned long long init_ready;       // epilogue: initial state written
@@ -251,10 +251,8 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
     const int half = w >> 2;
     const int chunk16 = 2 * (w & 3) + (pi >> 2);
     const int inoff = 4 * (pi & 3);
-    ProdShared& PS = S.pr;
-
-    for (int c = 0; c <= U.nch; ++c) {
-        if (c < U.nch) {
+    for (int c = 0; c < U.nch; ++c) {
+        {
             const int len = min(kChunk, U.L - c * kChunk);
             const int rslot = c % kRaw;
             bool ok = mbar_wait(&S.raw_full[rslot], (unsigned)((c / kRaw) & 1), err);
@@ -284,7 +282,6 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
             mbar_arrive(&S.raw_empty[rslot]);
             const int slot = c % kRing;
             Stage& st = S.st[slot];
-            const int par = c & 1;
             if (c >= kRing) ok = mbar_wait(&S.empty[slot], (unsigned)(((c / kRing) - 1) & 1), err);
             if (!__all_sync(0xffffffffu, ok)) return;
 
@@ -321,8 +318,7 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
 
             // decay factors and operand tiles
             unsigned char* x = reinterpret_cast<unsigned char*>(st.x);
-            unsigned char* ki = reinterpret_cast<unsigned char*>(S.ki[par]);
-            __half* kgt = PS.kg[w][par];
+            unsigned char* ki = reinterpret_cast<unsigned char*>(st.ki);
             float kd0[4], kd1[4];
             __half v0[4], v1[4];
 #pragma unroll
@@ -342,7 +338,7 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
                     make_float2(tf32_round(qg.x), tf32_round(qg.y));
                 *reinterpret_cast<float2*>(ki + tc::swizzled32_offset(r, c0, kChunk)) =
                     make_float2(tf32_round(kin.x), tf32_round(kin.y));
-                *reinterpret_cast<uint32_t*>(&kgt[r * KG_LD + 2 * pi]) = pack_half2(kg.x, kg.y);
+                *reinterpret_cast<uint32_t*>(&st.kgh[r * KGH_LD + c0]) = pack_half2(kg.x, kg.y);
                 kd0[i] = tf32_round(kd.x);
                 kd1[i] = tf32_round(kd.y);
                 v0[i] = __float2half_rn(vv.x);
@@ -362,35 +358,7 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
                 make_uint2(pack_halves(v1[0], v1[1]), pack_halves(v1[2], v1[3]));
             // generic-proxy writes of this thread -> visible to the tensor core
             tc::fence_proxy_async_smem();
-            mbar_arrive(&S.kq_ready[par]);
-        }
-        // ---- one chunk behind: w = T diag(b)(K 2^G) for this warp's channels -------
-        if (c >= 1) {
-            const int cp = c - 1;
-            const int par = cp & 1;
-            const bool ok = mbar_wait(&S.t_ready[par], (unsigned)((cp >> 1) & 1), err);
-            if (!__all_sync(0xffffffffu, ok)) return;
-            __syncwarp();
-            Stage& st = S.st[cp % kRing];
-            unsigned char* x = reinterpret_cast<unsigned char*>(st.x);
-            uint32_t ta[4], b[4];
-            ldsm_x4(ta, &PS.tb[par][((lane & 7) + 8 * ((lane >> 3) & 1)) * TB_LD + 8 * (lane >> 4)]);
-            ldsm_x4_t(b, &PS.kg[w][par][((lane & 7) + 8 * ((lane >> 3) & 1)) * KG_LD + 8 * (lane >> 4)]);
-            float cw0[4] = {}, cw1[4] = {};
-            mma_f16(cw0, ta, b[0], b[1]);
-            mma_f16(cw1, ta, b[2], b[3]);
-            const int lg = lane >> 2, lt = lane & 3;
-            const int col0 = 16 * w + 2 * lt, col1 = col0 + 8;
-            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(32 + lg, col0, X_ROWS)) =
-                make_float2(tf32_round(-cw0[0]), tf32_round(-cw0[1]));
-            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(40 + lg, col0, X_ROWS)) =
-                make_float2(tf32_round(-cw0[2]), tf32_round(-cw0[3]));
-            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(32 + lg, col1, X_ROWS)) =
-                make_float2(tf32_round(-cw1[0]), tf32_round(-cw1[1]));
-            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(40 + lg, col1, X_ROWS)) =
-                make_float2(tf32_round(-cw1[2]), tf32_round(-cw1[3]));
-            tc::fence_proxy_async_smem();
-            mbar_arrive(&S.full[cp % kRing]);
+            mbar_arrive(&S.kq_ready[slot]);
         }
     }
 }
@@ -407,13 +375,14 @@ __device__ void aprod(const Unit& U, Smem& S, int which, int lane, int* err) {
     const int m = lane >> 3, i8 = lane & 7;   // ldmatrix: matrix and row this lane addresses
     const int arow0 = 16 * which;            // rows of K 2^G (0) or Q 2^G (16) in the x tile
     for (int c = 0; c < U.nch; ++c) {
-        const int par = c & 1;
-        bool ok = true;
-        if (c >= 2) ok = mbar_wait(&S.t_ready[par], (unsigned)(((c - 2) >> 1) & 1), err);
-        ok = ok && mbar_wait(&S.kq_ready[par], (unsigned)((c >> 1) & 1), err);
+        const int par = c & 1, slot = c % kRing;
+        bool ok = mbar_wait(&S.kq_ready[slot], (unsigned)((c / kRing) & 1), err);
+        // A_kk buffer of this parity: the solver is done with chunk c - 2
+        if (c >= 2) ok = ok && mbar_wait(&S.t_ready[(c - 2) % kRing], (unsigned)(((c - 2) / kRing) & 1), err);
         if (!__all_sync(0xffffffffu, ok)) return;
-        const unsigned char* x = reinterpret_cast<const unsigned char*>(S.st[c % kRing].x);
-        const unsigned char* ki = reinterpret_cast<const unsigned char*>(S.ki[par]);
+        Stage& st = S.st[slot];
+        const unsigned char* x = reinterpret_cast<const unsigned char*>(st.x);
+        const unsigned char* ki = reinterpret_cast<const unsigned char*>(st.ki);
         float acc[2][2][4] = {};   // [channel half][n-tile][fragment]
 #pragma unroll 4
         for (int kk = 0; kk < 8; ++kk) {
@@ -430,7 +399,7 @@ __device__ void aprod(const Unit& U, Smem& S, int which, int lane, int* err) {
             }
         }
         // rows g, g + 8; columns (tokens s) 8 nt + 2t, + 1
-        unsigned char* aqk = reinterpret_cast<unsigned char*>(S.st[c % kRing].aqk);
+        unsigned char* aqk = reinterpret_cast<unsigned char*>(st.aqk);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             const int s0 = 8 * nt + 2 * t;
@@ -448,12 +417,44 @@ __device__ void aprod(const Unit& U, Smem& S, int which, int lane, int* err) {
                                 s0 + 1 <= g + 8 ? tf32_round(r[3]) : 0.0f);
             }
         }
-        if (which == 0) {
-            mbar_arrive(&S.a_ready[par]);
-        } else {
-            tc::fence_proxy_async_smem();   // the A_qk tile is read by the chain's MMA
-            mbar_arrive(&S.t_ready[par]);
+        if (which == 1) tc::fence_proxy_async_smem();   // the A_qk tile is read by the chain's MMA
+        mbar_arrive(&S.a_ready[par]);
+    }
+}
+
+// ---- w warps: -w = -T diag(b)(K 2^G) for channels 64 which .. + 63 -------------------
+// fp16 m16n8k16 MMAs: A = T diag(b) (row-major fp16), B = K 2^G (fp16 [token][channel]);
+// the result, negated and rounded to tf32, fills rows 32-47 of the x tile.
+__device__ void wcalc(const Unit& U, Smem& S, int which, int lane, int* err) {
+    const int g = lane >> 2, t = lane & 3;
+    for (int c = 0; c < U.nch; ++c) {
+        const int slot = c % kRing;
+        const bool ok = mbar_wait(&S.t_ready[slot], (unsigned)((c / kRing) & 1), err);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        Stage& st = S.st[slot];
+        unsigned char* x = reinterpret_cast<unsigned char*>(st.x);
+        uint32_t ta[4];
+        ldsm_x4(ta, &st.tbr[((lane & 7) + 8 * ((lane >> 3) & 1)) * TB_LD + 8 * (lane >> 4)]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {   // 16 channels per step: two n-tiles
+            const int cb = 64 * which + 16 * q;
+            uint32_t b[4];
+            ldsm_x4_t(b, &st.kgh[((lane & 7) + 8 * ((lane >> 3) & 1)) * KGH_LD + cb + 8 * (lane >> 4)]);
+            float cw0[4] = {}, cw1[4] = {};
+            mma_f16(cw0, ta, b[0], b[1]);
+            mma_f16(cw1, ta, b[2], b[3]);
+            const int col0 = cb + 2 * t, col1 = col0 + 8;
+            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(32 + g, col0, X_ROWS)) =
+                make_float2(tf32_round(-cw0[0]), tf32_round(-cw0[1]));
+            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(40 + g, col0, X_ROWS)) =
+                make_float2(tf32_round(-cw0[2]), tf32_round(-cw0[3]));
+            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(32 + g, col1, X_ROWS)) =
+                make_float2(tf32_round(-cw1[0]), tf32_round(-cw1[1]));
+            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(40 + g, col1, X_ROWS)) =
+                make_float2(tf32_round(-cw1[2]), tf32_round(-cw1[3]));
         }
+        tc::fence_proxy_async_smem();   // -w is read by the chain's MMA
+        mbar_arrive(&S.full[slot]);
     }
 }
 
@@ -579,14 +580,14 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
             const uint32_t lo = pack_half2(cI[nt][0] * s0, cI[nt][1] * s1);   // row g
             const uint32_t hi = pack_half2(cI[nt][2] * s0, cI[nt][3] * s1);   // row g + 8
             const int col = 8 * nt + 2 * t;
-            *reinterpret_cast<uint32_t*>(&PS.tb[par][g * TB_LD + col]) = lo;
-            *reinterpret_cast<uint32_t*>(&PS.tb[par][(g + 8) * TB_LD + col]) = hi;
+            *reinterpret_cast<uint32_t*>(&st.tbr[g * TB_LD + col]) = lo;
+            *reinterpret_cast<uint32_t*>(&st.tbr[(g + 8) * TB_LD + col]) = hi;
             *reinterpret_cast<uint32_t*>(tbt + tc::interleaved_offset(16 + g, col, kChunk)) = lo;
             *reinterpret_cast<uint32_t*>(tbt + tc::interleaved_offset(24 + g, col, kChunk)) = hi;
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
-        mbar_arrive(&S.t_ready[par]);
+        mbar_arrive(&S.t_ready[c % kRing]);
     }
 }
 
@@ -805,7 +806,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRing; ++s) {
-            mbar_init(&S.full[s], kProdThreads);   // every producer thread
+            mbar_init(&S.full[s], 64);             // both w warps
+            mbar_init(&S.kq_ready[s], kProdThreads);   // every producer thread
+            mbar_init(&S.t_ready[s], 32);          // solver warp
             mbar_init(&S.empty[s], 1);             // one tensor-core commit
         }
         mbar_init(&S.uo_done, 1);
@@ -814,9 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&S.scaled, kEpiWarps * 32);
         mbar_init(&S.epi_done, kEpiWarps * 32);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&S.kq_ready[b], kProdThreads);   // every producer thread
-            mbar_init(&S.a_ready[b], 32);              // A-product warp
-            mbar_init(&S.t_ready[b], 64);              // solver + A_qk warp
+            mbar_init(&S.a_ready[b], 64);              // both A-product warps
         }
         for (int s = 0; s < kRaw; ++s) {
             mbar_init(&S.raw_full[s], 1);                 // loader's arrive + TMA bytes
@@ -856,6 +857,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         solve(P, U, S, lane, err);
     } else if (warp == kAprodWarp || warp == kAprodWarp + 1) {
         aprod(U, S, warp - kAprodWarp, lane, err);
+    } else if (warp == kWWarp || warp == kWWarp + 1) {
+        wcalc(U, S, warp - kWWarp, lane, err);
     } else if (warp == kLoadWarp) {
         if (lane == 0) loader(TM, U, S, err);
     } else {
