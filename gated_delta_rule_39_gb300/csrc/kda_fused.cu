@@ -40,17 +40,54 @@ namespace kda {
 namespace {
 
 constexpr int kEpiWarps = 4;                // epilogue: one warp per TMEM lane quarter
-constexpr int kSolveWarp = kEpiWarps;       // (I + diag(b) A_kk)^-1
-constexpr int kAprodWarp = kSolveWarp + 1;  // decay-ratio products: A_kk, then A_qk
-constexpr int kWWarp = kAprodWarp + 2;      // -w, 64 channels each (two warps)
-constexpr int kMmaWarp = kWWarp + 2;        // recurrence MMAs, owns tensor memory
-constexpr int kProdWarp0 = kMmaWarp + 1;
 constexpr int kProdWarps = 8;               // 16 key channels each
 constexpr int kProdThreads = kProdWarps * 32;
-constexpr int kLoadWarp = kProdWarp0 + kProdWarps;   // TMA loads of the raw rows (one lane)
 constexpr int kRing = 3;                    // chunk-operand slots
 constexpr int kRaw = 4;                     // raw-row slots: chunks in flight from HBM
-constexpr int kThreads = (kLoadWarp + 1) * 32;
+
+// Warp roles.  A warp's SM sub-partition (scheduler) is its index mod 4, so the
+// placement decides which roles share issue slots; the producers (most of the
+// instructions) are spread two per sub-partition.  Epilogue warp q must have
+// index = q (mod 4) to reach TMEM lanes 32q .. 32q + 31.
+enum Role : uint8_t { kEpi, kSolve, kAprod0, kAprod1, kW0, kW1, kMma, kProd, kLoad };
+constexpr int kNumWarps = 19;
+constexpr int kThreads = kNumWarps * 32;
+__host__ __device__ constexpr Role role_of(int warp) {
+    switch (warp) {
+        case 0: case 1: case 2: case 3: return kEpi;   // lane quarters 0-3
+        case 4: return kSolve;                          // sub-partition 0
+        case 5: return kW0;                             // 1
+        case 6: return kAprod1;                         // 2
+        case 7: return kAprod0;                         // 3 (the only single-warp role there)
+        case 8: return kW1;                             // 0
+        case 9: return kMma;                            // 1
+        case 18: return kLoad;                          // 2
+        default: return kProd;                          // 10-17: two per sub-partition
+    }
+}
+// producer slice of warp i: its rank among the producer warps
+__host__ __device__ constexpr int prod_index(int warp) {
+    int n = 0;
+    for (int i = 0; i < warp; ++i) n += role_of(i) == kProd;
+    return n;
+}
+__host__ __device__ constexpr int count_role(Role r) {
+    int n = 0;
+    for (int i = 0; i < kNumWarps; ++i) n += role_of(i) == r;
+    return n;
+}
+__host__ __device__ constexpr int find_role(Role r) {
+    for (int i = 0; i < kNumWarps; ++i)
+        if (role_of(i) == r) return i;
+    return -1;
+}
+static_assert(count_role(kProd) == kProdWarps && count_role(kEpi) == kEpiWarps, "role table");
+static_assert(count_role(kSolve) == 1 && count_role(kMma) == 1 && count_role(kLoad) == 1 &&
+              count_role(kAprod0) == 1 && count_role(kAprod1) == 1 && count_role(kW0) == 1 &&
+              count_role(kW1) == 1, "role table");
+static_assert(role_of(0) == kEpi && role_of(1) == kEpi && role_of(2) == kEpi && role_of(3) == kEpi,
+              "epilogue warps 0-3 own lane quarters 0-3");
+constexpr int kMmaWarp = find_role(kMma);
 
 constexpr int AH_LD = 24;     // fp16 per row of the solver's A tile (48 B: ldmatrix conflict-free)
 constexpr int AK_LD = 20;     // fp32 per row of A_kk handed to the solver (16-byte rows)
@@ -840,11 +877,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem = S.tmem_base;
 
-    if (warp < kEpiWarps) {
+    const Role role = role_of(warp);
+    if (role == kEpi) {
         epilogue(P, U, S, tmem, warp, lane, err);
         tc::fence_before_sync();
         mbar_arrive(&S.epi_done);
-    } else if (warp == kMmaWarp) {
+    } else if (role == kMma) {
         if (lane == 0) mma_issuer(U, S, tmem, err);
         __syncwarp();
         // free tensor memory once the epilogue is done with it
@@ -853,16 +891,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)ok;
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
-    } else if (warp == kSolveWarp) {
+    } else if (role == kSolve) {
         solve(P, U, S, lane, err);
-    } else if (warp == kAprodWarp || warp == kAprodWarp + 1) {
-        aprod(U, S, warp - kAprodWarp, lane, err);
-    } else if (warp == kWWarp || warp == kWWarp + 1) {
-        wcalc(U, S, warp - kWWarp, lane, err);
-    } else if (warp == kLoadWarp) {
+    } else if (role == kAprod0 || role == kAprod1) {
+        aprod(U, S, role == kAprod1, lane, err);
+    } else if (role == kW0 || role == kW1) {
+        wcalc(U, S, role == kW1, lane, err);
+    } else if (role == kLoad) {
         if (lane == 0) loader(TM, U, S, err);
     } else {
-        produce(P, U, S, warp - kProdWarp0, lane, err);
+        produce(P, U, S, prod_index(warp), lane, err);
     }
 }
 
