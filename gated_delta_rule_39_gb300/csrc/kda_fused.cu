@@ -227,11 +227,12 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t raw) {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&raw);
     return __bfloat1622float2(v);
 }
-// fp32 -> tf32 (10 mantissa bits kept): add half a tf32 ulp to the bit pattern and
-// clear the 13 dropped bits, i.e. round half away from zero in two integer operations
-// (Inf and NaN stay Inf and NaN; the largest finite values round up to Inf).
+// fp32 -> tf32 operand (10 mantissa bits used): add half a tf32 ulp to the bit
+// pattern.  The tensor cores read only the top 19 bits of an fp32 operand (measured:
+// results are bit-identical to clearing the 13 low bits first), so the operand they
+// see is the value rounded half away from zero, for one integer addition.
 __device__ __forceinline__ float tf32_round(float x) {
-    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+    return __uint_as_float(__float_as_uint(x) + 0x1000u);
 }
 
 struct Unit {
