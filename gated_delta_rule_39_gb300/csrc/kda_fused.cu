@@ -42,8 +42,9 @@ namespace {
 constexpr int kEpiWarps = 4;                // epilogue: one warp per TMEM lane quarter
 constexpr int kProdWarps = 8;               // 16 key channels each
 constexpr int kProdThreads = kProdWarps * 32;
-constexpr int kRing = 3;                    // chunk-operand slots
-constexpr int kRaw = 4;                     // raw-row slots: chunks in flight from HBM
+constexpr int kRing = 4;                    // chunk-operand slots (live until the recurrence is done)
+constexpr int kEarly = 2;                   // K 2^G / K 2^-G slots (live until the products are done)
+constexpr int kRaw = 3;                     // raw-row slots: chunks in flight from HBM
 
 // Warp roles.  A warp's SM sub-partition (scheduler) is its index mod 4, so the
 // placement decides which roles share issue slots; the producers (most of the
@@ -89,15 +90,12 @@ static_assert(role_of(0) == kEpi && role_of(1) == kEpi && role_of(2) == kEpi && 
               "epilogue warps 0-3 own lane quarters 0-3");
 constexpr int kMmaWarp = find_role(kMma);
 
-constexpr int AH_LD = 24;     // fp16 per row of the solver's A tile (48 B: ldmatrix conflict-free)
 constexpr int AK_LD = 20;     // fp32 per row of A_kk handed to the solver (16-byte rows)
 constexpr int TB_LD = 24;     // fp16 per row of T diag(b) (48 B: ldmatrix conflict-free)
-constexpr int KGH_LD = 136;   // fp16 per row of the K 2^G tile (272 B: ldmatrix conflict-free)
-constexpr int T_SBO = 272;    // byte step between 8-row groups of the transposed fp16
-                              // 128 x 16 tile (16 bytes past 256 spreads row groups over banks)
+constexpr int T_SBO = 256;    // byte step between 8-row groups of the transposed fp16 128 x 16 tile
 constexpr int KD_SBO = 528;   // same for the fp32 128 x 16 tile
 constexpr int AQ_SBO = 512;   // fp32 16 x 16 A_qk tile
-constexpr int X_ROWS = 48;    // rows of the [K 2^G ; Q 2^G ; -w] tile
+constexpr int X_ROWS = 32;    // rows of the [Q 2^G ; -w] tile
 
 // tensor-memory columns (one allocation of 512)
 constexpr uint32_t kTmemCols = 512;
@@ -108,20 +106,30 @@ constexpr uint32_t TM_UO = 256;    // [O | U] accumulators: three buffers of 32 
 // The operands multiplied by the fp32 state or by U are fp32 values rounded to
 // tf32 (kind::tf32 MMAs read the state and U straight from tensor memory).
 struct Stage {
-    // rows 0-15 K 2^G, rows 16-31 Q 2^G, rows 32-47 -w; 128 key channels; 128B swizzle,
-    // [K block of 32 channels][48 rows][128 bytes].  Rows 0-31 feed the decay-ratio
-    // products, rows 16-47 are the B operand of [O|U] += S^T [Q 2^G ; -w]^T.
+    // rows 0-15 Q 2^G, rows 16-31 -w; 128 key channels; 128B swizzle, [K block of 32
+    // channels][32 rows][128 bytes]: the B operand of [O|U] += S^T [Q 2^G ; -w]^T
     float x[4 * X_ROWS * 32];
-    float ki[4 * kChunk * 32];     // K 2^-G, [K block][16 rows][128 bytes], 128B swizzle
     float kdt[16 * KD_SBO / 4];    // B of the state update: (K 2^(G_last-G))^T 128 x 16
     float aqk[2 * AQ_SBO / 4];     // B of O += U A_qk^T: A_qk 16 x 16
     __half vt[16 * T_SBO / 2];     // A of u^T = V^T (T diag b)^T: V^T 128 x 16, interleaved
-    __half tbt[32 * 16];           // B of the u MMA: rows 0-15 zero, rows 16-31 T diag(b)
+    __half tbt[16 * 16];           // B of the u MMA: T diag(b), 16 x 16, interleaved
     float gc[kDim];                // 2^G_last
-    __half kgh[kChunk * KGH_LD];   // K 2^G in fp16, [token][channel]: B of w = T diag(b) K 2^G
-    __half tbr[kChunk * TB_LD];    // T diag(b) fp16 row-major: A of w (sizeof(Stage) % 1024 == 0)
+    __half kgh[kChunk * kDim];     // K 2^G in fp16, [token][channel] (kgh_offset): B of w
+    __half tbr[kChunk * TB_LD];    // T diag(b) fp16 row-major: A of w
+};
+// K 2^G and K 2^-G (tf32, [K block][16 rows][128 bytes], 128B swizzle): read only by
+// the decay-ratio products, so they live in a shorter ring than the operand stages.
+struct EarlySlot {
+    float kg[4 * kChunk * 32];
+    float ki[4 * kChunk * 32];
 };
 static_assert(sizeof(Stage) % 1024 == 0, "stages keep the swizzled tiles 1024-byte aligned");
+// fp16 K 2^G tile: 256-byte rows, 16-byte chunks XOR-swizzled by row % 8 so that the
+// eight rows an ldmatrix reads fall in distinct banks.  Byte offset of (row, col).
+__device__ __forceinline__ int kgh_offset(int row, int col) {
+    return row * 256 + ((((col >> 3) ^ (row & 7))) << 4) + (col & 7) * 2;
+}
+
 // One chunk's raw rows of q, k, v, g as the TMA engine writes them: per tensor two
 // boxes of 16 rows x 64 channels (128 bytes per row, 128-byte swizzle).
 struct RawSlot {
@@ -131,10 +139,10 @@ constexpr uint32_t kRawBytes = sizeof(RawSlot);
 static_assert(kRawBytes == 16384, "four tensors x 16 rows x 256 bytes");
 struct ProdShared {
     float Akk[2][kChunk * AK_LD];                  // A_kk (before diag(b)) per chunk parity
-    __half Ah[kChunk * AH_LD];                     // solver: diag(b) A_kk, strictly lower
 };
 struct Smem {
     Stage st[kRing];
+    EarlySlot early[kEarly];
     RawSlot raw[kRaw];
     ProdShared pr;
     unsigned long long raw_full[kRaw];   // TMA bytes landed
@@ -144,6 +152,7 @@ struct Smem {
     unsigned long long kq_ready[kRing];  // producers: the chunk's tiles written
     unsigned long long a_ready[2];       // A-product warps: A_kk / A_qk written
     unsigned long long t_ready[kRing];   // solver: T diag(b) written
+    unsigned long long e_free[kEarly];   // both A-product warps are done with the early slot
     unsigned long long uo_done;          // O|U MMAs complete
     unsigned long long s_done;           // state update + O MMAs complete
     unsigned long long init_ready;       // epilogue: initial state written
@@ -355,8 +364,13 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
             if (j == 0) *reinterpret_cast<float2*>(&st.gc[c0]) = gc;
 
             // decay factors and operand tiles
+            // the early slot of this parity: both A-product warps are done with chunk c - 2
+            if (c >= kEarly)
+                ok = mbar_wait(&S.e_free[c & 1], (unsigned)(((c - kEarly) >> 1) & 1), err);
+            if (!__all_sync(0xffffffffu, ok)) return;
             unsigned char* x = reinterpret_cast<unsigned char*>(st.x);
-            unsigned char* ki = reinterpret_cast<unsigned char*>(st.ki);
+            unsigned char* kge = reinterpret_cast<unsigned char*>(S.early[c & 1].kg);
+            unsigned char* ki = reinterpret_cast<unsigned char*>(S.early[c & 1].ki);
             float kd0[4], kd1[4];
             __half v0[4], v1[4];
 #pragma unroll
@@ -370,13 +384,14 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
                 const float2 qg = f2mul(bf2_to_f2(rq[i]), e);
                 const float2 kd = f2mul(kin, gc);
                 const float2 vv = bf2_to_f2(rv[i]);
-                *reinterpret_cast<float2*>(x + tc::swizzled32_offset(r, c0, X_ROWS)) =
+                *reinterpret_cast<float2*>(kge + tc::swizzled32_offset(r, c0, kChunk)) =
                     make_float2(tf32_round(kg.x), tf32_round(kg.y));
-                *reinterpret_cast<float2*>(x + tc::swizzled32_offset(16 + r, c0, X_ROWS)) =
+                *reinterpret_cast<float2*>(x + tc::swizzled32_offset(r, c0, X_ROWS)) =
                     make_float2(tf32_round(qg.x), tf32_round(qg.y));
                 *reinterpret_cast<float2*>(ki + tc::swizzled32_offset(r, c0, kChunk)) =
                     make_float2(tf32_round(kin.x), tf32_round(kin.y));
-                *reinterpret_cast<uint32_t*>(&st.kgh[r * KGH_LD + c0]) = pack_half2(kg.x, kg.y);
+                *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(st.kgh) + kgh_offset(r, c0)) =
+                    pack_half2(kg.x, kg.y);
                 kd0[i] = tf32_round(kd.x);
                 kd1[i] = tf32_round(kd.y);
                 v0[i] = __float2half_rn(vv.x);
@@ -411,7 +426,7 @@ __device__ void aprod(const Unit& U, Smem& S, int which, int lane, int* err) {
     ProdShared& PS = S.pr;
     const int g = lane >> 2, t = lane & 3;
     const int m = lane >> 3, i8 = lane & 7;   // ldmatrix: matrix and row this lane addresses
-    const int arow0 = 16 * which;            // rows of K 2^G (0) or Q 2^G (16) in the x tile
+
     for (int c = 0; c < U.nch; ++c) {
         const int par = c & 1, slot = c % kRing;
         bool ok = mbar_wait(&S.kq_ready[slot], (unsigned)((c / kRing) & 1), err);
@@ -419,8 +434,11 @@ __device__ void aprod(const Unit& U, Smem& S, int which, int lane, int* err) {
         if (c >= 2) ok = ok && mbar_wait(&S.t_ready[(c - 2) % kRing], (unsigned)(((c - 2) / kRing) & 1), err);
         if (!__all_sync(0xffffffffu, ok)) return;
         Stage& st = S.st[slot];
-        const unsigned char* x = reinterpret_cast<const unsigned char*>(st.x);
-        const unsigned char* ki = reinterpret_cast<const unsigned char*>(st.ki);
+        // A operand: K 2^G (early slot) or Q 2^G (rows 0-15 of the x tile)
+        const unsigned char* xa = which ? reinterpret_cast<const unsigned char*>(st.x)
+                                        : reinterpret_cast<const unsigned char*>(S.early[par].kg);
+        const int xrows = which ? X_ROWS : kChunk;
+        const unsigned char* ki = reinterpret_cast<const unsigned char*>(S.early[par].ki);
         float acc[2][2][4] = {};   // [channel half][n-tile][fragment]
 #pragma unroll 4
         for (int kk = 0; kk < 8; ++kk) {
@@ -430,12 +448,13 @@ __device__ void aprod(const Unit& U, Smem& S, int which, int lane, int* err) {
                 // A: matrices (rows 0-7 | 8-15) x (channels 8 k8 .. +3 | +4 .. +7)
                 // B: matrices (tokens 0-7 | 8-15) x (channels 8 k8 .. +3 | +4 .. +7)
                 uint32_t a4[4], b4[4];
-                ldsm_x4(a4, x + tc::swizzled32_offset(arow0 + (m & 1) * 8 + i8, 8 * k8 + 4 * (m >> 1), X_ROWS));
+                ldsm_x4(a4, xa + tc::swizzled32_offset((m & 1) * 8 + i8, 8 * k8 + 4 * (m >> 1), xrows));
                 ldsm_x4(b4, ki + tc::swizzled32_offset((m >> 1) * 8 + i8, 8 * k8 + 4 * (m & 1), kChunk));
                 mma_tf32(acc[hh][0], a4, b4[0], b4[1]);
                 mma_tf32(acc[hh][1], a4, b4[2], b4[3]);
             }
         }
+        mbar_arrive(&S.e_free[par]);   // the early slot's tiles are no longer read
         // rows g, g + 8; columns (tokens s) 8 nt + 2t, + 1
         unsigned char* aqk = reinterpret_cast<unsigned char*>(st.aqk);
 #pragma unroll
@@ -462,7 +481,7 @@ __device__ void aprod(const Unit& U, Smem& S, int which, int lane, int* err) {
 
 // ---- w warps: -w = -T diag(b)(K 2^G) for channels 64 which .. + 63 -------------------
 // fp16 m16n8k16 MMAs: A = T diag(b) (row-major fp16), B = K 2^G (fp16 [token][channel]);
-// the result, negated and rounded to tf32, fills rows 32-47 of the x tile.
+// the result, negated and rounded to tf32, fills rows 16-31 of the x tile.
 __device__ void wcalc(const Unit& U, Smem& S, int which, int lane, int* err) {
     const int g = lane >> 2, t = lane & 3;
     for (int c = 0; c < U.nch; ++c) {
@@ -477,18 +496,19 @@ __device__ void wcalc(const Unit& U, Smem& S, int which, int lane, int* err) {
         for (int q = 0; q < 4; ++q) {   // 16 channels per step: two n-tiles
             const int cb = 64 * which + 16 * q;
             uint32_t b[4];
-            ldsm_x4_t(b, &st.kgh[((lane & 7) + 8 * ((lane >> 3) & 1)) * KGH_LD + cb + 8 * (lane >> 4)]);
+            ldsm_x4_t(b, reinterpret_cast<const unsigned char*>(st.kgh) +
+                             kgh_offset((lane & 7) + 8 * ((lane >> 3) & 1), cb + 8 * (lane >> 4)));
             float cw0[4] = {}, cw1[4] = {};
             mma_f16(cw0, ta, b[0], b[1]);
             mma_f16(cw1, ta, b[2], b[3]);
             const int col0 = cb + 2 * t, col1 = col0 + 8;
-            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(32 + g, col0, X_ROWS)) =
+            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(16 + g, col0, X_ROWS)) =
                 make_float2(tf32_round(-cw0[0]), tf32_round(-cw0[1]));
-            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(40 + g, col0, X_ROWS)) =
+            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(24 + g, col0, X_ROWS)) =
                 make_float2(tf32_round(-cw0[2]), tf32_round(-cw0[3]));
-            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(32 + g, col1, X_ROWS)) =
+            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(16 + g, col1, X_ROWS)) =
                 make_float2(tf32_round(-cw1[0]), tf32_round(-cw1[1]));
-            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(40 + g, col1, X_ROWS)) =
+            *reinterpret_cast<float2*>(x + tc::swizzled32_offset(24 + g, col1, X_ROWS)) =
                 make_float2(tf32_round(-cw1[2]), tf32_round(-cw1[3]));
         }
         tc::fence_proxy_async_smem();   // -w is read by the chain's MMA
@@ -538,8 +558,6 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
     };
     float bw0 = 0.0f, bw1 = 0.0f, nb0 = 0.0f, nb1 = 0.0f;
     if (U.nch > 0) load_window(0, nb0, nb1);
-    // identity in A-fragment layout: rows g / g+8, columns 2t, 2t+1 / 8+2t, 9+2t
-    const uint32_t id0 = pack_half2(g == 2 * t ? 1.0f : 0.0f, g == 2 * t + 1 ? 1.0f : 0.0f);
     for (int c = 0; c < U.nch; ++c) {
         const int len = min(kChunk, U.L - c * kChunk);
         if ((c & 3) == 0) {
@@ -553,45 +571,28 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
         const bool ok = mbar_wait(&S.a_ready[par], (unsigned)((c >> 1) & 1), err);
         if (!__all_sync(0xffffffffu, ok)) return;
         Stage& st = S.st[c % kRing];
-        if (lane < kChunk) {   // A = diag(b) A_kk, strictly lower, as an fp16 16 x 16 tile
-            float a[16];
+        // A = diag(b) A_kk strictly lower, in accumulator layout (rows g, g + 8; columns
+        // 8 nt + 2t, + 1), rounded to fp16; its fragments, and I - A in fp32 and fp16
+        const float bg = __shfl_sync(0xffffffffu, bl, g), bg8 = __shfl_sync(0xffffffffu, bl, g + 8);
+        float cA[2][4], cI[2][4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 f = *reinterpret_cast<const float4*>(&PS.Akk[par][lane * AK_LD + 4 * q]);
-                a[4 * q] = f.x;
-                a[4 * q + 1] = f.y;
-                a[4 * q + 2] = f.z;
-                a[4 * q + 3] = f.w;
-            }
-            uint32_t h[8];
+        for (int nt = 0; nt < 2; ++nt) {
+            const float2 lo = *reinterpret_cast<const float2*>(&PS.Akk[par][g * AK_LD + 8 * nt + 2 * t]);
+            const float2 hi = *reinterpret_cast<const float2*>(&PS.Akk[par][(g + 8) * AK_LD + 8 * nt + 2 * t]);
+            const float raw[4] = {lo.x, lo.y, hi.x, hi.y};
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                h[q] = pack_half2((2 * q < lane) ? bl * a[2 * q] : 0.0f,
-                                  (2 * q + 1 < lane) ? bl * a[2 * q + 1] : 0.0f);
-            uint4* row = reinterpret_cast<uint4*>(&PS.Ah[lane * AH_LD]);
-            row[0] = make_uint4(h[0], h[1], h[2], h[3]);
-            row[1] = make_uint4(h[4], h[5], h[6], h[7]);
-        }
-        __syncwarp();
-        uint32_t aA[4], bA[4];
-        ldsm_x4(aA, &PS.Ah[(lane & 15) * AH_LD + 8 * (lane >> 4)]);
-        ldsm_x4_t(bA, &PS.Ah[((lane & 7) + 8 * ((lane >> 3) & 1)) * AH_LD + 8 * (lane >> 4)]);
-        // I - A: fragment and fp32 accumulator
-        uint32_t aIA[4];
-        float cI[2][4];
-        {
-            const __half2 i2 = *reinterpret_cast<const __half2*>(&id0);
-            const __half2 z2 = __float2half2_rn(0.0f);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const __half2 x = *reinterpret_cast<const __half2*>(&aA[k]);
-                const __half2 y = __hsub2((k == 0 || k == 3) ? i2 : z2, x);
-                aIA[k] = *reinterpret_cast<const uint32_t*>(&y);
-                const float2 f = __half22float2(y);
-                cI[k >> 1][2 * (k & 1)] = f.x;
-                cI[k >> 1][2 * (k & 1) + 1] = f.y;
+            for (int e = 0; e < 4; ++e) {
+                const int r = (e < 2) ? g : g + 8, col = 8 * nt + 2 * t + (e & 1);
+                const float av =
+                    (col < r) ? __half2float(__float2half_rn((e < 2 ? bg : bg8) * raw[e])) : 0.0f;
+                cA[nt][e] = av;
+                cI[nt][e] = (col == r ? 1.0f : 0.0f) - av;
             }
         }
+        uint32_t aA[4], bA[4], aIA[4];
+        frag_a(cA, aA);
+        frag_b(aA, bA);
+        frag_a(cI, aIA);
         float c2[2][4] = {}, c4[2][4] = {}, c8[2][4] = {};
         uint32_t aP[4], bA2[4], bA4[4], bA8[4];
         mma16(c2, aA, bA);                 // A^2
@@ -620,8 +621,8 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
             const int col = 8 * nt + 2 * t;
             *reinterpret_cast<uint32_t*>(&st.tbr[g * TB_LD + col]) = lo;
             *reinterpret_cast<uint32_t*>(&st.tbr[(g + 8) * TB_LD + col]) = hi;
-            *reinterpret_cast<uint32_t*>(tbt + tc::interleaved_offset(16 + g, col, kChunk)) = lo;
-            *reinterpret_cast<uint32_t*>(tbt + tc::interleaved_offset(24 + g, col, kChunk)) = hi;
+            *reinterpret_cast<uint32_t*>(tbt + tc::interleaved_offset(g, col, kChunk)) = lo;
+            *reinterpret_cast<uint32_t*>(tbt + tc::interleaved_offset(g + 8, col, kChunk)) = hi;
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
@@ -632,21 +633,21 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
 // ---- sequential stage: tensor-core issue (one thread) -------------------------------
 // Per chunk c (slot s), in the transposed orientation (TMEM lane = value row v), with
 // S^T of the chunk's start in state buffer c & 1:
-//   [O|U] = V^T [0 ; T diag(b)]^T             (zeros into O, u^T into U; fp16)
-//   [O|U] += S^T [Q 2^G ; -w]^T               (16 tf32 MMAs over the 128 key channels)
+//   [O|U] = S^T [Q 2^G ; -w]^T               (16 tf32 MMAs over the 128 key channels)
+//   U    += V^T (T diag b)^T                  (u^T, fp16, after the first of them)
 //   S'^T += U^T (K 2^(G_last-G))              (S'^T = S^T 2^G_last, written by the
 //                                              epilogue into the other state buffer)
 //   O    += U^T A_qk^T
 // The state and U are read from tensor memory as fp32 A operands (kind::tf32).
 __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
-    constexpr uint32_t id_u = tc::idesc_f16_f32(128, 32);
+    constexpr uint32_t id_u = tc::idesc_f16_f32(128, 16);
     constexpr uint32_t id_s = tc::idesc_tf32_f32(128, 32);
     constexpr uint32_t id_k = tc::idesc_tf32_f32(128, 128);
     constexpr uint32_t id_q = tc::idesc_tf32_f32(128, 16);
     // descriptors of slot 0; slot s adds its byte offset >> 4 to the start field
     const uint64_t d_vt = tc::smem_desc(smem_u32(S.st[0].vt), 128, T_SBO, tc::kSwizzleNone);
     const uint64_t d_tbt = tc::smem_desc(smem_u32(S.st[0].tbt), 128, 256, tc::kSwizzleNone);
-    const uint64_t d_xb = tc::smem_desc(smem_u32(S.st[0].x) + 16 * 128, 16, 1024, tc::kSwizzle128B);
+    const uint64_t d_xb = tc::smem_desc(smem_u32(S.st[0].x), 16, 1024, tc::kSwizzle128B);
     const uint64_t d_kdt = tc::smem_desc(smem_u32(S.st[0].kdt), 128, KD_SBO, tc::kSwizzleNone);
     const uint64_t d_aqk = tc::smem_desc(smem_u32(S.st[0].aqk), 128, AQ_SBO, tc::kSwizzleNone);
     for (int c = 0; c < U.nch; ++c) {
@@ -662,9 +663,12 @@ __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
             if (!mbar_wait(&S.s_done, (unsigned)((c - 1) & 1), err)) return;
         }
         tc::fence_after_sync();
-        tc::mma_ss(uo, d_vt + so, d_tbt + so, id_u, 0);
+        // [O|U] = S^T [Q 2^G ; -w]^T over key channels 0-7 (fresh accumulator), then
+        // U += u^T = V^T (T diag b)^T, then the remaining 15 key-channel steps
+        tc::mma_ts_tf32(uo, sc, d_xb + so, id_s, 0);
+        tc::mma_ss(uo + 16, d_vt + so, d_tbt + so, id_u, 1);
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
+        for (int kk = 1; kk < 16; ++kk)
             tc::mma_ts_tf32(uo, sc + 8 * kk,
                             d_xb + so + (uint64_t)(((kk >> 2) * X_ROWS * 128 + (kk & 3) * 32) >> 4),
                             id_s, 1);
@@ -845,10 +849,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRing; ++s) {
             mbar_init(&S.full[s], 64);             // both w warps
+            mbar_init(&S.empty[s], 1);             // one tensor-core commit
             mbar_init(&S.kq_ready[s], kProdThreads);   // every producer thread
             mbar_init(&S.t_ready[s], 32);          // solver warp
-            mbar_init(&S.empty[s], 1);             // one tensor-core commit
         }
+        for (int s = 0; s < kEarly; ++s) mbar_init(&S.e_free[s], 64);   // both A-product warps
         mbar_init(&S.uo_done, 1);
         mbar_init(&S.s_done, 1);
         mbar_init(&S.init_ready, kEpiWarps * 32);
@@ -862,11 +867,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&S.raw_empty[s], kProdThreads);     // every producer thread
         }
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    }
-    // rows 0..15 of every slot's T diag(b) operand stay zero
-    for (int i = threadIdx.x; i < kRing * 16 * 16 / 2; i += kThreads) {
-        const int slot = i / 128, e = i % 128;
-        reinterpret_cast<uint32_t*>(S.st[slot].tbt)[e] = 0u;
     }
     tc::fence_proxy_async_smem();
     if (warp == kMmaWarp) {
