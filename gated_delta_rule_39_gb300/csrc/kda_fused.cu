@@ -172,10 +172,10 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* b, unsigned pa
     unsigned ok;
     asm volatile(
         "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity), "r"(1000000u)   // may sleep up to 1 ms per try
+        : "r"(smem_u32(b)), "r"(parity)   // suspends for a system-dependent time limit
         : "memory");
     return ok != 0;
 }
@@ -440,7 +440,7 @@ __device__ void aprod(const Unit& U, Smem& S, int which, int lane, int* err) {
         const int xrows = which ? X_ROWS : kChunk;
         const unsigned char* ki = reinterpret_cast<const unsigned char*>(S.early[par].ki);
         float acc[2][2][4] = {};   // [channel half][n-tile][fragment]
-#pragma unroll 4
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
