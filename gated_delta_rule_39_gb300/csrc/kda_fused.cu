@@ -147,10 +147,10 @@ struct Smem {
     ProdShared pr;
     unsigned long long raw_full[kRaw];   // TMA bytes landed
     unsigned long long raw_empty[kRaw];  // producers have read the slot
-    unsigned long long full[kRing];      // operands complete (-w written) -> MMA / epilogue
+    unsigned long long full[kRing];      // operands complete (-w, A_qk written) -> MMA / epilogue
     unsigned long long empty[kRing];     // MMA commit -> producers
     unsigned long long kq_ready[kRing];  // producers: the chunk's tiles written
-    unsigned long long a_ready[2];       // A-product warps: A_kk / A_qk written
+    unsigned long long a_ready[2];       // A_kk warp: A_kk written (per chunk parity)
     unsigned long long t_ready[kRing];   // solver: T diag(b) written
     unsigned long long e_free[kEarly];   // both A-product warps are done with the early slot
     unsigned long long uo_done;          // O|U MMAs complete
@@ -431,7 +431,8 @@ __device__ void aprod(const Unit& U, Smem& S, int which, int lane, int* err) {
         const int par = c & 1, slot = c % kRing;
         bool ok = mbar_wait(&S.kq_ready[slot], (unsigned)((c / kRing) & 1), err);
         // A_kk buffer of this parity: the solver is done with chunk c - 2
-        if (c >= 2) ok = ok && mbar_wait(&S.t_ready[(c - 2) % kRing], (unsigned)(((c - 2) / kRing) & 1), err);
+        if (which == 0 && c >= 2)
+            ok = ok && mbar_wait(&S.t_ready[(c - 2) % kRing], (unsigned)(((c - 2) / kRing) & 1), err);
         if (!__all_sync(0xffffffffu, ok)) return;
         Stage& st = S.st[slot];
         // A operand: K 2^G (early slot) or Q 2^G (rows 0-15 of the x tile)
@@ -474,8 +475,12 @@ __device__ void aprod(const Unit& U, Smem& S, int which, int lane, int* err) {
                                 s0 + 1 <= g + 8 ? tf32_round(r[3]) : 0.0f);
             }
         }
-        if (which == 1) tc::fence_proxy_async_smem();   // the A_qk tile is read by the chain's MMA
-        mbar_arrive(&S.a_ready[par]);
+        if (which == 1) {   // the A_qk tile is one of the chain's operands
+            tc::fence_proxy_async_smem();
+            mbar_arrive(&S.full[slot]);
+        } else {
+            mbar_arrive(&S.a_ready[par]);
+        }
     }
 }
 
@@ -848,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRing; ++s) {
-            mbar_init(&S.full[s], 64);             // both w warps
+            mbar_init(&S.full[s], 96);             // both w warps and the A_qk warp
             mbar_init(&S.empty[s], 1);             // one tensor-core commit
             mbar_init(&S.kq_ready[s], kProdThreads);   // every producer thread
             mbar_init(&S.t_ready[s], 32);          // solver warp
@@ -860,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&S.scaled, kEpiWarps * 32);
         mbar_init(&S.epi_done, kEpiWarps * 32);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&S.a_ready[b], 64);              // both A-product warps
+            mbar_init(&S.a_ready[b], 32);              // the A_kk warp
         }
         for (int s = 0; s < kRaw; ++s) {
             mbar_init(&S.raw_full[s], 1);                 // loader's arrive + TMA bytes
