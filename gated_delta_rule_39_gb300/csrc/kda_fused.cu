@@ -639,7 +639,7 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
 // Per chunk c (slot s), in the transposed orientation (TMEM lane = value row v), with
 // S^T of the chunk's start in state buffer c & 1:
 //   [O|U] = S^T [Q 2^G ; -w]^T               (16 tf32 MMAs over the 128 key channels)
-//   U    += V^T (T diag b)^T                  (u^T, fp16, after the first of them)
+//   U    += V^T (T diag b)^T                  (u^T, fp16, after them)
 //   S'^T += U^T (K 2^(G_last-G))              (S'^T = S^T 2^G_last, written by the
 //                                              epilogue into the other state buffer)
 //   O    += U^T A_qk^T
@@ -668,15 +668,15 @@ __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
             if (!mbar_wait(&S.s_done, (unsigned)((c - 1) & 1), err)) return;
         }
         tc::fence_after_sync();
-        // [O|U] = S^T [Q 2^G ; -w]^T over key channels 0-7 (fresh accumulator), then
-        // U += u^T = V^T (T diag b)^T, then the remaining 15 key-channel steps
+        // [O|U] = S^T [Q 2^G ; -w]^T over the 16 key-channel steps (the first one starts
+        // a fresh accumulator), then U += u^T = V^T (T diag b)^T
         tc::mma_ts_tf32(uo, sc, d_xb + so, id_s, 0);
-        tc::mma_ss(uo + 16, d_vt + so, d_tbt + so, id_u, 1);
 #pragma unroll
         for (int kk = 1; kk < 16; ++kk)
             tc::mma_ts_tf32(uo, sc + 8 * kk,
                             d_xb + so + (uint64_t)(((kk >> 2) * X_ROWS * 128 + (kk & 3) * 32) >> 4),
                             id_s, 1);
+        tc::mma_ss(uo + 16, d_vt + so, d_tbt + so, id_u, 1);
         tc::commit(smem_u32(&S.uo_done));
         if (!mbar_wait(&S.uo_done, (unsigned)(c & 1), err)) return;
         if (!mbar_wait(&S.scaled, (unsigned)(c & 1), err)) return;
