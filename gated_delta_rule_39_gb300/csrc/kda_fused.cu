@@ -12,10 +12,12 @@
 //                       K 2^-G, K 2^(G_last-G), V), up to kRing chunks ahead.
 //   A-product warps (2) the decay-ratio products A_kk = (K 2^G)(K 2^-G)^T (to the
 //                       solver) and A_qk = (Q 2^G)(K 2^-G)^T (inclusive lower, to
-//                       an operand tile): tf32 mma.sync from ldmatrix fragments.
+//                       an operand tile, which completes the stage with -w): tf32
+//                       mma.sync from ldmatrix fragments.
 //   w warps (2)         once the solver has T: -w = -T diag(b)(K 2^G), 64 channels
 //                       each, which completes the chunk's operands.
-//   solver warp         (I + diag(b) A_kk)^-1 by forward substitution, T diag(b).
+//   solver warp         T = (I + diag(b) A_kk)^-1 as a four-factor Neumann product
+//                       (fp16 mma.sync), then T diag(b).
 //   MMA warp            issues the tcgen05 MMAs of the recurrence (one thread).
 //   epilogue warps (4)  own the tensor-memory state S^T (lane v = value channel v):
 //                       decay rescale, outputs, initial and final state.
