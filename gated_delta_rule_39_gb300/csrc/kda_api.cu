@@ -25,7 +25,11 @@ int cuda_fail(int status, cudaError_t e) {
 __device__ int g_error_word;
 
 constexpr int kMaxDevices = 64;
-constexpr float kLowerBoundMin = -5.5f;  // 16 * 5.5 / ln 2 = 127 bits of decay per chunk
+// A 16-token chunk of gates at the bound spans 16 * 5.4 / ln 2 = 124.6 bits of decay.
+// The in-chunk factors 2^G of its last rows then stay normal fp32 numbers; much
+// closer to 2^-126 the products q 2^G, k 2^G fall into the subnormal range and lose
+// precision, and at -5.5 (126.96 bits) 2^G itself underflows.
+constexpr float kLowerBoundMin = -5.4f;
 
 struct DeviceInfo {
     bool ready = false;
@@ -212,7 +216,7 @@ const char* kda_status_string(int status) {
         case KDA_ERR_ARCH: return "KDA_ERR_ARCH: needs a compute capability 10.3 (sm_103) GPU";
         case KDA_ERR_ALLOC: return "KDA_ERR_ALLOC: scratch allocation failed";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
-        case KDA_ERR_ARG: return "KDA_ERR_ARG: scale must be finite, lower_bound in [-5.5, 0]";
+        case KDA_ERR_ARG: return "KDA_ERR_ARG: scale must be finite, lower_bound in [-5.4, 0]";
         case KDA_ERR_ALIAS: return "KDA_ERR_ALIAS: out overlaps an input or states alias unsafely";
         case KDA_ERR_SCRATCH_LIMIT:
             return "KDA_ERR_SCRATCH_LIMIT: kda_fwd_noalloc takes at most KDA_NOALLOC_MAX_SEQS "

@@ -72,9 +72,10 @@ typedef enum {
  *   beta        bf16 [B, T, H]           logits; sigmoid is applied inside
  *   scale       multiplies the output    (finite)
  *   A_log       fp32 [H]                 dt_bias  fp32 [H, K]
- *   lower_bound fp32 scalar, in [-5.5, 0]: the per-token log-decay lies in
- *               [lower_bound, 0]; with 16-token chunks this keeps every
- *               decay ratio inside the fp32 exponent range
+ *   lower_bound fp32 scalar, in [-5.4, 0]: the per-token log-decay lies in
+ *               [lower_bound, 0]; with 16-token chunks the in-chunk decay
+ *               factors 2^(+-G) then stay within 2^124.6 of 1, inside the range
+ *               of normal fp32 numbers (KDA_ERR_ARG outside it)
  *   initial_state  NULL (zero state) or [N, H, K, V] of initial_state_dtype
  *   final_state    NULL (not written) or [N, H, K, V] of final_state_dtype
  *               State element [n][h][i][j] is S[i][j]: row i = key channel,

@@ -90,6 +90,7 @@ def test_rejects_bad_dtypes_and_args(lib):
     assert _call(lib, s0=fake, s0_dtype=7) == -5
     assert _call(lib, s1=fake, s1_dtype=-1) == -5
     assert _call(lib, lower_bound=-6.0) == -12
+    assert _call(lib, lower_bound=-5.45) == -12
     assert _call(lib, lower_bound=0.5) == -12
     assert _call(lib, scale=float("inf")) == -12
 

@@ -62,6 +62,26 @@ def test_state_dtypes(init, final):
     _check(d, final_dtype=final, tag=f"init={init} final={final}")
 
 
+@pytest.mark.parametrize("lower_bound", [-5.4, 0.0])
+@pytest.mark.parametrize("pattern", ["saturated", "mixed"])
+def test_gate_range_edges(lower_bound, pattern):
+    """Gates at the ends of the accepted range.  "saturated": every per-token
+    log-decay equals lower_bound (at -5.4 a chunk spans 124.6 bits of decay, so the
+    in-chunk factors 2^(+-G) reach the edge of the normal fp32 range); "mixed": even
+    key channels decay at the bound and odd ones hardly at all.  lower_bound = 0 is
+    the ungated delta rule."""
+    d = synth.make_inputs(1, 100, 2, seed=21, init_dtype="f32", lower_bound=lower_bound)
+    g = synth.bf16_bits_to_f32(d["g"]).copy()
+    if pattern == "saturated":
+        g[:] = 8.0
+    else:
+        g[..., 0::2] = 8.0
+        g[..., 1::2] = -8.0
+    d["g"] = synth.f32_to_bf16_bits(g)
+    d["A_log"][:] = np.float32(np.log(16.0))   # sigmoid(16 (g + dt_bias)) is 0 or 1 in fp32
+    _check(d, tag=f"lower_bound={lower_bound} {pattern}")
+
+
 def test_varlen_edge_lengths():
     lens = [1, 15, 16, 17, 0, 33, 64, 5, 2]
     d = synth.make_inputs(1, sum(lens), 4, seed=11, lengths=lens, init_dtype="f32")
