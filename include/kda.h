@@ -69,6 +69,11 @@ typedef enum {
  * kda_fwd -- KDA forward (prefill) pass.
  *
  *   q, k, g     bf16 [B, T, H, K]        v, out   bf16 [B, T, H, V]
+ *               q and k are used as given (not normalised).  The kernel forms
+ *               k * 2^-G with G down to 16 * lower_bound / ln 2 per chunk, so a
+ *               key component must stay below 2^(128 + 16 * lower_bound / ln 2)
+ *               in magnitude (about 10 at lower_bound = -5.4, 6,000 at -5)
+ *               for that factor to stay finite; unit-norm keys always do.
  *   beta        bf16 [B, T, H]           logits; sigmoid is applied inside
  *   scale       multiplies the output    (finite)
  *   A_log       fp32 [H]                 dt_bias  fp32 [H, K]
