@@ -198,6 +198,124 @@ int noalloc_scratch(int dev, int** addr) {
 }
 }  // namespace
 
+namespace kda {
+namespace {
+
+// ---- kda_fwd_host for one long fixed-length sequence ---------------------------
+// The tokens are cut into blocks (multiples of the 16-token chunk, so that the
+// chunking and every result are those of one kda_fwd call); block i runs while
+// block i + 1 is copied in and block i - 1's output is copied out, on copy
+// streams ordered against `s` by events.  The state passes from block to block
+// through an fp32 device buffer (exact: the kernel keeps the state in fp32).
+constexpr int kHostBlockMin = 1024;   // tokens per block, at least
+
+int host_block_len(int T) {
+    int blk = (T + 3) / 4;             // about four blocks
+    blk = (blk + kChunk - 1) / kChunk * kChunk;
+    return blk > kHostBlockMin ? blk : kHostBlockMin;
+}
+
+bool host_pipelined(const int32_t* cu_seqlens, int B, int T) {
+    return cu_seqlens == nullptr && B == 1 && T >= 2 * kHostBlockMin;
+}
+
+int host_fwd_blocks(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                    float scale, void* out, const float* A_log, const float* dt_bias,
+                    float lower_bound, const void* initial_state, int initial_state_dtype,
+                    void* final_state, int final_state_dtype, int T, int H, cudaStream_t s) {
+    const int blk = host_block_len(T);
+    const int nblk = (T + blk - 1) / blk;
+    const size_t row = (size_t)H * kDim * 2, brow = (size_t)H * 2;   // bytes per token
+    const size_t n_qk = (size_t)T * row, n_b = (size_t)T * brow;
+    const size_t n_s = (size_t)H * kDim * kDim;
+    const size_t b_s0 = initial_state ? n_s * (initial_state_dtype == KDA_F32 ? 4 : 2) : 0;
+    const size_t b_s1 = final_state ? n_s * (final_state_dtype == KDA_F32 ? 4 : 2) : 0;
+    // q, k, v, g, beta, out, A_log, dt_bias, initial, final, carried fp32 state
+    const size_t sizes[] = {n_qk, n_qk, n_qk, n_qk, n_b, n_qk, sizeof(float) * H,
+                            sizeof(float) * H * kDim, b_s0, b_s1, n_s * 4};
+    size_t total = 0, offs[11];
+    for (int i = 0; i < 11; ++i) {
+        offs[i] = total;
+        total += align_up(sizes[i]);
+    }
+    unsigned char* d = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&d), total, s);
+    if (e != cudaSuccess) return cuda_fail(KDA_ERR_ALLOC, e);
+    cudaStream_t sin = nullptr, sout = nullptr;
+    std::vector<cudaEvent_t> ev(2 * nblk + 2, nullptr);   // in[i], kernel[i], alloc, out
+    int rc = KDA_OK;
+    e = cudaStreamCreateWithFlags(&sin, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&sout, cudaStreamNonBlocking);
+    for (size_t i = 0; i < ev.size() && e == cudaSuccess; ++i)
+        e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    cudaEvent_t ev_alloc = ev[2 * nblk], ev_out = ev[2 * nblk + 1];
+    // copies in: parameters and initial state, then the blocks back to back
+    if (e == cudaSuccess) e = cudaEventRecord(ev_alloc, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(sin, ev_alloc, 0);
+    const void* params[] = {A_log, dt_bias, initial_state};
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+        if (params[i] && sizes[6 + i])
+            e = cudaMemcpyAsync(d + offs[6 + i], params[i], sizes[6 + i], cudaMemcpyHostToDevice, sin);
+    const void* tok_src[] = {q, k, v, g};
+    for (int b = 0; b < nblk && e == cudaSuccess; ++b) {
+        const size_t t0 = (size_t)b * blk, len = (size_t)((b + 1) * blk < T ? blk : T - b * blk);
+        for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+            e = cudaMemcpyAsync(d + offs[i] + t0 * row, static_cast<const unsigned char*>(tok_src[i]) + t0 * row,
+                                len * row, cudaMemcpyHostToDevice, sin);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(d + offs[4] + t0 * brow, static_cast<const unsigned char*>(beta) + t0 * brow,
+                                len * brow, cudaMemcpyHostToDevice, sin);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[b], sin);
+    }
+    // blocks in order on `s`, each output block copied out as soon as it is written
+    void* carry = d + offs[10];
+    for (int b = 0; b < nblk && e == cudaSuccess && rc == KDA_OK; ++b) {
+        const size_t t0 = (size_t)b * blk;
+        const int len = (b + 1) * blk < T ? blk : T - b * blk;
+        const bool first = b == 0, last = b == nblk - 1;
+        e = cudaStreamWaitEvent(s, ev[b], 0);
+        if (e != cudaSuccess) break;
+        rc = kda_fwd(d + offs[0] + t0 * row, d + offs[1] + t0 * row, d + offs[2] + t0 * row,
+                     d + offs[3] + t0 * row, d + offs[4] + t0 * brow, scale, d + offs[5] + t0 * row,
+                     reinterpret_cast<const float*>(d + offs[6]),
+                     reinterpret_cast<const float*>(d + offs[7]), lower_bound,
+                     first ? (initial_state ? static_cast<void*>(d + offs[8]) : nullptr) : carry,
+                     first ? initial_state_dtype : KDA_F32,
+                     last ? (final_state ? static_cast<void*>(d + offs[9]) : nullptr) : carry,
+                     last ? final_state_dtype : KDA_F32, nullptr, 0, 1, len, H, kDim, kDim, s);
+        if (rc != KDA_OK) break;
+        e = cudaEventRecord(ev[nblk + b], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(sout, ev[nblk + b], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<unsigned char*>(out) + t0 * row, d + offs[5] + t0 * row,
+                                (size_t)len * row, cudaMemcpyDeviceToHost, sout);
+        if (e == cudaSuccess && last && final_state)
+            e = cudaMemcpyAsync(final_state, d + offs[9], b_s1, cudaMemcpyDeviceToHost, sout);
+    }
+    // `s` takes over the copy streams' work before the buffer is freed
+    if (sin) {
+        const cudaError_t e1 = cudaEventRecord(ev_alloc, sin);
+        if (e1 == cudaSuccess) cudaStreamWaitEvent(s, ev_alloc, 0);
+    }
+    if (sout) {
+        const cudaError_t e1 = cudaEventRecord(ev_out, sout);
+        if (e1 == cudaSuccess) cudaStreamWaitEvent(s, ev_out, 0);
+    }
+    cudaFreeAsync(d, s);
+    const cudaError_t es = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = es;
+    for (cudaEvent_t x : ev)
+        if (x) cudaEventDestroy(x);
+    if (sin) cudaStreamDestroy(sin);
+    if (sout) cudaStreamDestroy(sout);
+    if (rc != KDA_OK) return rc;
+    if (e != cudaSuccess) return cuda_fail(KDA_ERR_CUDA, e);
+    return KDA_OK;
+}
+
+}  // namespace
+}  // namespace kda
+
 using namespace kda;
 
 extern "C" {
@@ -323,6 +441,10 @@ int kda_fwd_host(const void* q, const void* k, const void* v, const void* g, con
     rc = device_setup(&dev, &err);
     if (rc != KDA_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (host_pipelined(cu_seqlens, B, T))
+        return host_fwd_blocks(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+                               initial_state, initial_state_dtype, final_state, final_state_dtype,
+                               T, H, s);
     const size_t tok = (size_t)B * T;
     const int N = cu_seqlens ? num_seqs : B;
     const size_t n_qk = tok * H * kDim * 2, n_b = tok * H * 2;

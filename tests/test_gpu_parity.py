@@ -236,6 +236,30 @@ def test_host_entry_point_matches_device_entry_point():
     assert torch.equal(out, o_dev.cpu()) and torch.equal(fs, s_dev.cpu())
 
 
+@pytest.mark.parametrize("init,final", [("f32", "f32"), ("bf16", "bf16"), (None, None)])
+def test_host_entry_point_blocks_match_device_entry_point(init, final):
+    """T = 3000 on the host entry point runs as token blocks of 1024, 1024 and 952
+    with the state carried between them; the result must be that of one call."""
+    import torch
+    import gated_delta_rule_39_gb300 as kda
+    d = synth.make_inputs(1, 3000, 2, seed=17, init_dtype=init)
+    o_dev, s_dev = run_gpu(d, final_dtype=final)
+    x = upload(d, "cpu")
+    out = torch.empty((1, 3000, 2, 128), dtype=torch.bfloat16).pin_memory()
+    fs = None
+    if final is not None:
+        dt = torch.float32 if final == "f32" else torch.bfloat16
+        fs = torch.empty((1, 2, 128, 128), dtype=dt).pin_memory()
+    s0 = x["initial_state"]
+    kda.kda_fwd_host(x["q"].pin_memory(), x["k"].pin_memory(), x["v"].pin_memory(),
+                     x["g"].pin_memory(), x["beta"].pin_memory(), d["scale"], out, x["A_log"],
+                     x["dt_bias"], d["lower_bound"],
+                     initial_state=None if s0 is None else s0.pin_memory(), final_state=fs)
+    assert torch.equal(out, o_dev.cpu())
+    if fs is not None:
+        assert torch.equal(fs, s_dev.cpu())
+
+
 def test_profile_counts_launches():
     import gated_delta_rule_39_gb300 as kda
     d = synth.make_inputs(1, 64, 2, seed=2, lengths=[20, 44])
