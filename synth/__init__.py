@@ -173,6 +173,48 @@ def make_inputs(B: int, T: int, H: int, K: int = 128, V: int = 128, seed: int = 
     return out
 
 
+def make_inputs_device(T: int, H: int, seed: int = 0, device="cuda:0",
+                       lower_bound: float = LOWER_BOUND) -> dict:
+    """The recipe of make_inputs (B = 1, fixed length, no initial state) drawn on the
+    device with torch's generator, for sizes too large to draw on the host.
+
+    q, k: N(0,1) rows normalised in fp32, rounded to bf16; v, g, beta: N(0,1) in bf16;
+    torch tensors [1, T, H, 128] ([1, T, H] for beta).  A_log, dt_bias and the scalars
+    come from numpy as in make_inputs.  A token window of the result is handed to a
+    host-side consumer with ``window_bits``.
+    """
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+
+    def normal(shape):
+        return torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+
+    def unit_rows():
+        x = normal((1, T, H, 128))
+        x /= torch.linalg.vector_norm(x, dim=-1, keepdim=True)
+        return x.to(torch.bfloat16)
+
+    out = {"q": unit_rows(), "k": unit_rows()}
+    for name in ("v", "g"):
+        out[name] = normal((1, T, H, 128)).to(torch.bfloat16)
+    out["beta"] = normal((1, T, H)).to(torch.bfloat16)
+    rng = np.random.default_rng(seed)
+    out["A_log"] = rng.uniform(0.0, math.log(16.0), size=H).astype(np.float32)
+    out["dt_bias"] = (0.1 * rng.standard_normal((H, 128))).astype(np.float32)
+    out["lower_bound"] = float(lower_bound)
+    out["scale"] = float(1.0 / math.sqrt(128))
+    out["N"] = 1
+    return out
+
+
+def window_bits(t, start: int, stop: int) -> np.ndarray:
+    """Tokens start .. stop - 1 of a bf16 torch tensor [1, T, ...] as host uint16 bits."""
+    import torch
+    w = t[:, start:stop].contiguous().cpu().view(torch.int16).numpy()
+    return w.view(np.uint16)
+
+
 def make_workload(name: str, seed: int = 0) -> dict:
     w = WORKLOADS[name]
     d = make_inputs(w.B, w.T, w.H, w.K, w.V, seed=seed, lengths=w.lengths,

@@ -158,6 +158,47 @@ def test_long_context_state_carry():
     assert se["ok"], se
 
 
+def test_maximum_size_tail():
+    """The largest call the boundary accepts with one head: T = 2^24 - 7 tokens, so each
+    token tensor holds 2^31 - 896 elements (the limit is 2^31) and the last chunk is
+    ragged.  The oracle cannot replay 16.8 M tokens, but the recurrence forgets: over
+    256 tokens every channel's decay exp(sum of gates) is below exp(-300) in this
+    recipe, so the outputs of the last 256 tokens and the final state equal those of
+    the oracle started from a zero state on the last 512 tokens (checked here against a
+    768-token window).  This covers the far end of maximal tensors, where 32-bit index
+    arithmetic would overflow first."""
+    import torch
+    import gated_delta_rule_39_gb300 as kda
+    T, H = (1 << 24) - 7, 1
+    assert T * H * 128 < (1 << 31)
+    d = synth.make_inputs_device(T, H, seed=31)
+    out = torch.empty((1, T, H, 128), dtype=torch.bfloat16, device="cuda:0")
+    fs = torch.empty((1, H, 128, 128), dtype=torch.float32, device="cuda:0")
+    kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], out,
+                torch.from_numpy(d["A_log"]).cuda(), torch.from_numpy(d["dt_bias"]).cuda(),
+                d["lower_bound"], final_state=fs)
+    torch.cuda.synchronize()
+    assert kda.kda_fwd_get_error() == 0
+    tail = 256
+
+    def oracle_window(w):
+        win = {n: synth.window_bits(d[n], T - w, T) for n in ("q", "k", "v", "g", "beta")}
+        win.update(A_log=d["A_log"], dt_bias=d["dt_bias"], lower_bound=d["lower_bound"],
+                   scale=d["scale"], initial_state=None, cu_seqlens=None)
+        return run_oracle(win)
+
+    ro, rs = oracle_window(512)
+    ro2, rs2 = oracle_window(768)
+    # the window is long enough: a longer one changes nothing
+    assert np.max(np.abs(ro[:, -tail:] - ro2[:, -tail:])) < 1e-12
+    assert np.max(np.abs(rs - rs2)) < 1e-12
+    o = to_f64(out[:, T - tail:])
+    e = out_error(o, ro[:, -tail:])
+    assert e["ok"], e
+    se = state_error(to_f64(fs), rs)
+    assert se["ok"], se
+
+
 def test_state_buffers_may_alias():
     import torch
     import gated_delta_rule_39_gb300 as kda
