@@ -88,6 +88,17 @@ def test_varlen_edge_lengths():
     _check(d, tag="varlen edges")
 
 
+@pytest.mark.parametrize("N", [3000, 9000])
+def test_varlen_many_short_sequences(N):
+    """Thousands of short sequences (lengths 0-20, empty ones included) in one call:
+    many waves of small units, the longest-first order for N <= 8192 and the input
+    order above it."""
+    rng = np.random.default_rng(N)
+    lens = rng.integers(0, 21, size=N)
+    d = synth.make_inputs(1, int(lens.sum()), 2, seed=N, lengths=list(lens), init_dtype="f32")
+    _check(d, tag=f"N={N}")
+
+
 def test_varlen_single_sequence_equals_fixed():
     import torch
     d = synth.make_inputs(1, 200, 2, seed=12, init_dtype="f32")
