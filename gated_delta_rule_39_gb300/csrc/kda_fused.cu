@@ -524,12 +524,18 @@ __device__ void wcalc(const Unit& U, Smem& S, int which, int lane, int* err) {
 }
 
 // ---- solver warp: (I + diag(b) A_kk)^-1 and T diag(b) for every chunk -----------------
-// A = diag(b) A_kk is strictly lower triangular, so A^16 = 0 and
-//   T = (I + A)^-1 = (I - A)(I + A^2)(I + A^4)(I + A^8)
-// ("Moonshot AI Open-Sources FlashKDA", "What makes the kernel fast": the 16 x 16
-// inverse in fp16).  Twelve m16n8k16 MMAs in registers, fp16 operands, fp32 accumulate;
-// products feed the next MMA as A fragments directly and as B fragments through an
-// 8 x 8 register transpose.
+// A = diag(b) A_kk is strictly lower triangular, so A^16 = 0 and T = (I + A)^-1 is
+// unit lower triangular.  Two evaluations, chosen per chunk:
+//  - rho = max_i sum_m |A[i][m]| <= 1 (the usual case): the fp16 product
+//      T = (I - A)(I + A^2)(I + A^4)(I + A^8)
+//    ("Moonshot AI Open-Sources FlashKDA", "What makes the kernel fast": the 16 x 16
+//    inverse in fp16), twelve m16n8k16 MMAs in registers; every power of A then has
+//    entries of at most 1, so fp16 holds them;
+//  - otherwise (keys of the chunk nearly parallel, b near 1, weak decay: the powers of
+//    A grow to C(14, 7) = 3,432 while T stays small, and fp16 would lose the
+//    cancellation) forward substitution in fp32,
+//      T[i][:] = e_i - b_i sum_{m < i} A_kk[i][m] T[m][:],
+//    lane j (and j + 16) forming column j, which keeps every intermediate the size of T.
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
@@ -550,6 +556,47 @@ __device__ __forceinline__ void frag_b(const uint32_t (&a)[4], uint32_t (&b)[4])
 __device__ __forceinline__ void mma16(float (&d)[2][4], const uint32_t (&a)[4], const uint32_t (&b)[4]) {
     mma_f16(d[0], a, b[0], b[1]);
     mma_f16(d[1], a, b[2], b[3]);
+}
+
+
+// forward substitution of one chunk (the rare path, kept out of the solver's loop body)
+__device__ __noinline__ void solve_substitution(const float* akk, float bl, int lane, __half* tbr,
+                                                unsigned char* tbt) {
+    const int j = lane & 15;   // column of T formed by this lane
+    float tcol[kChunk];        // T[i][j]
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+        float acc0 = 0.0f, acc1 = 0.0f;   // two chains over m, added in a fixed order
+#pragma unroll
+        for (int q = 0; q < kChunk / 4; ++q) {
+            if (4 * q < i) {
+                const float4 a4 = *reinterpret_cast<const float4*>(akk + i * AK_LD + 4 * q);
+                const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = 4 * q + e;
+                    if (m < i) {
+                        if (e & 1) acc1 = fmaf(a[e], tcol[m], acc1);
+                        else acc0 = fmaf(a[e], tcol[m], acc0);
+                    }
+                }
+            }
+        }
+        const float bi = __shfl_sync(0xffffffffu, bl, i);
+        tcol[i] = (i == j ? 1.0f : 0.0f) - bi * (acc0 + acc1);
+    }
+    // T diag(b): column j scaled by b_j; lanes 0-15 write it row-major (A of w),
+    // lanes 16-31 K-major (B of the u MMA)
+    const float bj = __shfl_sync(0xffffffffu, bl, j);
+    if (lane < 16) {
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) tbr[i * TB_LD + j] = __float2half_rn(tcol[i] * bj);
+    } else {
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i)
+            *reinterpret_cast<__half*>(tbt + tc::interleaved_offset(i, j, kChunk)) =
+                __float2half_rn(tcol[i] * bj);
+    }
 }
 
 __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* err) {
@@ -573,19 +620,23 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
             if (64 * (c / 4 + 1) < U.L) load_window(c / 4 + 1, nb0, nb1);
         }
         const float lw = __shfl_sync(0xffffffffu, (c & 2) ? bw1 : bw0, 16 * (c & 1) + (lane & 15));
-        const float bl = (lane < len) ? sigmoid_fast(lw) : 0.0f;   // b of row `lane`
+        // b of row `lane & 15`; rows past the sequence end get b = 0 (their T row is e_i)
+        const float bl = ((lane & 15) < len) ? sigmoid_fast(lw) : 0.0f;
         const int par = c & 1;
         const bool ok = mbar_wait(&S.a_ready[par], (unsigned)((c >> 1) & 1), err);
         if (!__all_sync(0xffffffffu, ok)) return;
         Stage& st = S.st[c % kRing];
+        const float* akk = PS.Akk[par];
+        unsigned char* tbt = reinterpret_cast<unsigned char*>(st.tbt);
         // A = diag(b) A_kk strictly lower, in accumulator layout (rows g, g + 8; columns
-        // 8 nt + 2t, + 1), rounded to fp16; its fragments, and I - A in fp32 and fp16
+        // 8 nt + 2t, + 1), rounded to fp16; I - A; and the row sums of |A|
         const float bg = __shfl_sync(0xffffffffu, bl, g), bg8 = __shfl_sync(0xffffffffu, bl, g + 8);
         float cA[2][4], cI[2][4];
+        float rs_g = 0.0f, rs_g8 = 0.0f;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            const float2 lo = *reinterpret_cast<const float2*>(&PS.Akk[par][g * AK_LD + 8 * nt + 2 * t]);
-            const float2 hi = *reinterpret_cast<const float2*>(&PS.Akk[par][(g + 8) * AK_LD + 8 * nt + 2 * t]);
+            const float2 lo = *reinterpret_cast<const float2*>(&akk[g * AK_LD + 8 * nt + 2 * t]);
+            const float2 hi = *reinterpret_cast<const float2*>(&akk[(g + 8) * AK_LD + 8 * nt + 2 * t]);
             const float raw[4] = {lo.x, lo.y, hi.x, hi.y};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -594,42 +645,55 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
                     (col < r) ? __half2float(__float2half_rn((e < 2 ? bg : bg8) * raw[e])) : 0.0f;
                 cA[nt][e] = av;
                 cI[nt][e] = (col == r ? 1.0f : 0.0f) - av;
+                if (e < 2) rs_g += fabsf(av);
+                else rs_g8 += fabsf(av);
             }
         }
-        uint32_t aA[4], bA[4], aIA[4];
-        frag_a(cA, aA);
-        frag_b(aA, bA);
-        frag_a(cI, aIA);
-        float c2[2][4] = {}, c4[2][4] = {}, c8[2][4] = {};
-        uint32_t aP[4], bA2[4], bA4[4], bA8[4];
-        mma16(c2, aA, bA);                 // A^2
-        frag_a(c2, aP);
-        frag_b(aP, bA2);
-        mma16(c4, aP, bA2);                // A^4
-        mma16(cI, aIA, bA2);               // T1 = (I - A)(I + A^2)
-        frag_a(c4, aP);
-        frag_b(aP, bA4);
-        mma16(c8, aP, bA4);                // A^8
-        frag_a(cI, aP);
-        mma16(cI, aP, bA4);                // T2 = T1 (I + A^4)
-        frag_a(c8, aP);
-        frag_b(aP, bA8);
-        frag_a(cI, aP);
-        mma16(cI, aP, bA8);                // T = T2 (I + A^8)
-        // T diag(b): column n scaled by b_n; rows g, g+8, columns 8 nt + 2t, +1
-        const float b0 = __shfl_sync(0xffffffffu, bl, 2 * t), b1 = __shfl_sync(0xffffffffu, bl, 2 * t + 1);
-        const float b8 = __shfl_sync(0xffffffffu, bl, 8 + 2 * t), b9 = __shfl_sync(0xffffffffu, bl, 9 + 2 * t);
-        unsigned char* tbt = reinterpret_cast<unsigned char*>(st.tbt);
+        // rho = largest row sum: add over the four lanes of a row, then the maximum over
+        // the warp (non-negative floats order like their bit patterns)
+        rs_g += __shfl_xor_sync(0xffffffffu, rs_g, 1);
+        rs_g8 += __shfl_xor_sync(0xffffffffu, rs_g8, 1);
+        rs_g += __shfl_xor_sync(0xffffffffu, rs_g, 2);
+        rs_g8 += __shfl_xor_sync(0xffffffffu, rs_g8, 2);
+        const float rho =
+            __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(rs_g, rs_g8))));
+        if (rho <= 1.0f) {
+            uint32_t aA[4], bA[4], aIA[4];
+            frag_a(cA, aA);
+            frag_b(aA, bA);
+            frag_a(cI, aIA);
+            float c2[2][4] = {}, c4[2][4] = {}, c8[2][4] = {};
+            uint32_t aP[4], bA2[4], bA4[4], bA8[4];
+            mma16(c2, aA, bA);                 // A^2
+            frag_a(c2, aP);
+            frag_b(aP, bA2);
+            mma16(c4, aP, bA2);                // A^4
+            mma16(cI, aIA, bA2);               // T1 = (I - A)(I + A^2)
+            frag_a(c4, aP);
+            frag_b(aP, bA4);
+            mma16(c8, aP, bA4);                // A^8
+            frag_a(cI, aP);
+            mma16(cI, aP, bA4);                // T2 = T1 (I + A^4)
+            frag_a(c8, aP);
+            frag_b(aP, bA8);
+            frag_a(cI, aP);
+            mma16(cI, aP, bA8);                // T = T2 (I + A^8)
+            // T diag(b): column n scaled by b_n; rows g, g+8, columns 8 nt + 2t, +1
+            const float b0 = __shfl_sync(0xffffffffu, bl, 2 * t), b1 = __shfl_sync(0xffffffffu, bl, 2 * t + 1);
+            const float b8 = __shfl_sync(0xffffffffu, bl, 8 + 2 * t), b9 = __shfl_sync(0xffffffffu, bl, 9 + 2 * t);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const float s0 = nt ? b8 : b0, s1 = nt ? b9 : b1;
-            const uint32_t lo = pack_half2(cI[nt][0] * s0, cI[nt][1] * s1);   // row g
-            const uint32_t hi = pack_half2(cI[nt][2] * s0, cI[nt][3] * s1);   // row g + 8
-            const int col = 8 * nt + 2 * t;
-            *reinterpret_cast<uint32_t*>(&st.tbr[g * TB_LD + col]) = lo;
-            *reinterpret_cast<uint32_t*>(&st.tbr[(g + 8) * TB_LD + col]) = hi;
-            *reinterpret_cast<uint32_t*>(tbt + tc::interleaved_offset(g, col, kChunk)) = lo;
-            *reinterpret_cast<uint32_t*>(tbt + tc::interleaved_offset(g + 8, col, kChunk)) = hi;
+            for (int nt = 0; nt < 2; ++nt) {
+                const float s0 = nt ? b8 : b0, s1 = nt ? b9 : b1;
+                const uint32_t lo = pack_half2(cI[nt][0] * s0, cI[nt][1] * s1);   // row g
+                const uint32_t hi = pack_half2(cI[nt][2] * s0, cI[nt][3] * s1);   // row g + 8
+                const int col = 8 * nt + 2 * t;
+                *reinterpret_cast<uint32_t*>(&st.tbr[g * TB_LD + col]) = lo;
+                *reinterpret_cast<uint32_t*>(&st.tbr[(g + 8) * TB_LD + col]) = hi;
+                *reinterpret_cast<uint32_t*>(tbt + tc::interleaved_offset(g, col, kChunk)) = lo;
+                *reinterpret_cast<uint32_t*>(tbt + tc::interleaved_offset(g + 8, col, kChunk)) = hi;
+            }
+        } else {
+            solve_substitution(akk, bl, lane, st.tbr, tbt);
         }
         tc::fence_proxy_async_smem();
         __syncwarp();

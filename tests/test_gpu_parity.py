@@ -82,6 +82,22 @@ def test_gate_range_edges(lower_bound, pattern):
     _check(d, tag=f"lower_bound={lower_bound} {pattern}")
 
 
+@pytest.mark.parametrize("similarity", [1.0, 0.99, 0.9])
+@pytest.mark.parametrize("lower_bound", [0.0, -1.0])
+def test_nearly_parallel_keys(similarity, lower_bound):
+    """Keys of every token nearly equal (cosine `similarity` with token 0's key), write
+    strength b ~ 1: A = diag(b) A_kk is then close to the all-ones strictly lower matrix,
+    whose inverse (I + A)^-1 is I minus the subdiagonal although the powers of A grow to
+    C(14, 7); with lower_bound = 0 nothing damps them."""
+    d = synth.make_inputs(1, 64, 2, seed=41, init_dtype="f32", lower_bound=lower_bound)
+    k = synth.bf16_bits_to_f32(d["k"]).astype(np.float64)
+    mix = similarity * k[:, :1] + np.sqrt(max(0.0, 1.0 - similarity ** 2)) * k
+    mix /= np.linalg.norm(mix, axis=-1, keepdims=True)
+    d["k"] = synth.f32_to_bf16_bits(mix.astype(np.float32))
+    d["beta"] = synth.f32_to_bf16_bits(np.full(d["beta"].shape, 12.0, np.float32))
+    _check(d, tag=f"similarity={similarity} lower_bound={lower_bound}")
+
+
 def test_varlen_edge_lengths():
     lens = [1, 15, 16, 17, 0, 33, 64, 5, 2]
     d = synth.make_inputs(1, sum(lens), 4, seed=11, lengths=lens, init_dtype="f32")
