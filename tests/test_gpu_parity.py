@@ -98,6 +98,22 @@ def test_nearly_parallel_keys(similarity, lower_bound):
     _check(d, tag=f"similarity={similarity} lower_bound={lower_bound}")
 
 
+@pytest.mark.parametrize("pattern", ["alternate", "random_sign"])
+def test_sign_flipping_keys(pattern):
+    """One key with flipping signs (k, -k, k, ... or random signs), b ~ 1, no decay: the
+    entries of A are +-1, the delta rule overwrites the same direction every token."""
+    d = synth.make_inputs(1, 64, 2, seed=43, init_dtype="f32", lower_bound=0.0)
+    k = synth.bf16_bits_to_f32(d["k"]).astype(np.float64)
+    T = k.shape[1]
+    if pattern == "alternate":
+        sign = np.where(np.arange(T) % 2 == 0, 1.0, -1.0)
+    else:
+        sign = np.random.default_rng(5).choice([-1.0, 1.0], size=T)
+    d["k"] = synth.f32_to_bf16_bits((k[:, :1] * sign[None, :, None, None]).astype(np.float32))
+    d["beta"] = synth.f32_to_bf16_bits(np.full(d["beta"].shape, 12.0, np.float32))
+    _check(d, tag=pattern)
+
+
 def test_varlen_edge_lengths():
     lens = [1, 15, 16, 17, 0, 33, 64, 5, 2]
     d = synth.make_inputs(1, sum(lens), 4, seed=11, lengths=lens, init_dtype="f32")
