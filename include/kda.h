@@ -74,6 +74,8 @@ typedef enum {
  *               key component must stay below 2^(128 + 16 * lower_bound / ln 2)
  *               in magnitude (about 10 at lower_bound = -5.4, 6,000 at -5)
  *               for that factor to stay finite; unit-norm keys always do.
+ *               v enters a tensor-core product as fp16: its components must stay
+ *               below 65,504 in magnitude.
  *   beta        bf16 [B, T, H]           logits; sigmoid is applied inside
  *   scale       multiplies the output    (finite)
  *   A_log       fp32 [H]                 dt_bias  fp32 [H, K]

@@ -114,6 +114,16 @@ def test_sign_flipping_keys(pattern):
     _check(d, tag=pattern)
 
 
+def test_large_values():
+    """v scaled by 1,000 (components up to a few thousand, inside the fp16 range that
+    the u product needs) and a large initial state: the error stays relative."""
+    d = synth.make_inputs(1, 100, 2, seed=45, init_dtype="f32")
+    v = synth.bf16_bits_to_f32(d["v"]) * np.float32(1000.0)
+    d["v"] = synth.f32_to_bf16_bits(v)
+    d["initial_state"] = d["initial_state"] * np.float32(1000.0)
+    _check(d, tag="large v")
+
+
 def test_varlen_edge_lengths():
     lens = [1, 15, 16, 17, 0, 33, 64, 5, 2]
     d = synth.make_inputs(1, sum(lens), 4, seed=11, lengths=lens, init_dtype="f32")
