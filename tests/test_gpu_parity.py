@@ -130,10 +130,10 @@ def test_varlen_edge_lengths():
     _check(d, tag="varlen edges")
 
 
-@pytest.mark.parametrize("N", [3000, 9000])
+@pytest.mark.parametrize("N", [3000, 9000, 20000])
 def test_varlen_many_short_sequences(N):
     """Thousands of short sequences (lengths 0-20, empty ones included) in one call:
-    many waves of small units, the longest-first order for N <= 8192 and the input
+    many waves of small units, the longest-first order for N <= 16384 and the input
     order above it."""
     rng = np.random.default_rng(N)
     lens = rng.integers(0, 21, size=N)
