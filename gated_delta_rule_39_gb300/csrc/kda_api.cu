@@ -210,7 +210,7 @@ namespace {
 constexpr int kHostBlockMin = 1024;   // tokens per block, at least
 
 int host_block_len(int T) {
-    int blk = (T + 3) / 4;             // about four blocks
+    int blk = (T + 7) / 8;             // about eight blocks
     blk = (blk + kChunk - 1) / kChunk * kChunk;
     return blk > kHostBlockMin ? blk : kHostBlockMin;
 }
