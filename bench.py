@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -63,7 +64,10 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        # raw samples go to KDA_BENCH_CLOCKS_DIR (default: the system temp directory);
+        # the JSON line carries their summary
+        out_dir = os.environ.get("KDA_BENCH_CLOCKS_DIR", tempfile.gettempdir())
+        self.path = os.path.join(out_dir, f"clocks_gpu{gpu_index}.csv")
 
     def __enter__(self):
         try:
