@@ -155,10 +155,10 @@ struct Smem {
     unsigned long long a_ready[2];       // A_kk warp: A_kk written (per chunk parity)
     unsigned long long t_ready[kRing];   // solver: T diag(b) written
     unsigned long long e_free[kEarly];   // both A-product warps are done with the early slot
-    unsigned long long uo_done;          // O|U MMAs complete
     unsigned long long s_done;           // state update + O MMAs complete
     unsigned long long init_ready;       // epilogue: initial state written
-    unsigned long long scaled;           // epilogue: 2^G_last S^T written to the other buffer
+    unsigned long long scaled;           // epilogue: 2^G_last S^T written to the other buffer,
+                                         // and the chunk's O|U MMAs complete (commit)
     unsigned long long epi_done;         // epilogue finished with tensor memory
     uint32_t tmem_base;
 };
@@ -743,8 +743,9 @@ __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
                             d_xb + so + (uint64_t)(((kk >> 2) * X_ROWS * 128 + (kk & 3) * 32) >> 4),
                             id_s, 1);
         tc::mma_ss(uo + 16, d_vt + so, d_tbt + so, id_u, 1);
-        tc::commit(smem_u32(&S.uo_done));
-        if (!mbar_wait(&S.uo_done, (unsigned)(c & 1), err)) return;
+        // one wait for both the [O|U] MMAs and the epilogue's rescale: a wait costs
+        // this thread ~100 cycles even on a completed barrier
+        tc::commit(smem_u32(&S.scaled));
         if (!mbar_wait(&S.scaled, (unsigned)(c & 1), err)) return;
         tc::fence_after_sync();
 #pragma unroll
@@ -925,10 +926,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&S.t_ready[s], 32);          // solver warp
         }
         for (int s = 0; s < kEarly; ++s) mbar_init(&S.e_free[s], 64);   // both A-product warps
-        mbar_init(&S.uo_done, 1);
         mbar_init(&S.s_done, 1);
         mbar_init(&S.init_ready, kEpiWarps * 32);
-        mbar_init(&S.scaled, kEpiWarps * 32);
+        mbar_init(&S.scaled, kEpiWarps * 32 + 1);   // epilogue threads + one commit
         mbar_init(&S.epi_done, kEpiWarps * 32);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&S.a_ready[b], 32);              // the A_kk warp
