@@ -104,7 +104,10 @@ typedef enum {
  * Fixed-length calls use no scratch memory.  Varlen calls take
  * kda_fwd_workspace_bytes() of scratch (the longest-first sequence order)
  * from the stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on
- * `stream`); the call does not synchronise.
+ * `stream`); the call does not synchronise.  The first call on a device
+ * raises the release threshold of that device's default memory pool to its
+ * maximum, so that freed scratch stays in the pool instead of going back to
+ * the driver at every synchronisation (a process-wide setting of that pool).
  */
 int kda_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
             float scale, void* out, const float* A_log, const float* dt_bias,
@@ -137,7 +140,10 @@ int kda_fwd_host(const void* q, const void* k, const void* v, const void* g,
 /*
  * kda_fwd_get_error -- synchronise `stream`, then return and clear the current
  * device's error word: KDA_OK, KDA_ERR_BAD_SEQLENS or KDA_ERR_DEVICE_TIMEOUT
- * (or KDA_ERR_CUDA if the synchronisation itself failed).
+ * (or KDA_ERR_CUDA if the synchronisation itself failed).  There is one word
+ * per device, shared by every call on it whatever its stream: it keeps the
+ * first error any kernel recorded since the last read, and a call still
+ * running on another stream may set it after this read.
  */
 int kda_fwd_get_error(void* stream);
 
