@@ -215,6 +215,25 @@ int host_block_len(int T) {
     return blk > kHostBlockMin ? blk : kHostBlockMin;
 }
 
+// First token of each block, then T.  The last block is halved down to 256 tokens
+// (512, 256, 256 after 1,024-token blocks): what runs after the last upload ends is
+// the last block's kernel and download, so a short tail finishes sooner.
+constexpr int kHostTailMin = 256;
+
+std::vector<int> host_blocks(int T) {
+    const int blk = host_block_len(T);
+    std::vector<int> starts;
+    for (int t = 0; t < T; t += blk) starts.push_back(t);
+    for (int last = starts.back();;) {
+        const int half = (T - last) / 2 / kChunk * kChunk;
+        if (half < kHostTailMin) break;
+        last += half;
+        starts.push_back(last);
+    }
+    starts.push_back(T);
+    return starts;
+}
+
 bool host_pipelined(const int32_t* cu_seqlens, int B, int T) {
     return cu_seqlens == nullptr && B == 1 && T >= 2 * kHostBlockMin;
 }
@@ -223,8 +242,8 @@ int host_fwd_blocks(const void* q, const void* k, const void* v, const void* g, 
                     float scale, void* out, const float* A_log, const float* dt_bias,
                     float lower_bound, const void* initial_state, int initial_state_dtype,
                     void* final_state, int final_state_dtype, int T, int H, cudaStream_t s) {
-    const int blk = host_block_len(T);
-    const int nblk = (T + blk - 1) / blk;
+    const std::vector<int> starts = host_blocks(T);
+    const int nblk = (int)starts.size() - 1;
     const size_t row = (size_t)H * kDim * 2, brow = (size_t)H * 2;   // bytes per token
     const size_t n_qk = (size_t)T * row, n_b = (size_t)T * brow;
     const size_t n_s = (size_t)H * kDim * kDim;
@@ -258,7 +277,7 @@ int host_fwd_blocks(const void* q, const void* k, const void* v, const void* g, 
             e = cudaMemcpyAsync(d + offs[6 + i], params[i], sizes[6 + i], cudaMemcpyHostToDevice, sin);
     const void* tok_src[] = {q, k, v, g};
     for (int b = 0; b < nblk && e == cudaSuccess; ++b) {
-        const size_t t0 = (size_t)b * blk, len = (size_t)((b + 1) * blk < T ? blk : T - b * blk);
+        const size_t t0 = (size_t)starts[b], len = (size_t)(starts[b + 1] - starts[b]);
         for (int i = 0; i < 4 && e == cudaSuccess; ++i)
             e = cudaMemcpyAsync(d + offs[i] + t0 * row, static_cast<const unsigned char*>(tok_src[i]) + t0 * row,
                                 len * row, cudaMemcpyHostToDevice, sin);
@@ -270,8 +289,8 @@ int host_fwd_blocks(const void* q, const void* k, const void* v, const void* g, 
     // blocks in order on `s`, each output block copied out as soon as it is written
     void* carry = d + offs[10];
     for (int b = 0; b < nblk && e == cudaSuccess && rc == KDA_OK; ++b) {
-        const size_t t0 = (size_t)b * blk;
-        const int len = (b + 1) * blk < T ? blk : T - b * blk;
+        const size_t t0 = (size_t)starts[b];
+        const int len = starts[b + 1] - starts[b];
         const bool first = b == 0, last = b == nblk - 1;
         e = cudaStreamWaitEvent(s, ev[b], 0);
         if (e != cudaSuccess) break;
