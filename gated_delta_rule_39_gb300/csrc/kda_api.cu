@@ -207,26 +207,19 @@ namespace {
 // block i + 1 is copied in and block i - 1's output is copied out, on copy
 // streams ordered against `s` by events.  The state passes from block to block
 // through an fp32 device buffer (exact: the kernel keeps the state in fp32).
-constexpr int kHostBlockMin = 1024;   // tokens per block, at least
+constexpr int kHostPipelineMin = 2048;   // tokens: shorter calls run in one block
+constexpr int kHostBlockMin = 256;       // tokens: no block is halved below this
 
-int host_block_len(int T) {
-    int blk = (T + 7) / 8;             // about eight blocks
-    blk = (blk + kChunk - 1) / kChunk * kChunk;
-    return blk > kHostBlockMin ? blk : kHostBlockMin;
-}
-
-// First token of each block, then T.  The last block is halved down to 256 tokens
-// (512, 256, 256 after 1,024-token blocks): what runs after the last upload ends is
-// the last block's kernel and download, so a short tail finishes sooner.
-constexpr int kHostTailMin = 256;
-
+// First token of each block, then T.  Each block takes half of the tokens still left
+// (rounded down to whole chunks) until that would be under kHostBlockMin: 4,096, 2,048,
+// 1,024, 512, 256 and 256 tokens at T = 8,192.  The uploads run back to back whatever
+// the split; what runs after the last one ends is the last block's kernel and download,
+// so short blocks at the end finish sooner, and long ones at the start make fewer copies.
 std::vector<int> host_blocks(int T) {
-    const int blk = host_block_len(T);
-    std::vector<int> starts;
-    for (int t = 0; t < T; t += blk) starts.push_back(t);
-    for (int last = starts.back();;) {
+    std::vector<int> starts{0};
+    for (int last = 0;;) {
         const int half = (T - last) / 2 / kChunk * kChunk;
-        if (half < kHostTailMin) break;
+        if (half < kHostBlockMin) break;
         last += half;
         starts.push_back(last);
     }
@@ -235,7 +228,7 @@ std::vector<int> host_blocks(int T) {
 }
 
 bool host_pipelined(const int32_t* cu_seqlens, int B, int T) {
-    return cu_seqlens == nullptr && B == 1 && T >= 2 * kHostBlockMin;
+    return cu_seqlens == nullptr && B == 1 && T >= kHostPipelineMin;
 }
 
 int host_fwd_blocks(const void* q, const void* k, const void* v, const void* g, const void* beta,

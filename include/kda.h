@@ -125,11 +125,11 @@ int kda_fwd(const void* q, const void* k, const void* v, const void* g, const vo
  * device -> host, frees the buffers and synchronises `stream` before
  * returning, so the outputs are ready on return.  cu_seqlens is validated on
  * the host (KDA_ERR_BAD_SEQLENS) before anything is copied.  A fixed-length
- * call with B == 1 and T >= 2048 runs in token blocks (multiples of 16 tokens:
- * about eight equal ones, the last halved down to 256 tokens; the state carried
- * in fp32 on the device) so that the copies in and out overlap the kernel on
- * two extra streams; its results are bit-identical to one kda_fwd call on the
- * same data.
+ * call with B == 1 and T >= 2048 runs in token blocks (each half of the
+ * tokens still left, in whole 16-token chunks, down to 256 tokens; the state
+ * carried in fp32 on the device) so that the copies in and out overlap the
+ * kernel on two extra streams; its results are bit-identical to one kda_fwd
+ * call on the same data.
  */
 int kda_fwd_host(const void* q, const void* k, const void* v, const void* g,
                  const void* beta, float scale, void* out, const float* A_log,
