@@ -1,0 +1,63 @@
+"""Host logic of bench.py that feeds its JSON line (no GPU): clock-sample
+summaries, the DRAM-traffic record tied to the kernel's source, the peaks."""
+import json
+import os
+
+import bench
+
+
+def _sampler_with(tmp_path, monkeypatch, rows):
+    monkeypatch.setenv("KDA_BENCH_CLOCKS_DIR", str(tmp_path))
+    s = bench.ClockSampler(0)
+    with open(s.path, "w") as f:
+        f.write("\n".join(rows) + "\n")
+    s.proc = object()   # stands for a sampler that ran
+    return s
+
+
+def test_clock_summary_loaded_samples_and_reasons(tmp_path, monkeypatch):
+    idle = "0, 1200, 2070, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active"
+    busy = "0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active"
+    capped = "0, 1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active"
+    s = _sampler_with(tmp_path, monkeypatch, [idle, busy, busy, capped, "garbage line"])
+    out = s.summary()
+    # the idle sample (power under 20 % of the peak) is not "under load"
+    assert out["samples"] == 4 and out["samples_under_load"] == 3
+    assert out["sm_mhz"] == 2070.0 and out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_summary_reports_thermal_slowdown(tmp_path, monkeypatch):
+    row = "0, 1500, 2070, 1000.0, 0x40, Not Active, Not Active, Active, Not Active"
+    out = _sampler_with(tmp_path, monkeypatch, [row]).summary()
+    assert out["reasons"] == ["sw_thermal_slowdown"] and out["sm_mhz"] == 1500.0
+
+
+def test_clock_summary_without_nvidia_smi(tmp_path, monkeypatch):
+    monkeypatch.setenv("KDA_BENCH_CLOCKS_DIR", str(tmp_path))
+    assert bench.ClockSampler(0).summary()["sm_mhz"] is None
+
+
+def test_traffic_record_follows_the_kernel_source(monkeypatch):
+    with open(os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")) as f:
+        rec = json.load(f)["fused_kernel"]
+    assert rec["bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
+    # the committed record was taken on the committed source
+    assert bench.ncu_traffic("fused_kernel") == rec["bytes_per_launch"]
+    # any change to the kernel's source voids it
+    monkeypatch.setattr(bench, "source_digest", lambda *names: "0" * 16)
+    assert bench.ncu_traffic("fused_kernel") is None
+    assert bench.ncu_traffic("no_such_kernel") is None
+
+
+def test_peaks_fall_back_when_unmeasured(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.peaks() == (6800.0, 1900.0, "of fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 7000, "bf16_tflops": 2000}))
+    assert bench.peaks() == (7000.0, 2000.0, "of measured")
+
+
+def test_algorithmic_work_per_token_head():
+    # 6KV + 2C(3K + 2V) flops and q, k, v, g, out (256 B each) + beta (2 B)
+    assert bench.FLOP_PER_TH == 118784
+    assert bench.BYTES_PER_TH == 1282
