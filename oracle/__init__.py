@@ -223,18 +223,5 @@ def kda_recurrence(*a, **kw):
     return get().kda_recurrence(*a, **kw)
 
 
-def round_to_bf16(x: np.ndarray) -> np.ndarray:
-    """Round float64 values to the nearest bf16 (ties to even), returned as float64.
-
-    Used to compare against a bf16 output at the output's own resolution.
-    """
-    f = np.ascontiguousarray(x, dtype=np.float64).astype(np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    nan = np.isnan(f)
-    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
-    r[nan] = 0x7FC0
-    return bf16_bits_to_f64(r)
-
-
 if __name__ == "__main__":  # pragma: no cover
     print(build(force="--force" in sys.argv))

@@ -1,8 +1,8 @@
 """CUDA path (through the C ABI) against the fp64 oracle, element by element.
 
-Small cases compare every output; the full-size workloads compare every
-output and state of a sample of heads (heads are independent recurrences, so
-a sampled head is checked completely, across all its chunks and tiles).
+Every case compares every output element and every final-state element of
+every (sequence, head) unit, the full-size workloads included (the oracle
+runs all heads of a T = 8192 workload in a few seconds on the host cores).
 """
 import numpy as np
 import pytest
@@ -151,29 +151,29 @@ def test_varlen_single_sequence_equals_fixed():
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
 
 
-def test_prefill_h64_sampled_heads():
+def test_prefill_h64_all_heads():
     d = synth.make_workload("prefill_t8192_h64")
-    _check(d, heads=[0, 17, 42, 63], tag="prefill h64")
+    _check(d, tag="prefill h64")
 
 
-def test_prefill_h96_sampled_heads():
+def test_prefill_h96_all_heads():
     d = synth.make_workload("prefill_t8192_h96")
-    _check(d, heads=[0, 31, 64, 95], tag="prefill h96")
+    _check(d, tag="prefill h96")
 
 
-def test_varlen_mixed_sampled_heads():
+def test_varlen_mixed_all_heads():
     d = synth.make_workload("varlen_mixed_t8192_h96")
-    _check(d, heads=[3, 50, 94], tag="varlen mixed")
+    _check(d, tag="varlen mixed")
 
 
-def test_varlen_uniform_sampled_heads():
+def test_varlen_uniform_all_heads():
     d = synth.make_workload("varlen_uniform_8x1024_h96")
-    _check(d, heads=[1, 48, 90], tag="varlen uniform")
+    _check(d, tag="varlen uniform")
 
 
 def test_long_context_state_carry():
     """T=65536, H=32 in two 32768-token calls carrying the fp32 state equals one call,
-    and both match the oracle on sampled heads."""
+    and both match the oracle on every head."""
     import torch
     import gated_delta_rule_39_gb300 as kda
     d = synth.make_workload("carry_t65536_h32")
@@ -203,11 +203,10 @@ def test_long_context_state_carry():
     # so the arithmetic is identical
     assert torch.equal(split, full)
     assert torch.equal(S_end, S_full)
-    heads = [5, 26]
-    ro, rs = run_oracle(d, heads=heads)
-    e = out_error(to_f64(full)[:, :, heads], ro[:, :, heads])
+    ro, rs = run_oracle(d)
+    e = out_error(to_f64(full), ro)
     assert e["ok"], e
-    se = state_error(to_f64(S_full)[:, heads], rs[:, heads])
+    se = state_error(to_f64(S_full), rs)
     assert se["ok"], se
 
 
