@@ -26,6 +26,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -172,8 +174,151 @@ def ncu_traffic(kernel: str):
 
 
 # ---------------------------------------------------------------------------
+# The other workloads of the pages' benchmark reported in the same line (each a
+# nested object with its own timing, roofline and CPU-oracle sample).
+OTHER_WORKLOADS = ("prefill_t8192_h64", "varlen_mixed_t8192_h96", "varlen_uniform_8x1024_h96",
+                   "carry_t65536_h32")
+
+
+def algorithmic_work(d, calls):
+    """(bytes, flops, token-heads) of one step: every kda_fwd call of the step moves its
+    inputs and outputs once, plus each call's state read (if any) and write."""
+    B, T, H, _ = d["q"].shape
+    N = d["N"]
+    th = B * T * H
+    s0 = d.get("initial_state")
+    init_b = 0 if s0 is None else (2 if s0.dtype == np.uint16 else 4)
+    state_bytes = 0
+    for i in range(calls):
+        read_b = init_b if i == 0 else 4      # later calls read the carried fp32 state
+        state_bytes += N * H * K * V * (read_b + 4)
+    return BYTES_PER_TH * th + state_bytes, FLOP_PER_TH * th, th
+
+
+def roofline_of(kernel, ms, bytes_, flop, hbm, tflops, src):
+    t_hbm = bytes_ / (hbm * 1e9)
+    t_tc = flop / (tflops * 1e12)
+    if t_tc >= t_hbm:
+        roof = {"bound": "tensor", "achieved": flop / (ms * 1e-3) / 1e12, "peak": tflops,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": bytes_ / (ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = kernel
+    roof["kernel_ms"] = ms
+    roof["peak_source"] = src
+    return roof
+
+
+class Runner:
+    """Device copies of one workload and the call sequence of one step."""
+
+    def __init__(self, d, device, stream):
+        import torch
+        import gated_delta_rule_39_gb300 as kda
+        self.kda = kda
+        self.d = d
+        self.stream = stream
+        B, T, H, _ = d["q"].shape
+        self.B, self.T, self.H, self.N = B, T, H, d["N"]
+
+        def bf16(bits):
+            return (torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
+                    .view(torch.bfloat16))
+
+        self.x = {n: bf16(d[n]) for n in ("q", "k", "v", "g", "beta")}
+        self.A_log = torch.from_numpy(d["A_log"]).to(device)
+        self.dt_bias = torch.from_numpy(d["dt_bias"]).to(device)
+        s0 = d.get("initial_state")
+        self.s0 = None if s0 is None else (bf16(s0) if s0.dtype == np.uint16
+                                           else torch.from_numpy(s0).to(device))
+        cu = d.get("cu_seqlens")
+        self.cu = None if cu is None else torch.from_numpy(cu.astype(np.int32)).to(device)
+        self.out = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=device)
+        self.s1 = torch.empty((self.N, H, K, V), dtype=torch.float32, device=device)
+        w = d.get("workload")
+        self.calls = w.carry_calls if w is not None else 1
+        if self.calls > 1:   # one sequence cut into `calls` pieces, the state carried
+            L = T // self.calls
+            sl = lambda t, a: t[:, a * L:(a + 1) * L]
+            self.pieces = [{n: sl(self.x[n], i) for n in self.x} for i in range(self.calls)]
+            self.opieces = [sl(self.out, i) for i in range(self.calls)]
+            self.carry = torch.empty_like(self.s1)
+
+    def step(self):
+        kda, x, d = self.kda, self.x, self.d
+        if self.calls == 1:
+            kda.kda_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], d["scale"], self.out,
+                        self.A_log, self.dt_bias, d["lower_bound"], initial_state=self.s0,
+                        final_state=self.s1, cu_seqlens=self.cu, stream=self.stream)
+            return
+        for i, xp in enumerate(self.pieces):
+            kda.kda_fwd(xp["q"], xp["k"], xp["v"], xp["g"], xp["beta"], d["scale"],
+                        self.opieces[i], self.A_log, self.dt_bias, d["lower_bound"],
+                        initial_state=(self.s0 if i == 0 else self.carry),
+                        final_state=(self.s1 if i == self.calls - 1 else self.carry),
+                        stream=self.stream)
+
+
+def timed_steps(runner, steps, warmup, pg=None, device=None, sampler=None):
+    """Warm up, then time `steps` steps with CUDA events on the launch stream; returns
+    (elapsed ms, {kernel: (total ms, launches)})."""
+    import torch
+    kda = runner.kda
+    for _ in range(warmup):
+        runner.step()
+    torch.cuda.synchronize(device)
+    err = kda.kda_fwd_get_error(runner.stream)
+    if err != 0:
+        raise RuntimeError(f"device error after warm-up: {kda.kda_status_string(err)}")
+    if sampler:
+        sampler.__enter__()
+    kda.kda_profile_enable(True)
+    barrier(pg, device)
+    torch.cuda.synchronize(device)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(runner.stream)
+    for _ in range(steps):
+        runner.step()
+    ev1.record(runner.stream)
+    torch.cuda.synchronize(device)
+    barrier(pg, device)
+    elapsed_ms = ev0.elapsed_time(ev1)
+    prof = kda.kda_profile_read()
+    kda.kda_profile_enable(False)
+    if sampler:
+        sampler.__exit__(None, None, None)
+    return elapsed_ms, prof
+
+
+def workload_line(name, d, elapsed_ms, prof, steps, world, calls):
+    """Throughput and roofline of one workload from its timing."""
+    hbm, tflops, src = peaks()
+    B, T, H, _ = d["q"].shape
+    bytes_, flop, th = algorithmic_work(d, calls)
+    tokens_per_step = B * T
+    dom = max(prof, key=lambda n: prof[n][0])
+    dom_ms = prof[dom][0] / max(1, prof[dom][1]) * calls   # one step's share of the kernel
+    ms_per_step = elapsed_ms / steps
+    roof = roofline_of(dom, dom_ms, bytes_, flop, hbm, tflops, src) if dom == "fused_kernel" else None
+    if roof is not None:
+        roof["traffic"] = ncu_traffic(dom) if name == WORKLOAD else None
+    t_roof = max(bytes_ / (hbm * 1e9), flop / (tflops * 1e12))
+    return {
+        "workload": name, "value": world * tokens_per_step * steps / (elapsed_ms / 1e3),
+        "unit": "tokens/s", "ms_per_step": ms_per_step, "calls_per_step": calls,
+        "roofline": roof,
+        "path_roofline": {"bound": "hbm" if bytes_ / (hbm * 1e9) >= flop / (tflops * 1e12) else "tensor",
+                          "roofline_ms": t_roof * 1e3, "measured_ms": ms_per_step,
+                          "frac": t_roof * 1e3 / ms_per_step, "bytes": bytes_, "flop": flop,
+                          "peak_source": src},
+        "kernel_ms": {n: (ms / max(1, c)) for n, (ms, c) in prof.items() if c},
+        "gpu_launches": sum(c for _, c in prof.values()),
+    }
+
+
 def run_cuda(args, world, rank, local, pg):
-    import numpy as np
     import torch
 
     import synth
@@ -182,108 +327,42 @@ def run_cuda(args, world, rank, local, pg):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     kda.load_library()
+    stream = torch.cuda.current_stream(device)
+    name = args.workload
     if args.heads:
-        w = synth.WORKLOADS[WORKLOAD]
+        w = synth.WORKLOADS[name]
         d = synth.make_inputs(w.B, w.T, args.heads, seed=rank, init_dtype=w.init_dtype)
     else:
-        d = synth.make_workload(WORKLOAD, seed=rank)
-    B, T, H, _ = d["q"].shape
-    N = d["N"]
-
-    def bf16(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
-
-    x = {n: bf16(d[n]) for n in ("q", "k", "v", "g", "beta")}
-    A_log = torch.from_numpy(d["A_log"]).to(device)
-    dt_bias = torch.from_numpy(d["dt_bias"]).to(device)
-    s0 = bf16(d["initial_state"])
-    out = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=device)
-    s1 = torch.empty((N, H, K, V), dtype=torch.float32, device=device)
-    stream = torch.cuda.current_stream(device)
-
-    def step():
-        kda.kda_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], d["scale"], out, A_log, dt_bias,
-                    d["lower_bound"], initial_state=s0, final_state=s1, stream=stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(device)
-    err = kda.kda_fwd_get_error(stream)
-    if err != 0:
-        raise RuntimeError(f"device error after warm-up: {kda.kda_status_string(err)}")
+        d = synth.make_workload(name, seed=rank)
+    runner = Runner(d, device, stream)
+    B, T, H, N = runner.B, runner.T, runner.H, runner.N
 
     # ---- timed region: K steps, launch timing on the launch stream -------------
     sampler = ClockSampler(local) if rank == 0 else None
-    if sampler:
-        sampler.__enter__()
-    kda.kda_profile_enable(True)
-    barrier(pg, device)
-    torch.cuda.synchronize(device)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize(device)
-    barrier(pg, device)
-    elapsed_ms = ev0.elapsed_time(ev1)
-    prof = kda.kda_profile_read()
-    kda.kda_profile_enable(False)
-    if sampler:
-        sampler.__exit__(None, None, None)
+    elapsed_ms, prof = timed_steps(runner, args.steps, args.warmup, pg, device, sampler)
     elapsed_ms = max_over_ranks(pg, elapsed_ms, device)
-
-    tokens_per_step = B * T
-    value = world * tokens_per_step * args.steps / (elapsed_ms / 1e3)
-    ms_per_step = elapsed_ms / args.steps
-    launches = sum(n for _, n in prof.values())
-
-    # ---- roofline of the dominant kernel and of the whole call --------------------
-    hbm, tflops, src = peaks()
-    th = B * T * H
-    dom = max(prof, key=lambda n: prof[n][0])
-    dom_ms = prof[dom][0] / max(1, prof[dom][1])
-    dom_flop = KERNEL_FLOP_PER_TH.get(dom, 0) * th
-    dom_bytes = KERNEL_BYTES_PER_TH.get(dom, 0) * th
-    if dom == "fused_kernel":
-        dom_bytes += N * H * K * V * (2 + 4)   # bf16 initial state read, fp32 final write
-    t_hbm = dom_bytes / (hbm * 1e9)
-    t_tc = dom_flop / (tflops * 1e12)
-    if t_tc >= t_hbm:
-        roof = {"bound": "tensor", "achieved": dom_flop / (dom_ms * 1e-3) / 1e12, "peak": tflops,
-                "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": dom_bytes / (dom_ms * 1e-3) / 1e9, "peak": hbm,
-                "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = dom
-    roof["kernel_ms"] = dom_ms
-    roof["traffic"] = ncu_traffic(dom)
-    roof["peak_source"] = src
-    path_bytes = BYTES_PER_TH * th + N * H * K * V * (2 + 4)
-    path_flop = FLOP_PER_TH * th
-    t_roof = max(path_bytes / (hbm * 1e9), path_flop / (tflops * 1e12))
-    path_roof = {"bound": "hbm" if path_bytes / (hbm * 1e9) >= path_flop / (tflops * 1e12)
-                 else "tensor",
-                 "roofline_ms": t_roof * 1e3, "measured_ms": ms_per_step,
-                 "frac": t_roof * 1e3 / ms_per_step, "bytes": path_bytes, "flop": path_flop,
-                 "peak_source": src}
+    main = workload_line(name, d, elapsed_ms, prof, args.steps, world, runner.calls)
 
     # ---- end-to-end through the host-buffer entry point ---------------------------
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and runner.calls == 1:
         hx = {n: torch.from_numpy(np.ascontiguousarray(d[n]).view(np.int16)).view(torch.bfloat16)
-              .pin_memory() for n in ("q", "k", "v", "g", "beta", "initial_state")}
+              .pin_memory() for n in ("q", "k", "v", "g", "beta")}
+        s0 = d.get("initial_state")
+        hs0 = None if s0 is None else (
+            torch.from_numpy(np.ascontiguousarray(s0).view(np.int16)).view(torch.bfloat16).pin_memory()
+            if s0.dtype == np.uint16 else torch.from_numpy(s0).pin_memory())
         hA = torch.from_numpy(d["A_log"]).pin_memory()
         hdt = torch.from_numpy(d["dt_bias"]).pin_memory()
+        hcu = None if d.get("cu_seqlens") is None else torch.from_numpy(
+            d["cu_seqlens"].astype(np.int32))
         hout = torch.empty((B, T, H, V), dtype=torch.bfloat16).pin_memory()
         hs1 = torch.empty((N, H, K, V), dtype=torch.float32).pin_memory()
 
         def host_step():
             kda.kda_fwd_host(hx["q"], hx["k"], hx["v"], hx["g"], hx["beta"], d["scale"], hout,
-                             hA, hdt, d["lower_bound"], initial_state=hx["initial_state"],
-                             final_state=hs1, stream=stream, device=device)
+                             hA, hdt, d["lower_bound"], initial_state=hs0, final_state=hs1,
+                             cu_seqlens=hcu, stream=stream, device=device)
 
         host_step()
         e2e_steps = max(1, min(args.steps, 5))
@@ -294,54 +373,82 @@ def run_cuda(args, world, rank, local, pg):
         t1 = time.perf_counter()
         e2e_s = max_over_ranks(pg, t1 - t0, device)
         h2d = sum(t.numel() * t.element_size() for t in hx.values()) + hA.numel() * 4 + hdt.numel() * 4
+        if hs0 is not None:
+            h2d += hs0.numel() * hs0.element_size()
+        if hcu is not None:
+            h2d += hcu.numel() * 4
         d2h = hout.numel() * 2 + hs1.numel() * 4
-        e2e = {"value": world * tokens_per_step * e2e_steps / e2e_s, "unit": "tokens/s",
+        e2e = {"value": world * B * T * e2e_steps / e2e_s, "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "entry_point": "kda_fwd_host"}
 
     # ---- CPU oracle on a bounded sample (rank 0, N = 1 only) -----------------------
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(d, target_s=args.cpu_seconds)
+        cpu = cpu_baseline(d, name, target_s=args.cpu_seconds)
 
     clocks = sampler.summary() if sampler else None
+
+    # ---- the pages' other workloads, one nested object each (rank 0 prints) --------
+    others = {}
+    if not args.heads and not args.no_other_workloads and name == WORKLOAD:
+        for other in OTHER_WORKLOADS:
+            od = synth.make_workload(other, seed=rank)
+            orun = Runner(od, device, stream)
+            ems, oprof = timed_steps(orun, max(3, args.steps // 2), 3, pg, device)
+            ems = max_over_ranks(pg, ems, device)
+            rec = workload_line(other, od, ems, oprof, max(3, args.steps // 2), world, orun.calls)
+            rec["steps"] = max(3, args.steps // 2)
+            rec["warmup"] = 3
+            if world == 1 and not args.no_cpu_baseline:
+                rec["cpu_baseline"] = cpu_baseline(od, other, target_s=args.cpu_seconds / 4)
+            others[other] = rec
+            del orun
+            torch.cuda.empty_cache()
+
     if rank == 0:
         if args.heads:
-            line_workload = f"{WORKLOAD} with H={H} (profiling case, not a bench line)"
+            line_workload = f"{name} with H={H} (profiling case, not a bench line)"
         else:
-            line_workload = WORKLOAD
-        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            line_workload = name
+        s0 = d.get("initial_state")
+        line = {"metric": METRIC, "value": main["value"], "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "compute": "f16 and tf32 tensor-core MMA, f32 accumulate",
                 "data": "synthetic (seeded; shapes of the pages' T=8192 H=96 D=128 benchmark)",
                 "config": {"workload": line_workload, "B": B, "T": T, "H": H, "K": K, "V": V,
-                           "initial_state": "bf16", "final_state": "f32",
+                           "initial_state": (None if s0 is None else
+                                             ("bf16" if s0.dtype == np.uint16 else "f32")),
+                           "final_state": "f32",
                            "l2": "inputs larger than L2 (1.02 GB read+written per step vs "
                                  "126 MB L2); no flush",
                            "parallelism": f"replicas x{world}"},
-                "roofline": roof, "path_roofline": path_roof, "cpu_baseline": cpu,
-                "e2e": e2e, "gpu_launches": launches,
-                "kernel_ms": {n: (ms / max(1, c)) for n, (ms, c) in prof.items() if c},
-                "clocks": clocks}
+                "roofline": main["roofline"], "path_roofline": main["path_roofline"],
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": main["gpu_launches"],
+                "kernel_ms": main["kernel_ms"], "clocks": clocks}
+        if others:
+            line["workloads"] = others
         print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(d, target_s: float = 12.0):
-    """Time the fp64 oracle on a subset of heads (full T) of the same inputs."""
+def cpu_baseline(d, workload: str = WORKLOAD, target_s: float = 12.0):
+    """Time the fp64 oracle on a subset of heads (all tokens) of the same inputs."""
     import oracle
     H = d["q"].shape[2]
     T = d["q"].shape[1]
     threads = oracle.default_threads()
     # the oracle works on float64 copies; convert once outside the timing
     conv = {n: oracle.bf16_bits_to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")}
-    s0 = oracle.bf16_bits_to_f64(d["initial_state"]) if d.get("initial_state") is not None else None
+    s0 = d.get("initial_state")
+    if s0 is not None:
+        s0 = oracle.bf16_bits_to_f64(s0) if s0.dtype == np.uint16 else s0.astype(np.float64)
 
     def run(heads):
         t0 = time.perf_counter()
         oracle.kda_fwd(conv["q"], conv["k"], conv["v"], conv["g"], conv["beta"], d["scale"],
                        d["A_log"], d["dt_bias"], d["lower_bound"], initial_state=s0,
-                       heads=heads, n_threads=threads)
+                       cu_seqlens=d.get("cu_seqlens"), heads=heads, n_threads=threads)
         return time.perf_counter() - t0
 
     probe = min(H, threads)
@@ -354,7 +461,7 @@ def cpu_baseline(d, target_s: float = 12.0):
     tokens_equiv = T * n_heads / H
     return {"value": tokens_equiv / t, "unit": "tokens/s", "cores": min(threads, n_heads),
             "kind": "oracle",
-            "sample": f"{n_heads} of {H} heads x {T} tokens of {WORKLOAD}; tokens/s counts "
+            "sample": f"{n_heads} of {H} heads x {T} tokens of {workload}; tokens/s counts "
                       f"a token as all {H} heads ({t:.1f} s)"}
 
 
@@ -391,7 +498,11 @@ def run_reference(args, world, rank, local, pg):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": 1, "T": T, "H": H, "K": K, "V": V},
+        "config": {"workload": WORKLOAD, "B": 1, "T": T, "H": H, "K": K, "V": V,
+                   "initial_state": "bf16", "final_state": "f32",
+                   "l2": "inputs larger than L2 (1.02 GB read+written per step vs 126 MB L2); "
+                         "no flush",
+                   "parallelism": f"replicas x{world}"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -409,6 +520,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--heads", type=int, default=0,
                     help="profiling only: run the workload with this many heads instead")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="time this workload instead of the headline one (profiling)")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the nested measurements of the other workloads")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "cuda":
         print("note: warm-up raised to 3 steps", file=sys.stderr)

@@ -54,7 +54,13 @@ def load_library():
     if not os.path.exists(_LIB_PATH):
         raise RuntimeError(f"CUDA library {_LIB_PATH} is missing; build it with "
                            "`python -c 'import __graft_entry__ as g; g.build()'`")
-    lib = ctypes.CDLL(_LIB_PATH)
+    _lib = declare(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def declare(lib):
+    """Set the argument and result types of the C ABI's functions on a loaded library
+    (this package's build, or a variant of it built with other flags)."""
     fwd_args = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, ctypes.c_float, _vp,
                 ctypes.c_int, _vp, ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp]
@@ -79,7 +85,6 @@ def load_library():
     lib.kda_profile_read.restype = ctypes.c_int
     lib.kda_kernel_name.argtypes = [ctypes.c_int]
     lib.kda_kernel_name.restype = ctypes.c_char_p
-    _lib = lib
     return lib
 
 

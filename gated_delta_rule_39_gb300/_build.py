@@ -31,18 +31,27 @@ def _inputs() -> list[str]:
         os.path.join(os.path.dirname(HERE), "include", "kda.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(path: str = LIB) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          lib: str | None = None) -> str:
+    """Build the library (or, with `lib`, a variant of it under another file name, e.g.
+    with -DKDA_SPIN_LIMIT=... for tests of the wait bounds) and return its path."""
+    if lib is not None:
+        return _build_to(os.path.join(OUT_DIR, lib), force, verbose, extra_flags)
+    return _build_to(LIB, force, verbose, extra_flags)
+
+
+def _build_to(path: str, force: bool, verbose: bool, extra_flags: list[str] | None) -> str:
+    if not force and up_to_date(path):
+        return path
     os.makedirs(OUT_DIR, exist_ok=True)
-    obj_dir = os.path.join(OUT_DIR, f"obj{os.getpid()}")
+    obj_dir = os.path.join(OUT_DIR, f"obj_{os.path.basename(path)}_{os.getpid()}")
     os.makedirs(obj_dir, exist_ok=True)
     flags = NVCC_FLAGS + (extra_flags or [])
     cc = nvcc()
@@ -59,13 +68,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 
     with ThreadPoolExecutor(max_workers=max(1, len(sources()))) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = path + f".tmp{os.getpid()}"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, path)
     shutil.rmtree(obj_dir, ignore_errors=True)
-    return LIB
+    return path
 
 
 if __name__ == "__main__":  # pragma: no cover

@@ -549,8 +549,9 @@ int kda_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
         M.valid = scratch + N;       // set to 0 or 1 by the sequence map
     }
     cudaError_t e = cudaSuccess;
-    if (varlen) e = launch_seqmap(P, M, err, s);
-    if (e == cudaSuccess) e = launch_fused(P, M, err, s);
+    if (varlen) e = timed_launch(KDA_KERNEL_SEQMAP, s, [&] { return launch_seqmap(P, M, err, s); });
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_FUSED, s, [&] { return launch_fused(P, M, err, s); });
     if (e != cudaSuccess) return cuda_fail(KDA_ERR_LAUNCH, e);
     return KDA_OK;
 }

@@ -31,11 +31,26 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
 #include "kda_internal.cuh"
 #include "kda_tcgen05.cuh"
+
+// Every wait of the kernel is bounded.  A pipeline wait gives up after KDA_SPIN_LIMIT
+// SM cycles (about 2 s at the default): it records KDA_ERR_DEVICE_TIMEOUT in the error
+// word and its role stops.  Before a CTA exits, the roles that started asynchronous work
+// wait for it (up to KDA_DRAIN_LIMIT cycles each): the loader for the TMA copies it
+// issued, the MMA thread for its MMAs and commits; tensor memory is released only after
+// the MMA thread has drained and the epilogue has finished with it.  Both limits can be
+// set at build time (-DKDA_SPIN_LIMIT=...).
+#ifndef KDA_SPIN_LIMIT
+#define KDA_SPIN_LIMIT (1LL << 32)
+#endif
+#ifndef KDA_DRAIN_LIMIT
+#define KDA_DRAIN_LIMIT (1LL << 33)
+#endif
 
 namespace kda {
 
@@ -160,6 +175,7 @@ struct Smem {
     unsigned long long scaled;           // epilogue: 2^G_last S^T written to the other buffer,
                                          // and the chunk's O|U MMAs complete (commit)
     unsigned long long epi_done;         // epilogue finished with tensor memory
+    unsigned long long drain;            // the MMA thread's exit drain (one commit)
     uint32_t tmem_base;
 };
 
@@ -181,12 +197,13 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* b, unsigned pa
         : "memory");
     return ok != 0;
 }
-// Bounded wait: gives up after about 2^32 SM cycles (~2 s) and reports a timeout.
-__device__ __forceinline__ bool mbar_wait(unsigned long long* b, unsigned parity, int* err) {
+// Bounded wait: gives up after `limit` SM cycles and reports a timeout.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* b, unsigned parity, int* err,
+                                          long long limit = KDA_SPIN_LIMIT) {
     if (mbar_try_wait(b, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(b, parity)) {
-        if (clock64() - t0 > (1LL << 32)) {
+        if (clock64() - t0 > limit) {
             set_error(err, KDA_ERR_DEVICE_TIMEOUT);
             return false;
         }
@@ -265,7 +282,8 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 
 __device__ void loader(const RawMaps& TM, const Unit& U, Smem& S, int* err) {
     const CUtensorMap* maps[4] = {&TM.q, &TM.k, &TM.v, &TM.g};
-    for (int c = 0; c < U.nch; ++c) {
+    int c = 0;   // chunks issued
+    for (; c < U.nch; ++c) {
         const int slot = c % kRaw;
         if (c >= kRaw && !mbar_wait(&S.raw_empty[slot], (unsigned)(((c / kRaw) - 1) & 1), err))
             break;
@@ -278,10 +296,12 @@ __device__ void loader(const RawMaps& TM, const Unit& U, Smem& S, int* err) {
             for (int half = 0; half < 2; ++half)
                 tma_load_3d(smem_u32(S.raw[slot].x[t][half]), maps[t], 64 * half, U.h, row, full);
     }
-    // do not let the CTA exit while copies it issued are still landing
-    const int first = U.nch > kRaw ? U.nch - kRaw : 0;
-    for (int c = first; c < U.nch; ++c)
-        if (!mbar_wait(&S.raw_full[c % kRaw], (unsigned)((c / kRaw) & 1), err)) break;
+    // Do not let the CTA exit while copies it issued are still landing.  Each slot has at
+    // most one copy in flight (the next one waits for raw_empty), so the last issues of
+    // the slots are the only phases that may be pending; also after a wait gave up.
+    const int first = c > kRaw ? c - kRaw : 0;
+    for (int i = first; i < c; ++i)
+        mbar_wait(&S.raw_full[i % kRaw], (unsigned)((i / kRaw) & 1), err, KDA_DRAIN_LIMIT);
 }
 
 // ---- token-parallel stage: producer warp w, channels 16w .. 16w+15 ----------------
@@ -721,17 +741,18 @@ __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
     const uint64_t d_xb = tc::smem_desc(smem_u32(S.st[0].x), 16, 1024, tc::kSwizzle128B);
     const uint64_t d_kdt = tc::smem_desc(smem_u32(S.st[0].kdt), 128, KD_SBO, tc::kSwizzleNone);
     const uint64_t d_aqk = tc::smem_desc(smem_u32(S.st[0].aqk), 128, AQ_SBO, tc::kSwizzleNone);
-    for (int c = 0; c < U.nch; ++c) {
+    int c = 0;
+    for (; c < U.nch; ++c) {
         const int slot = c % kRing;
         const uint64_t so = (uint64_t)((slot * sizeof(Stage)) >> 4);
         const uint32_t sc = tmem + TM_S + 128u * (c & 1);
         const uint32_t sn = tmem + TM_S + 128u * ((c + 1) & 1);
         const uint32_t uo = tmem + TM_UO + 32u * (c % 3);
-        if (!mbar_wait(&S.full[slot], (unsigned)((c / kRing) & 1), err)) return;
+        if (!mbar_wait(&S.full[slot], (unsigned)((c / kRing) & 1), err)) break;
         if (c == 0) {
-            if (!mbar_wait(&S.init_ready, 0u, err)) return;
+            if (!mbar_wait(&S.init_ready, 0u, err)) break;
         } else {
-            if (!mbar_wait(&S.s_done, (unsigned)((c - 1) & 1), err)) return;
+            if (!mbar_wait(&S.s_done, (unsigned)((c - 1) & 1), err)) break;
         }
         tc::fence_after_sync();
         // [O|U] = S^T [Q 2^G ; -w]^T over the 16 key-channel steps (the first one starts
@@ -746,7 +767,10 @@ __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
         // one wait for both the [O|U] MMAs and the epilogue's rescale: a wait costs
         // this thread ~100 cycles even on a completed barrier
         tc::commit(smem_u32(&S.scaled));
-        if (!mbar_wait(&S.scaled, (unsigned)(c & 1), err)) return;
+        if (!mbar_wait(&S.scaled, (unsigned)(c & 1), err)) {
+            // the [O|U] MMAs of this chunk were issued and committed: drain them below
+            break;
+        }
         tc::fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
@@ -756,12 +780,17 @@ __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
         tc::commit(smem_u32(&S.s_done));
         tc::commit(smem_u32(&S.empty[slot]));
     }
-    // Nobody else waits for the last kRing empty-slot commits.  Their arrivals must
-    // land before the CTA exits: a late one would hit the barrier that the next CTA
-    // on this SM initialises at the same shared-memory address.
-    const int first = U.nch > kRing ? U.nch - kRing : 0;
-    for (int c = first; c < U.nch; ++c)
-        if (!mbar_wait(&S.empty[c % kRing], (unsigned)((c / kRing) & 1), err)) return;
+    // Every MMA this thread issued completes before the CTA goes on to release tensor
+    // memory and exit, also after a wait gave up part-way through a chunk: one more
+    // commit, on a barrier of its own, tracks all of them.  Then the empty-slot commits
+    // of the last chunks, which nobody else waits for, must have arrived: a late arrival
+    // would hit the barrier that the next CTA on this SM initialises at the same
+    // shared-memory address.
+    tc::commit(smem_u32(&S.drain));
+    mbar_wait(&S.drain, 0u, err, KDA_DRAIN_LIMIT);
+    const int first = c > kRing ? c - kRing : 0;   // chunks 0 .. c - 1 were committed
+    for (int i = first; i < c; ++i)
+        mbar_wait(&S.empty[i % kRing], (unsigned)((i / kRing) & 1), err, KDA_DRAIN_LIMIT);
 }
 
 __device__ __forceinline__ float state_in(const Problem& P, size_t idx) {
@@ -930,6 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&S.init_ready, kEpiWarps * 32);
         mbar_init(&S.scaled, kEpiWarps * 32 + 1);   // epilogue threads + one commit
         mbar_init(&S.epi_done, kEpiWarps * 32);
+        mbar_init(&S.drain, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&S.a_ready[b], 32);              // the A_kk warp
         }
@@ -957,8 +987,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (role == kMma) {
         if (lane == 0) mma_issuer(U, S, tmem, err);
         __syncwarp();
-        // free tensor memory once the epilogue is done with it
-        const bool ok = mbar_wait(&S.epi_done, 0u, err);
+        // free tensor memory once the epilogue is done with it (after a timeout the
+        // epilogue stops at its next wait, so a longer limit than a pipeline wait's)
+        const bool ok = mbar_wait(&S.epi_done, 0u, err, KDA_DRAIN_LIMIT);
         __syncwarp();
         (void)ok;
         tc::fence_after_sync();
@@ -976,7 +1007,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-bool g_attr_set[64] = {};
+// per-device flag: the kernel attribute below is set once (setting it is idempotent,
+// so two threads racing on a first call both succeed)
+std::atomic<bool> g_attr_set[64];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -1012,11 +1045,11 @@ cudaError_t launch_fused(const Problem& P, const SeqMap& M, int* err, cudaStream
     const size_t smem = fused_smem_bytes();
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
+    if (dev >= 0 && dev < 64 && !g_attr_set[dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(fused_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        g_attr_set[dev] = true;
+        g_attr_set[dev].store(true, std::memory_order_release);
     }
     const long long ctas = (long long)P.N * P.H;
     if (ctas == 0) return cudaSuccess;

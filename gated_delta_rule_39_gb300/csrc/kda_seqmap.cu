@@ -3,6 +3,8 @@
 // the longest recurrences first; no host synchronisation.
 // Variable-length batching through cu_seqlens: "Moonshot AI Rilis FlashKDA"
 // (captivela.com), paragraph on cu_seqlens.
+#include <atomic>
+
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -68,18 +70,20 @@ __global__ void __launch_bounds__(kThreads) seqmap_kernel(Problem P, SeqMap M, i
     if (threadIdx.x == 0) *M.valid = 1;
 }
 
-bool g_attr_set[64] = {};
+// per-device flag: the kernel attribute below is set once (setting it is idempotent,
+// so two threads racing on a first call both succeed)
+std::atomic<bool> g_attr_set[64];
 
 }  // namespace
 
 cudaError_t launch_seqmap(const Problem& P, const SeqMap& M, int* err, cudaStream_t s) {
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
+    if (dev >= 0 && dev < 64 && !g_attr_set[dev].load(std::memory_order_acquire)) {
         const cudaError_t e = cudaFuncSetAttribute(seqmap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    (int)kSortSmem);
         if (e != cudaSuccess) return e;
-        g_attr_set[dev] = true;
+        g_attr_set[dev].store(true, std::memory_order_release);
     }
     // shared memory for the keys only when there is something to sort
     const size_t smem = P.N <= kSortMax ? kSortSmem : 0;

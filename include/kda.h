@@ -145,6 +145,11 @@ int kda_fwd_host(const void* q, const void* k, const void* v, const void* g,
  * per device, shared by every call on it whatever its stream: it keeps the
  * first error any kernel recorded since the last read, and a call still
  * running on another stream may set it after this read.
+ * KDA_ERR_DEVICE_TIMEOUT: a wait between the kernel's pipeline stages ran past
+ * its bound (KDA_SPIN_LIMIT SM cycles, about 2 s with the default build); the
+ * kernel then stops at its next wait, after its own asynchronous copies and
+ * tensor-core operations have completed, and returns.  out and final_state are
+ * then undefined for that call; the device and later calls are unaffected.
  */
 int kda_fwd_get_error(void* stream);
 
@@ -199,7 +204,8 @@ int kda_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
 
 /* ---- launch accounting (for measurement; off by default) ------------------
  *
- * kda_profile_enable(1) makes every later kda_fwd record a CUDA event before
+ * kda_profile_enable(1) makes every later kda_fwd and kda_fwd_noalloc call
+ * (and the kda_fwd calls that kda_fwd_host makes) record a CUDA event before
  * and after each of its kernel launches, on the launch stream; enable(0)
  * stops recording.  Enabling clears the totals.  kda_profile_read
  * synchronises on the recorded events and returns, per kernel id

@@ -1,0 +1,49 @@
+"""The bounded waits of the fused kernel, exercised without faulting anything.
+
+A variant of the library is built with a pipeline-wait bound of 64 SM cycles
+(-DKDA_SPIN_LIMIT=64), far below the time a TMA copy from HBM takes, so a wait
+runs out on the first chunk of every CTA.  The call must then report
+KDA_ERR_DEVICE_TIMEOUT through the device error word, having drained its own
+copies and tensor-core operations, and the GPU must stay usable: a normal call
+right after it matches the fp64 oracle.
+"""
+import ctypes
+
+import pytest
+
+import synth
+from gpu_harness import run_gpu, run_oracle, to_f64, upload
+from parity import out_error, state_error
+
+KDA_ERR_DEVICE_TIMEOUT = -7
+
+
+@pytest.mark.gpu
+def test_wait_that_runs_out_reports_timeout_and_the_gpu_stays_usable():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gated_delta_rule_39_gb300 as kda
+    from gated_delta_rule_39_gb300 import _build
+    kda.load_library()
+    path = _build.build(lib="libkda_spin64.so", extra_flags=["-DKDA_SPIN_LIMIT=64"])
+    short = kda.declare(ctypes.CDLL(path))
+    d = synth.make_inputs(1, 300, 2, seed=41, init_dtype="f32")
+    x = upload(d)
+    out = torch.full((1, 300, 2, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    fs = torch.full((1, 2, 128, 128), float("nan"), device="cuda")
+    stream = torch.cuda.current_stream()
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    rc = short.kda_fwd(p(x["q"]), p(x["k"]), p(x["v"]), p(x["g"]), p(x["beta"]),
+                       ctypes.c_float(d["scale"]), p(out), p(x["A_log"]), p(x["dt_bias"]),
+                       ctypes.c_float(d["lower_bound"]), p(x["initial_state"]), 1, p(fs), 1,
+                       None, 0, 1, 300, 2, 128, 128, ctypes.c_void_p(stream.cuda_stream))
+    assert rc == 0
+    assert short.kda_fwd_get_error(ctypes.c_void_p(stream.cuda_stream)) == KDA_ERR_DEVICE_TIMEOUT
+    # the word is cleared by the read, and the device answers normally afterwards
+    assert short.kda_fwd_get_error(ctypes.c_void_p(stream.cuda_stream)) == 0
+    o, s = run_gpu(d)
+    assert kda.kda_fwd_get_error() == 0
+    ro, rs = run_oracle(d)
+    assert out_error(to_f64(o), ro)["ok"]
+    assert state_error(to_f64(s), rs)["ok"]

@@ -122,3 +122,34 @@ def test_noalloc_rejects_too_many_sequences():
                              ctypes.c_void_p(0x20000), n, 1, 16, 1, 128, 128, None)
     assert rc == -14
     assert "KDA_NOALLOC_MAX_SEQS" in kda.kda_status_string(rc)
+
+
+@pytest.mark.gpu
+def test_noalloc_at_the_scratch_limit():
+    """Exactly KDA_NOALLOC_MAX_SEQS (65,536) sequences: the valid flag lands in the last
+    element of the fixed array and the sequence map takes its input-order path.  One
+    head, mostly empty sequences and a few non-empty ones; the result equals kda_fwd's
+    and no device error is raised."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gated_delta_rule_39_gb300 as kda
+    lib = kda.load_library()
+    stream = torch.cuda.current_stream()
+    n = 65536
+    lens = np.zeros(n, dtype=np.int64)
+    lens[[0, 1, 777, 40000, n - 1]] = [17, 3, 32, 5, 20]
+    d = synth.make_inputs(1, int(lens.sum()), 1, seed=36, lengths=list(lens), init_dtype=None)
+    x = upload(d)
+    T = int(lens.sum())
+    ref_out = torch.full((1, T, 1, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = torch.full_like(ref_out, float("nan"))
+    assert _call(lib.kda_fwd, d, x, ref_out, None, stream) == 0
+    assert _call(lib.kda_fwd_noalloc, d, x, out, None, stream) == 0
+    torch.cuda.synchronize()
+    assert kda.kda_fwd_get_error() == 0
+    assert torch.equal(out, ref_out)
+    from gpu_harness import run_oracle
+    ro, _ = run_oracle(d)
+    e = out_error(to_f64(out), ro)
+    assert e["ok"], e
