@@ -158,9 +158,10 @@ def source_digest(*names) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str):
+def ncu_traffic(kernel: str, workload: str | None = None):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if the kernel's
-    source has not changed since the capture; else None."""
+    source has not changed since the capture and (when given) the capture was taken on
+    `workload`; else None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
@@ -169,6 +170,8 @@ def ncu_traffic(kernel: str):
     if not rec:
         return None
     if rec.get("source_digest") != source_digest(*rec.get("sources", [])):
+        return None
+    if workload is not None and rec.get("workload_name") != workload:
         return None
     return rec.get("bytes_per_launch")
 
@@ -260,6 +263,46 @@ class Runner:
                         stream=self.stream)
 
 
+class DecodeRunner:
+    """One kda_decode step over N sequences x H heads, fp32 states updated in place."""
+
+    def __init__(self, d, device, stream):
+        import torch
+        import gated_delta_rule_39_gb300 as kda
+        self.kda = kda
+        self.d = d
+        self.stream = stream
+        N, T, H, _ = d["q"].shape
+        assert T == 1
+        self.B, self.T, self.H, self.N = N, 1, H, N
+        self.calls = 1
+
+        def bf16(bits, shape):
+            return (torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
+                    .view(torch.bfloat16).reshape(shape))
+
+        self.x = {n: bf16(d[n], (N, H, 128)) for n in ("q", "k", "v", "g")}
+        self.x["beta"] = bf16(d["beta"], (N, H))
+        self.A_log = torch.from_numpy(d["A_log"]).to(device)
+        self.dt_bias = torch.from_numpy(d["dt_bias"]).to(device)
+        self.state = torch.from_numpy(d["initial_state"]).to(device)
+        self.out = torch.empty((N, H, V), dtype=torch.bfloat16, device=device)
+
+    def step(self):
+        x, d = self.x, self.d
+        self.kda.kda_decode(x["q"], x["k"], x["v"], x["g"], x["beta"], d["scale"], self.out,
+                            self.A_log, self.dt_bias, d["lower_bound"], state_in=self.state,
+                            state_out=self.state, stream=self.stream)
+
+
+DECODE_WORKLOAD = "decode_n256_h96"
+
+
+def make_decode_inputs(seed):
+    import synth
+    return synth.make_inputs(256, 1, 96, seed=seed, init_dtype="f32")
+
+
 def timed_steps(runner, steps, warmup, pg=None, device=None, sampler=None):
     """Warm up, then time `steps` steps with CUDA events on the launch stream; returns
     (elapsed ms, {kernel: (total ms, launches)})."""
@@ -292,18 +335,22 @@ def timed_steps(runner, steps, warmup, pg=None, device=None, sampler=None):
     return elapsed_ms, prof
 
 
-def workload_line(name, d, elapsed_ms, prof, steps, world, calls):
+def workload_line(name, d, elapsed_ms, prof, steps, world, calls, decode=False):
     """Throughput and roofline of one workload from its timing."""
     hbm, tflops, src = peaks()
     B, T, H, _ = d["q"].shape
     bytes_, flop, th = algorithmic_work(d, calls)
+    if decode:   # the state is read and written in fp32 once per (sequence, head)
+        bytes_ = B * H * (BYTES_PER_TH + K * V * (4 + 4))
+        flop = B * H * 8 * K * V   # decay, S'^T k, update, S^T q: 4 multiply-adds per element
     tokens_per_step = B * T
     dom = max(prof, key=lambda n: prof[n][0])
     dom_ms = prof[dom][0] / max(1, prof[dom][1]) * calls   # one step's share of the kernel
     ms_per_step = elapsed_ms / steps
-    roof = roofline_of(dom, dom_ms, bytes_, flop, hbm, tflops, src) if dom == "fused_kernel" else None
+    roof = (roofline_of(dom, dom_ms, bytes_, flop, hbm, tflops, src)
+            if dom in ("fused_kernel", "decode_kernel") else None)
     if roof is not None:
-        roof["traffic"] = ncu_traffic(dom) if name == WORKLOAD else None
+        roof["traffic"] = ncu_traffic(dom, name)
     t_roof = max(bytes_ / (hbm * 1e9), flop / (tflops * 1e12))
     return {
         "workload": name, "value": world * tokens_per_step * steps / (elapsed_ms / 1e3),
@@ -329,23 +376,28 @@ def run_cuda(args, world, rank, local, pg):
     kda.load_library()
     stream = torch.cuda.current_stream(device)
     name = args.workload
-    if args.heads:
-        w = synth.WORKLOADS[name]
-        d = synth.make_inputs(w.B, w.T, args.heads, seed=rank, init_dtype=w.init_dtype)
+    decode = name == DECODE_WORKLOAD
+    if decode:
+        d = make_decode_inputs(rank)
+        runner = DecodeRunner(d, device, stream)
     else:
-        d = synth.make_workload(name, seed=rank)
-    runner = Runner(d, device, stream)
+        if args.heads:
+            w = synth.WORKLOADS[name]
+            d = synth.make_inputs(w.B, w.T, args.heads, seed=rank, init_dtype=w.init_dtype)
+        else:
+            d = synth.make_workload(name, seed=rank)
+        runner = Runner(d, device, stream)
     B, T, H, N = runner.B, runner.T, runner.H, runner.N
 
     # ---- timed region: K steps, launch timing on the launch stream -------------
     sampler = ClockSampler(local) if rank == 0 else None
     elapsed_ms, prof = timed_steps(runner, args.steps, args.warmup, pg, device, sampler)
     elapsed_ms = max_over_ranks(pg, elapsed_ms, device)
-    main = workload_line(name, d, elapsed_ms, prof, args.steps, world, runner.calls)
+    main = workload_line(name, d, elapsed_ms, prof, args.steps, world, runner.calls, decode)
 
     # ---- end-to-end through the host-buffer entry point ---------------------------
     e2e = None
-    if not args.no_e2e and runner.calls == 1:
+    if not args.no_e2e and runner.calls == 1 and not decode:
         hx = {n: torch.from_numpy(np.ascontiguousarray(d[n]).view(np.int16)).view(torch.bfloat16)
               .pin_memory() for n in ("q", "k", "v", "g", "beta")}
         s0 = d.get("initial_state")
@@ -405,6 +457,20 @@ def run_cuda(args, world, rank, local, pg):
             others[other] = rec
             del orun
             torch.cuda.empty_cache()
+        # one decode step over a serving-sized batch (states in HBM, updated in place)
+        dd = make_decode_inputs(rank)
+        drun = DecodeRunner(dd, device, stream)
+        ems, dprof = timed_steps(drun, args.steps, 3, pg, device)
+        ems = max_over_ranks(pg, ems, device)
+        rec = workload_line(DECODE_WORKLOAD, dd, ems, dprof, args.steps, world, 1, decode=True)
+        rec["steps"], rec["warmup"] = args.steps, 3
+        rec["config"] = {"N": 256, "H": 96, "K": K, "V": V, "state": "f32 in place",
+                         "entry_point": "kda_decode"}
+        if world == 1 and not args.no_cpu_baseline:
+            rec["cpu_baseline"] = cpu_baseline(dd, DECODE_WORKLOAD, target_s=args.cpu_seconds / 8)
+        others[DECODE_WORKLOAD] = rec
+        del drun
+        torch.cuda.empty_cache()
 
     if rank == 0:
         if args.heads:
@@ -458,10 +524,11 @@ def cpu_baseline(d, workload: str = WORKLOAD, target_s: float = 12.0):
         t = run(list(range(n_heads)))
     else:
         n_heads, t = probe, t_probe
-    tokens_equiv = T * n_heads / H
+    tokens_equiv = d["q"].shape[0] * T * n_heads / H
     return {"value": tokens_equiv / t, "unit": "tokens/s", "cores": min(threads, n_heads),
             "kind": "oracle",
-            "sample": f"{n_heads} of {H} heads x {T} tokens of {workload}; tokens/s counts "
+            "sample": f"{n_heads} of {H} heads x {d['q'].shape[0] * T} tokens of {workload}; "
+                      f"tokens/s counts "
                       f"a token as all {H} heads ({t:.1f} s)"}
 
 

@@ -13,7 +13,8 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["KdaError", "kda_fwd", "kda_fwd_host", "kda_fwd_noalloc", "kda_fwd_get_error", "kda_status_string",
+__all__ = ["KdaError", "kda_fwd", "kda_fwd_host", "kda_fwd_noalloc", "kda_decode",
+           "kda_fwd_get_error", "kda_status_string",
            "kda_last_cuda_error",
            "kda_fwd_workspace_bytes", "kda_profile_enable", "kda_profile_read",
            "kda_kernel_name", "lib_path", "load_library", "KDA_BF16", "KDA_F32",
@@ -24,8 +25,8 @@ _LIB_PATH = os.path.join(_HERE, "_lib", "libkda.so")
 
 KDA_BF16 = 0
 KDA_F32 = 1
-KDA_NUM_KERNELS = 2
-KERNEL_NAMES = ("seqmap_kernel", "fused_kernel")
+KDA_NUM_KERNELS = 3
+KERNEL_NAMES = ("seqmap_kernel", "fused_kernel", "decode_kernel")
 
 _lib = None
 _vp = ctypes.c_void_p
@@ -70,6 +71,10 @@ def declare(lib):
     lib.kda_fwd_host.restype = ctypes.c_int
     lib.kda_fwd_noalloc.argtypes = fwd_args
     lib.kda_fwd_noalloc.restype = ctypes.c_int
+    lib.kda_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp,
+                               ctypes.c_float, _vp, ctypes.c_int, _vp, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp]
+    lib.kda_decode.restype = ctypes.c_int
     lib.kda_fwd_get_error.argtypes = [_vp]
     lib.kda_fwd_get_error.restype = ctypes.c_int
     lib.kda_last_cuda_error.argtypes = []
@@ -186,6 +191,46 @@ def kda_fwd(q, k, v, g, beta, scale: float, out, A_log, dt_bias, lower_bound: fl
             _ptr(cu_seqlens), N if cu_seqlens is not None else 0, B, T, H, K, V, s)
     if rc != 0:
         raise KdaError(rc)
+
+
+def kda_decode(q, k, v, g, beta, scale: float, out, A_log, dt_bias, lower_bound: float,
+               state_in=None, state_out=None, stream=None) -> None:
+    """One decode step on CUDA tensors (asynchronous on ``stream``): a single token per
+    sequence applied to the states.
+
+    q, k, g: bf16 [N, H, 128]; v, out: bf16 [N, H, 128]; beta: bf16 [N, H] (logits);
+    A_log: fp32 [H]; dt_bias: fp32 [H, 128]; state_in / state_out: optional bf16 or
+    fp32 [N, H, 128, 128] (the same tensor updates the states in place).
+    Raises KdaError on a rejected call.
+    """
+    import torch
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("kda_decode takes CUDA tensors")
+    N, H, K = q.shape
+    V = v.shape[-1]
+    for name, t in (("q", q), ("k", k), ("g", g)):
+        _check(t, name, torch.bfloat16, (N, H, K), dev)
+    _check(v, "v", torch.bfloat16, (N, H, V), dev)
+    _check(out, "out", torch.bfloat16, (N, H, V), dev)
+    _check(beta, "beta", torch.bfloat16, (N, H), dev)
+    _check(A_log, "A_log", torch.float32, (H,), dev)
+    _check(dt_bias, "dt_bias", torch.float32, (H, K), dev)
+    for name, t in (("state_in", state_in), ("state_out", state_out)):
+        if t is not None:
+            if t.dtype not in (torch.bfloat16, torch.float32):
+                raise TypeError(f"{name} must be bfloat16 or float32")
+            _check(t, name, t.dtype, (N, H, K, V), dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    s = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    with torch.cuda.device(dev):
+        rc = load_library().kda_decode(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
+            _ptr(A_log), _ptr(dt_bias), float(lower_bound), _ptr(state_in),
+            _state_dtype(state_in), _ptr(state_out), _state_dtype(state_out), N, H, K, V, s)
+    if rc != 0:
+        raise KdaError(rc, "kda_decode")
 
 
 def kda_fwd_noalloc(q, k, v, g, beta, scale: float, out, A_log, dt_bias, lower_bound: float,

@@ -170,6 +170,36 @@ int validate(const void* q, const void* k, const void* v, const void* g, const v
     return KDA_OK;
 }
 
+// Host-side checks of kda_decode; no CUDA call.
+int validate_decode(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                    float scale, const void* out, const float* A_log, const float* dt_bias,
+                    float lower_bound, const void* s0, int s0_dtype, const void* s1, int s1_dtype,
+                    int N, int H, int K, int V) {
+    if (K != kDim || V != kDim) return KDA_ERR_UNSUPPORTED_DIM;
+    if (N < 0 || H < 1) return KDA_ERR_SHAPE;
+    if ((long long)N * H >= (1LL << 31) || (long long)N * H * kDim * kDim >= (1LL << 40))
+        return KDA_ERR_SHAPE;
+    if (N > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL;
+    if (!A_log || !dt_bias) return KDA_ERR_NULL;
+    if (s0 && s0_dtype != KDA_BF16 && s0_dtype != KDA_F32) return KDA_ERR_DTYPE;
+    if (s1 && s1_dtype != KDA_BF16 && s1_dtype != KDA_F32) return KDA_ERR_DTYPE;
+    if (!std::isfinite(scale)) return KDA_ERR_ARG;
+    if (!(lower_bound >= kLowerBoundMin && lower_bound <= 0.0f)) return KDA_ERR_ARG;
+    for (const void* p : {q, k, v, g, static_cast<const void*>(out), s0, static_cast<const void*>(s1)})
+        if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return KDA_ERR_ALIGN;
+    const size_t n_row = (size_t)N * H * kDim * 2, n_b = (size_t)N * H * 2;
+    for (const void* p : {q, k, v, g})
+        if (overlaps(out, n_row, p, n_row)) return KDA_ERR_ALIAS;
+    if (overlaps(out, n_row, beta, n_b)) return KDA_ERR_ALIAS;
+    const size_t ns = (size_t)N * H * kDim * kDim;
+    if (s0 && s1) {
+        const size_t b0 = ns * (s0_dtype == KDA_F32 ? 4 : 2), b1 = ns * (s1_dtype == KDA_F32 ? 4 : 2);
+        if (overlaps(s0, b0, s1, b1) && (s0 != s1 || s0_dtype != s1_dtype)) return KDA_ERR_ALIAS;
+    }
+    if (s1 && overlaps(out, n_row, s1, ns * (s1_dtype == KDA_F32 ? 4 : 2))) return KDA_ERR_ALIAS;
+    return KDA_OK;
+}
+
 }  // namespace
 }  // namespace kda
 
@@ -556,6 +586,42 @@ int kda_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
     return KDA_OK;
 }
 
+int kda_decode(const void* q, const void* k, const void* v, const void* g, const void* beta,
+               float scale, void* out, const float* A_log, const float* dt_bias, float lower_bound,
+               const void* state_in, int state_in_dtype, void* state_out, int state_out_dtype,
+               int N, int H, int K, int V, void* stream) {
+    int rc = validate_decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, state_in,
+                             state_in_dtype, state_out, state_out_dtype, N, H, K, V);
+    if (rc != KDA_OK) return rc;
+    int dev = 0;
+    int* err = nullptr;
+    rc = device_setup(&dev, &err);
+    if (rc != KDA_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Problem P{};
+    P.q = static_cast<const __nv_bfloat16*>(q);
+    P.k = static_cast<const __nv_bfloat16*>(k);
+    P.v = static_cast<const __nv_bfloat16*>(v);
+    P.g = static_cast<const __nv_bfloat16*>(g);
+    P.beta = static_cast<const __nv_bfloat16*>(beta);
+    P.out = static_cast<__nv_bfloat16*>(out);
+    P.A_log = A_log;
+    P.dt_bias = dt_bias;
+    P.scale = scale;
+    P.lower_bound = lower_bound;
+    P.init_state = state_in;
+    P.init_dtype = state_in_dtype;
+    P.final_state = state_out;
+    P.final_dtype = state_out_dtype;
+    P.cu_seqlens = nullptr;
+    P.N = N;
+    P.T = 1;
+    P.H = H;
+    const cudaError_t e = timed_launch(KDA_KERNEL_DECODE, s, [&] { return launch_decode(P, s); });
+    if (e != cudaSuccess) return cuda_fail(KDA_ERR_LAUNCH, e);
+    return KDA_OK;
+}
+
 int kda_profile_enable(int on) {
     std::lock_guard<std::mutex> lk(g_prof.mu);
     if (on) {
@@ -604,6 +670,7 @@ const char* kda_kernel_name(int kernel_id) {
     switch (kernel_id) {
         case KDA_KERNEL_SEQMAP: return "seqmap_kernel";
         case KDA_KERNEL_FUSED: return "fused_kernel";
+        case KDA_KERNEL_DECODE: return "decode_kernel";
         default: return "unknown";
     }
 }

@@ -134,6 +134,7 @@ __device__ __forceinline__ void cp_async_wait() {
 // Host-side launchers (defined in the kernel translation units).
 cudaError_t launch_seqmap(const Problem& P, const SeqMap& M, int* err, cudaStream_t s);
 cudaError_t launch_fused(const Problem& P, const SeqMap& M, int* err, cudaStream_t s);
+cudaError_t launch_decode(const Problem& P, cudaStream_t s);
 size_t fused_smem_bytes();
 
 }  // namespace kda

@@ -202,17 +202,45 @@ int kda_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
                     const int32_t* cu_seqlens, int num_seqs, int B, int T, int H, int K, int V,
                     void* stream);
 
+/*
+ * kda_decode -- one decode step: a single new token for each of N sequences,
+ * applied to their states (the incremental decoding that the final state of a
+ * prefill feeds: "FlashKDA" (productcool.com), "Main Features").  The result
+ * equals kda_fwd on B = N sequences of T = 1 token with these states; per
+ * (n, h) it reads the state once and writes it once, so its cost is the state
+ * traffic (128 KB per (n, h) with fp32 states in and out).
+ *
+ *   q, k, g     bf16 [N, H, K]   (one token per sequence; [N, 1, H, K] in kda_fwd's layout)
+ *   v, out      bf16 [N, H, V]
+ *   beta        bf16 [N, H]      logits; sigmoid is applied inside
+ *   scale, A_log, dt_bias, lower_bound   as for kda_fwd (same gate, same ranges)
+ *   state_in    NULL (zero state) or [N, H, K, V] of state_in_dtype
+ *   state_out   NULL (not written) or [N, H, K, V] of state_out_dtype; the
+ *               usual call passes the same buffer as state_in (same dtype) to
+ *               update the states in place
+ *   N >= 0, H >= 1, N*H < 2^31; K = V = 128
+ *
+ * Device pointers, owned by the caller; q, k, v, g, out and both states must be
+ * 16-byte aligned; out must not overlap an input or state_out, and state_in and
+ * state_out must be the same buffer or disjoint.  Asynchronous on `stream`; no
+ * scratch memory; argument errors as for kda_fwd (nothing is launched).
+ */
+int kda_decode(const void* q, const void* k, const void* v, const void* g, const void* beta,
+               float scale, void* out, const float* A_log, const float* dt_bias,
+               float lower_bound, const void* state_in, int state_in_dtype, void* state_out,
+               int state_out_dtype, int N, int H, int K, int V, void* stream);
+
 /* ---- launch accounting (for measurement; off by default) ------------------
  *
- * kda_profile_enable(1) makes every later kda_fwd and kda_fwd_noalloc call
- * (and the kda_fwd calls that kda_fwd_host makes) record a CUDA event before
- * and after each of its kernel launches, on the launch stream; enable(0)
+ * kda_profile_enable(1) makes every later kda_fwd, kda_fwd_noalloc and
+ * kda_decode call (and the kda_fwd calls that kda_fwd_host makes) record a CUDA
+ * event before and after each of its kernel launches, on the launch stream; enable(0)
  * stops recording.  Enabling clears the totals.  kda_profile_read
  * synchronises on the recorded events and returns, per kernel id
  * (KDA_KERNEL_*), the summed device time in milliseconds and the number of
  * launches since the last enable.  Arrays must hold KDA_NUM_KERNELS entries.
  * Returns KDA_OK, or KDA_ERR_CUDA. */
-enum { KDA_KERNEL_SEQMAP = 0, KDA_KERNEL_FUSED = 1, KDA_NUM_KERNELS = 2 };
+enum { KDA_KERNEL_SEQMAP = 0, KDA_KERNEL_FUSED = 1, KDA_KERNEL_DECODE = 2, KDA_NUM_KERNELS = 3 };
 int kda_profile_enable(int on);
 int kda_profile_read(double* total_ms, long long* launches);
 const char* kda_kernel_name(int kernel_id);

@@ -47,6 +47,9 @@ def test_traffic_record_follows_the_kernel_source(monkeypatch):
     assert bench.ncu_traffic("fused_kernel") == (rec["bytes_per_launch"] if current else None)
     monkeypatch.setattr(bench, "source_digest", lambda *names: rec["source_digest"])
     assert bench.ncu_traffic("fused_kernel") == rec["bytes_per_launch"]
+    # a record taken on one workload is not reported for another
+    assert bench.ncu_traffic("fused_kernel", rec["workload_name"]) == rec["bytes_per_launch"]
+    assert bench.ncu_traffic("fused_kernel", "another_workload") is None
     # any change to the kernel's source voids it
     monkeypatch.setattr(bench, "source_digest", lambda *names: "0" * 16)
     assert bench.ncu_traffic("fused_kernel") is None
