@@ -12,11 +12,19 @@ namespace kda {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kSortMax = 16384;   // above this many sequences the input order is kept
+constexpr int kWarps = kThreads / 32;
+constexpr int kSortMax = 16384;   // up to this many sequences: exact longest-first order
 constexpr size_t kSortSmem = sizeof(unsigned long long) * kSortMax;   // 128 KB
+constexpr int kBuckets = 32;      // above it: order by floor(log2(length + 1)), descending
 
-// The order is a bitonic sort of the keys (max - length) << 32 | index in shared
-// memory: longest first, ties in input order (a stable order without a stable sort).
+// Up to kSortMax sequences the order is a bitonic sort of the keys
+// (max - length) << 32 | index in shared memory: longest first, ties in input order
+// (a stable order without a stable sort).  Above it, a stable counting sort by the
+// length's binary order of magnitude (longest bucket first, input order inside a
+// bucket): warp w owns a contiguous segment of the sequences, counts its buckets,
+// a scan over (bucket descending, warp) gives each warp's first slot per bucket, and
+// each warp places its segment in input order.  Both orders only decide which
+// (sequence, head) units start first; every unit's result is independent of them.
 __global__ void __launch_bounds__(kThreads) seqmap_kernel(Problem P, SeqMap M, int* err) {
     extern __shared__ unsigned long long keys[];
     __shared__ int bad;
@@ -35,7 +43,65 @@ __global__ void __launch_bounds__(kThreads) seqmap_kernel(Problem P, SeqMap M, i
         return;
     }
     if (N > kSortMax) {
-        for (int n = threadIdx.x; n < N; n += kThreads) M.seq_order[n] = n;
+        int* cnt = reinterpret_cast<int*>(keys);   // [kWarps][kBuckets] counts, then first slots
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int per = (N + kWarps - 1) / kWarps;
+        const int n0 = min(N, w * per), n1 = min(N, n0 + per);
+        const auto bucket = [&](int n) {   // floor(log2(length + 1)), 0 .. 31
+            return 31 - __clz((unsigned)(cu[n + 1] - cu[n]) + 1u);
+        };
+        if (lane < kBuckets) cnt[w * kBuckets + lane] = 0;
+        __syncwarp();
+        for (int base = n0; base < n1; base += 32) {
+            const int n = base + lane;
+            const bool in = n < n1;
+            const int b = in ? bucket(n) : -1 - lane;   // distinct dummies outside the segment
+            const unsigned same = __match_any_sync(0xffffffffu, b);
+            if (in && lane == __ffs(same) - 1) cnt[w * kBuckets + b] += __popc(same);
+            __syncwarp();
+        }
+        __syncthreads();
+        // exclusive scan in the order (bucket descending, warp ascending): thread
+        // i = (kBuckets - 1 - b) * kWarps + w holds the count of (w, b)
+        {
+            const int i = threadIdx.x;
+            const int b = kBuckets - 1 - i / kWarps, ww = i % kWarps;
+            const int c = cnt[ww * kBuckets + b];
+            int x = c;   // inclusive scan within the warp, then over warps
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, d);
+                if (lane >= d) x += y;
+            }
+            __shared__ int warp_tot[kWarps];
+            if (lane == 31) warp_tot[w] = x;
+            __syncthreads();
+            if (w == 0) {
+                int t = warp_tot[lane];
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, t, d);
+                    if (lane >= d) t += y;
+                }
+                warp_tot[lane] = t - warp_tot[lane];   // exclusive
+            }
+            __syncthreads();
+            cnt[ww * kBuckets + b] = warp_tot[w] + x - c;   // first slot of (ww, b)
+        }
+        __syncthreads();
+        for (int base = n0; base < n1; base += 32) {
+            const int n = base + lane;
+            const bool in = n < n1;
+            const int b = in ? bucket(n) : -1 - lane;
+            const unsigned same = __match_any_sync(0xffffffffu, b);
+            if (in) {
+                const int rank = __popc(same & ((1u << lane) - 1u));
+                M.seq_order[cnt[w * kBuckets + b] + rank] = n;
+            }
+            __syncwarp();
+            if (in && lane == __ffs(same) - 1) cnt[w * kBuckets + b] += __popc(same);
+            __syncwarp();
+        }
     } else {
         int n2 = 1;   // sorted length: a power of two, padded with keys that sort last
         while (n2 < N) n2 <<= 1;
@@ -85,8 +151,8 @@ cudaError_t launch_seqmap(const Problem& P, const SeqMap& M, int* err, cudaStrea
         if (e != cudaSuccess) return e;
         g_attr_set[dev].store(true, std::memory_order_release);
     }
-    // shared memory for the keys only when there is something to sort
-    const size_t smem = P.N <= kSortMax ? kSortSmem : 0;
+    // shared memory for the keys, or for the bucket counts of the counting sort
+    const size_t smem = P.N <= kSortMax ? kSortSmem : sizeof(int) * kWarps * kBuckets;
     seqmap_kernel<<<1, kThreads, smem, s>>>(P, M, err);
     return cudaGetLastError();
 }

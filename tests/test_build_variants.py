@@ -1,4 +1,5 @@
-"""The bounded waits of the fused kernel, exercised without faulting anything.
+"""Build variants of the fused kernel: the bounded waits, exercised without faulting
+anything, and the tf32 operand rounding.
 
 A variant of the library is built with a pipeline-wait bound of 64 SM cycles
 (-DKDA_SPIN_LIMIT=64), far below the time a TMA copy from HBM takes, so a wait
@@ -47,3 +48,36 @@ def test_wait_that_runs_out_reports_timeout_and_the_gpu_stays_usable():
     ro, rs = run_oracle(d)
     assert out_error(to_f64(o), ro)["ok"]
     assert state_error(to_f64(s), rs)["ok"]
+
+
+@pytest.mark.gpu
+def test_tf32_rounding_by_addition_equals_the_conversion():
+    """The kernel rounds tf32 operands by adding half an ulp to the fp32 bits and lets
+    the tensor core drop the low 13 bits.  A build that rounds with cvt.rna.tf32.f32
+    instead (-DKDA_TF32_CVT) gives bit-identical outputs and states on a multi-chunk
+    varlen call with both state dtypes."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gated_delta_rule_39_gb300 as kda
+    from gated_delta_rule_39_gb300 import _build
+    lib = kda.load_library()
+    cvt = kda.declare(ctypes.CDLL(_build.build(lib="libkda_tf32cvt.so",
+                                               extra_flags=["-DKDA_TF32_CVT"])))
+    lens = [300, 17, 0, 529, 64]
+    d = synth.make_inputs(1, sum(lens), 4, seed=42, lengths=lens, init_dtype="bf16")
+    x = upload(d)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    res = []
+    for lib_ in (lib, cvt):
+        out = torch.full((1, sum(lens), 4, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        fs = torch.full((5, 4, 128, 128), float("nan"), device="cuda")
+        rc = lib_.kda_fwd(p(x["q"]), p(x["k"]), p(x["v"]), p(x["g"]), p(x["beta"]),
+                          ctypes.c_float(d["scale"]), p(out), p(x["A_log"]), p(x["dt_bias"]),
+                          ctypes.c_float(d["lower_bound"]), p(x["initial_state"]), 0, p(fs), 1,
+                          p(x["cu_seqlens"]), 5, 1, sum(lens), 4, 128, 128, None)
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert lib_.kda_fwd_get_error(None) == 0
+        res.append((out, fs))
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
