@@ -65,50 +65,6 @@ def test_noalloc_matches_kda_fwd_on_consecutive_calls():
         assert torch.equal(out, ref_out) and torch.equal(fs, ref_fs)
 
 
-@pytest.mark.gpu
-@pytest.mark.parametrize("entry", ["kda_fwd_noalloc", "kda_fwd"])
-def test_call_captured_in_a_cuda_graph(entry):
-    """A varlen call (sequence map + fused kernel) captured once into a CUDA graph and
-    replayed after new values are written into the captured buffers gives what a
-    direct kda_fwd call on those values gives, bit for bit.  kda_fwd's scratch becomes
-    an allocation node of the graph; kda_fwd_noalloc needs none."""
-    torch = pytest.importorskip("torch")
-    if not torch.cuda.is_available():
-        pytest.skip("no CUDA device")
-    import gated_delta_rule_39_gb300 as kda
-    lib = kda.load_library()
-    fn = getattr(lib, entry)
-    lens = [100, 7, 0, 176, 17]
-    d1 = synth.make_inputs(1, sum(lens), 3, seed=34, lengths=lens, init_dtype="f32")
-    d2 = synth.make_inputs(1, sum(lens), 3, seed=35, lengths=lens, init_dtype="f32")
-    x = upload(d1)
-    H, N = 3, d1["N"]
-    out = torch.empty((1, sum(lens), H, 128), dtype=torch.bfloat16, device="cuda")
-    fs = torch.empty((N, H, 128, 128), device="cuda")
-    # the first call (outside any capture) sets the kernels' attributes and, for
-    # kda_fwd_noalloc, looks up its scratch array
-    assert _call(fn, d1, x, out, fs, torch.cuda.current_stream()) == 0
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        rc = _call(fn, d1, x, out, fs, torch.cuda.current_stream())
-    assert rc == 0
-    x2 = upload(d2)
-    for name in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state", "cu_seqlens"):
-        x[name].copy_(x2[name])
-    out.fill_(float("nan"))
-    fs.fill_(float("nan"))
-    graph.replay()
-    torch.cuda.synchronize()
-    assert kda.kda_fwd_get_error() == 0
-    ref_out = torch.full_like(out, float("nan"))
-    ref_fs = torch.full_like(fs, float("nan"))
-    assert _call(lib.kda_fwd, d2, x2, ref_out, ref_fs, torch.cuda.current_stream()) == 0
-    torch.cuda.synchronize()
-    assert torch.equal(out, ref_out) and torch.equal(fs, ref_fs)
-    del graph
-
-
 def test_noalloc_rejects_too_many_sequences():
     """More sequences than the fixed scratch holds: a clear error, nothing launched."""
     import gated_delta_rule_39_gb300 as kda
