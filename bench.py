@@ -345,7 +345,8 @@ def workload_line(name, d, elapsed_ms, prof, steps, world, calls, decode=False):
         flop = B * H * 8 * K * V   # decay, S'^T k, update, S^T q: 4 multiply-adds per element
     tokens_per_step = B * T
     dom = max(prof, key=lambda n: prof[n][0])
-    dom_ms = prof[dom][0] / max(1, prof[dom][1]) * calls   # one step's share of the kernel
+    # the dominant kernel's device time per step (a split call launches it twice)
+    dom_ms = prof[dom][0] / steps
     ms_per_step = elapsed_ms / steps
     roof = (roofline_of(dom, dom_ms, bytes_, flop, hbm, tflops, src)
             if dom in ("fused_kernel", "decode_kernel") else None)

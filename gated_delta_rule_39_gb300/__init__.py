@@ -13,7 +13,8 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["KdaError", "kda_fwd", "kda_fwd_host", "kda_fwd_noalloc", "kda_decode",
+__all__ = ["KdaError", "kda_fwd", "kda_fwd_segments", "kda_fwd_host", "kda_fwd_noalloc",
+           "kda_decode",
            "kda_fwd_get_error", "kda_status_string",
            "kda_last_cuda_error",
            "kda_fwd_workspace_bytes", "kda_profile_enable", "kda_profile_read",
@@ -25,8 +26,8 @@ _LIB_PATH = os.path.join(_HERE, "_lib", "libkda.so")
 
 KDA_BF16 = 0
 KDA_F32 = 1
-KDA_NUM_KERNELS = 3
-KERNEL_NAMES = ("seqmap_kernel", "fused_kernel", "decode_kernel")
+KDA_NUM_KERNELS = 4
+KERNEL_NAMES = ("seqmap_kernel", "fused_kernel", "decode_kernel", "combine_kernel")
 
 _lib = None
 _vp = ctypes.c_void_p
@@ -71,6 +72,8 @@ def declare(lib):
     lib.kda_fwd_host.restype = ctypes.c_int
     lib.kda_fwd_noalloc.argtypes = fwd_args
     lib.kda_fwd_noalloc.restype = ctypes.c_int
+    lib.kda_fwd_segments.argtypes = fwd_args[:-1] + [ctypes.c_int, _vp]
+    lib.kda_fwd_segments.restype = ctypes.c_int
     lib.kda_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp,
                                ctypes.c_float, _vp, ctypes.c_int, _vp, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp]
@@ -172,25 +175,45 @@ def kda_fwd(q, k, v, g, beta, scale: float, out, A_log, dt_bias, lower_bound: fl
     q, k, g: bf16 [B, T, H, 128]; v, out: bf16 [B, T, H, 128]; beta: bf16 [B, T, H] (logits);
     A_log: fp32 [H]; dt_bias: fp32 [H, 128]; initial_state / final_state: optional
     bf16 or fp32 [N, H, 128, 128]; cu_seqlens: optional int32 [N + 1] (then B == 1).
+    Long fixed-length calls with few (sequence, head) recurrences are split into
+    segments automatically (``kda_fwd_segments`` with ``num_segments=0``).
     Raises KdaError on a rejected call.
     """
+    _fwd_call("kda_fwd", None, q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+              initial_state, final_state, cu_seqlens, stream)
+
+
+def kda_fwd_segments(q, k, v, g, beta, scale: float, out, A_log, dt_bias, lower_bound: float,
+                     initial_state=None, final_state=None, cu_seqlens=None, stream=None,
+                     num_segments: int = 0) -> None:
+    """``kda_fwd`` with the sequence split chosen by the caller: ``num_segments`` 0 picks
+    it (as kda_fwd), 1 runs one pass, s >= 2 cuts every sequence of a fixed-length call
+    into s segments that run side by side (two windows and a combine step)."""
+    _fwd_call("kda_fwd_segments", int(num_segments), q, k, v, g, beta, scale, out, A_log,
+              dt_bias, lower_bound, initial_state, final_state, cu_seqlens, stream)
+
+
+def _fwd_call(name, segments, q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+              initial_state, final_state, cu_seqlens, stream):
     import torch
     dev = q.device
     if dev.type != "cuda":
-        raise ValueError("kda_fwd takes CUDA tensors; use kda_fwd_host for host buffers")
+        raise ValueError(f"{name} takes CUDA tensors; use kda_fwd_host for host buffers")
     B, T, H, K, V, N = _marshal(q, k, v, g, beta, out, A_log, dt_bias, initial_state,
                                 final_state, cu_seqlens, dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     s = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
-    with torch.cuda.device(dev):
-        rc = load_library().kda_fwd(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
             _ptr(A_log), _ptr(dt_bias), float(lower_bound), _ptr(initial_state),
             _state_dtype(initial_state), _ptr(final_state), _state_dtype(final_state),
-            _ptr(cu_seqlens), N if cu_seqlens is not None else 0, B, T, H, K, V, s)
+            _ptr(cu_seqlens), N if cu_seqlens is not None else 0, B, T, H, K, V]
+    if segments is not None:
+        args.append(segments)
+    with torch.cuda.device(dev):
+        rc = getattr(load_library(), name)(*args, s)
     if rc != 0:
-        raise KdaError(rc)
+        raise KdaError(rc, name)
 
 
 def kda_decode(q, k, v, g, beta, scale: float, out, A_log, dt_bias, lower_bound: float,

@@ -1,5 +1,6 @@
 // Host side of the C ABI declared in include/kda.h: argument validation,
 // stream-ordered scratch memory, kernel launches, error word, launch timing.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -34,12 +35,13 @@ constexpr float kLowerBoundMin = -5.4f;
 struct DeviceInfo {
     bool ready = false;
     bool arch_ok = false;
+    int sms = 0;   // streaming multiprocessors
     int* err = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-int device_setup(int* dev_out, int** err_out) {
+int device_setup(int* dev_out, int** err_out, int* sms_out = nullptr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(KDA_ERR_CUDA, e);
@@ -52,6 +54,8 @@ int device_setup(int* dev_out, int** err_out) {
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
         if (e != cudaSuccess) return cuda_fail(KDA_ERR_CUDA, e);
         d.arch_ok = (major == 10 && minor == 3);
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(KDA_ERR_CUDA, e);
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_error_word);
         if (e != cudaSuccess) return cuda_fail(KDA_ERR_CUDA, e);
@@ -67,6 +71,7 @@ int device_setup(int* dev_out, int** err_out) {
     }
     *dev_out = dev;
     *err_out = d.err;
+    if (sms_out) *sms_out = d.sms;
     return d.arch_ok ? KDA_OK : KDA_ERR_ARCH;
 }
 
@@ -122,9 +127,36 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Scratch of one call: the varlen sequence map (longest-first order + valid
-// flag); fixed-length calls need none.
+// flag); fixed-length calls need none unless they are split into segments.
 size_t scratch_bytes(int N, bool varlen) {
     return varlen ? align_up(sizeof(int) * ((size_t)N + 1)) : 0;
+}
+
+// ---- sequence split (kda_split.cu) -----------------------------------------------
+// Shortest segment the automatic split makes: 64 chunks, so that the two launches,
+// the combine step and each CTA's pipeline fill stay small against a segment's time.
+constexpr int kSplitMinTokens = 1024;
+
+// Segments for a fixed-length call: `requested` 0 picks them (the largest s whose
+// window-0 units, (2s - 3) B H, fit on the device's SMs in one wave, with at least
+// kSplitMinTokens per segment; 1 when that gives fewer than 3), 1 is one pass, s >= 2
+// is s segments of whole chunks, at most one per chunk.  Returns 0 if `requested`
+// cannot be met.
+int plan_segments(int B, int T, int H, int requested, int sms) {
+    if (requested == 1) return 1;
+    if (requested >= 2) return requested <= (T + kChunk - 1) / kChunk ? requested : 0;
+    const double units = (double)B * H;
+    if (sms <= 0 || T < 1 || units <= 0) return 1;
+    int s = (int)(((double)sms / units + 3.0) / 2.0);
+    s = std::min(s, T / kSplitMinTokens);
+    return s >= 3 ? s : 1;
+}
+
+// window-0 end states and window-1 initial states of a split call (fp32)
+size_t split_bytes(int N, int H, int s) {
+    if (s < 2) return 0;
+    const size_t st = (size_t)kDim * kDim * sizeof(float) * N * H;
+    return align_up(st * (2 * s - 3)) + align_up(st * (s - 1));
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -317,14 +349,16 @@ int host_fwd_blocks(const void* q, const void* k, const void* v, const void* g, 
         const bool first = b == 0, last = b == nblk - 1;
         e = cudaStreamWaitEvent(s, ev[b], 0);
         if (e != cudaSuccess) break;
-        rc = kda_fwd(d + offs[0] + t0 * row, d + offs[1] + t0 * row, d + offs[2] + t0 * row,
-                     d + offs[3] + t0 * row, d + offs[4] + t0 * brow, scale, d + offs[5] + t0 * row,
-                     reinterpret_cast<const float*>(d + offs[6]),
-                     reinterpret_cast<const float*>(d + offs[7]), lower_bound,
-                     first ? (initial_state ? static_cast<void*>(d + offs[8]) : nullptr) : carry,
-                     first ? initial_state_dtype : KDA_F32,
-                     last ? (final_state ? static_cast<void*>(d + offs[9]) : nullptr) : carry,
-                     last ? final_state_dtype : KDA_F32, nullptr, 0, 1, len, H, kDim, kDim, s);
+        // one pass per block (num_segments = 1): the blocks follow one another, so the
+        // result is that of one one-pass call on all the tokens
+        rc = kda_fwd_segments(
+            d + offs[0] + t0 * row, d + offs[1] + t0 * row, d + offs[2] + t0 * row,
+            d + offs[3] + t0 * row, d + offs[4] + t0 * brow, scale, d + offs[5] + t0 * row,
+            reinterpret_cast<const float*>(d + offs[6]), reinterpret_cast<const float*>(d + offs[7]),
+            lower_bound, first ? (initial_state ? static_cast<void*>(d + offs[8]) : nullptr) : carry,
+            first ? initial_state_dtype : KDA_F32,
+            last ? (final_state ? static_cast<void*>(d + offs[9]) : nullptr) : carry,
+            last ? final_state_dtype : KDA_F32, nullptr, 0, 1, len, H, kDim, kDim, 1, s);
         if (rc != KDA_OK) break;
         e = cudaEventRecord(ev[nblk + b], s);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(sout, ev[nblk + b], 0);
@@ -378,6 +412,9 @@ const char* kda_status_string(int status) {
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
         case KDA_ERR_ARG: return "KDA_ERR_ARG: scale must be finite, lower_bound in [-5.4, 0]";
         case KDA_ERR_ALIAS: return "KDA_ERR_ALIAS: out overlaps an input or states alias unsafely";
+        case KDA_ERR_SEGMENTS:
+            return "KDA_ERR_SEGMENTS: num_segments must be 0 (automatic), 1, or at most the "
+                   "number of 16-token chunks of a fixed-length call";
         case KDA_ERR_SCRATCH_LIMIT:
             return "KDA_ERR_SCRATCH_LIMIT: kda_fwd_noalloc takes at most KDA_NOALLOC_MAX_SEQS "
                    "(65536) sequences";
@@ -387,28 +424,43 @@ const char* kda_status_string(int status) {
 
 size_t kda_fwd_workspace_bytes(int B, int T, int H, int num_seqs, int varlen) {
     if (B < 1 || T < 0 || H < 1) return 0;
-    return scratch_bytes(varlen ? num_seqs : B, varlen != 0);
+    if (varlen) return scratch_bytes(num_seqs, true);
+    // a fixed-length call that kda_fwd splits into segments on the current device
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    const int segs = plan_segments(B, T, H, 0, sms);
+    return segs >= 2 ? split_bytes(B, H, segs) : 0;
 }
 
-int kda_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
-            float scale, void* out, const float* A_log, const float* dt_bias, float lower_bound,
-            const void* initial_state, int initial_state_dtype, void* final_state,
-            int final_state_dtype, const int32_t* cu_seqlens, int num_seqs, int B, int T, int H,
-            int K, int V, void* stream) {
+int kda_fwd_segments(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                     float scale, void* out, const float* A_log, const float* dt_bias,
+                     float lower_bound, const void* initial_state, int initial_state_dtype,
+                     void* final_state, int final_state_dtype, const int32_t* cu_seqlens,
+                     int num_seqs, int B, int T, int H, int K, int V, int num_segments,
+                     void* stream) {
     int rc = validate(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
                       initial_state_dtype, final_state, final_state_dtype, cu_seqlens, num_seqs,
                       B, T, H, K, V, true);
     if (rc != KDA_OK) return rc;
-    int dev = 0;
+    const bool varlen = cu_seqlens != nullptr;
+    if (num_segments < 0 || (varlen && num_segments > 1)) return KDA_ERR_SEGMENTS;
+    if (!varlen && num_segments >= 2 && plan_segments(B, T, H, num_segments, 0) == 0)
+        return KDA_ERR_SEGMENTS;
+    int dev = 0, sms = 0;
     int* err = nullptr;
-    rc = device_setup(&dev, &err);
+    rc = device_setup(&dev, &err, &sms);
     if (rc != KDA_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool varlen = cu_seqlens != nullptr;
     const int N = varlen ? num_seqs : B;
-    const size_t bytes = scratch_bytes(N, varlen);
+    const int segs = varlen ? 1 : plan_segments(B, T, H, num_segments, sms);
+    if (segs == 0) return KDA_ERR_SEGMENTS;
+    const size_t bytes = segs >= 2 ? split_bytes(N, H, segs) : scratch_bytes(N, varlen);
 
-    int* scratch = nullptr;
+    unsigned char* scratch = nullptr;
     if (bytes > 0) {
         const cudaError_t ea = cudaMallocAsync(reinterpret_cast<void**>(&scratch), bytes, s);
         if (ea != cudaSuccess) return cuda_fail(KDA_ERR_ALLOC, ea);
@@ -434,18 +486,49 @@ int kda_fwd(const void* q, const void* k, const void* v, const void* g, const vo
     P.H = H;
 
     SeqMap M{};
-    if (varlen) {
-        M.seq_order = scratch;
-        M.valid = scratch + N;
-    }
     cudaError_t e = cudaSuccess;
-    if (varlen)
-        e = timed_launch(KDA_KERNEL_SEQMAP, s, [&] { return launch_seqmap(P, M, err, s); });
-    if (e == cudaSuccess)
-        e = timed_launch(KDA_KERNEL_FUSED, s, [&] { return launch_fused(P, M, err, s); });
+    if (segs >= 2) {
+        // window 0 -> combine -> window 1, all on the caller's stream
+        const size_t st = (size_t)kDim * kDim * sizeof(float) * N * H;
+        float* w0 = reinterpret_cast<float*>(scratch);
+        float* sin = reinterpret_cast<float*>(scratch + align_up(st * (2 * segs - 3)));
+        Problem P0 = P, P1 = P;
+        P0.window = 0;
+        P0.nseg = segs;
+        P0.final_state = w0;
+        P0.final_dtype = KDA_F32;
+        P1.window = 1;
+        P1.nseg = segs;
+        P1.init_state = sin;
+        P1.init_dtype = KDA_F32;
+        e = timed_launch(KDA_KERNEL_FUSED, s, [&] { return launch_fused(P0, M, err, s); });
+        if (e == cudaSuccess)
+            e = timed_launch(KDA_KERNEL_COMBINE, s,
+                             [&] { return launch_combine(w0, sin, N, H, segs, s); });
+        if (e == cudaSuccess)
+            e = timed_launch(KDA_KERNEL_FUSED, s, [&] { return launch_fused(P1, M, err, s); });
+    } else {
+        if (varlen) {
+            M.seq_order = reinterpret_cast<int*>(scratch);
+            M.valid = M.seq_order + N;
+            e = timed_launch(KDA_KERNEL_SEQMAP, s, [&] { return launch_seqmap(P, M, err, s); });
+        }
+        if (e == cudaSuccess)
+            e = timed_launch(KDA_KERNEL_FUSED, s, [&] { return launch_fused(P, M, err, s); });
+    }
     if (scratch) cudaFreeAsync(scratch, s);
     if (e != cudaSuccess) return cuda_fail(KDA_ERR_LAUNCH, e);
     return KDA_OK;
+}
+
+int kda_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+            float scale, void* out, const float* A_log, const float* dt_bias, float lower_bound,
+            const void* initial_state, int initial_state_dtype, void* final_state,
+            int final_state_dtype, const int32_t* cu_seqlens, int num_seqs, int B, int T, int H,
+            int K, int V, void* stream) {
+    return kda_fwd_segments(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+                            initial_state, initial_state_dtype, final_state, final_state_dtype,
+                            cu_seqlens, num_seqs, B, T, H, K, V, 0, stream);
 }
 
 int kda_fwd_get_error(void* stream) {
@@ -671,6 +754,7 @@ const char* kda_kernel_name(int kernel_id) {
         case KDA_KERNEL_SEQMAP: return "seqmap_kernel";
         case KDA_KERNEL_FUSED: return "fused_kernel";
         case KDA_KERNEL_DECODE: return "decode_kernel";
+        case KDA_KERNEL_COMBINE: return "combine_kernel";
         default: return "unknown";
     }
 }

@@ -50,6 +50,18 @@ struct Problem {
     int N;                   // sequences
     int T;                   // tokens per sequence (fixed) or total tokens (varlen)
     int H;
+    // Sequence split of fixed-length calls (window >= 0; see kda_split.cu).  Every
+    // sequence's n = ceil(T / 16) chunks are cut into nseg segments: segment j holds
+    // chunks floor(j n / nseg) .. floor((j + 1) n / nseg) - 1.
+    //   window 0: 2 nseg - 3 units per sequence: segment 0 from the caller's initial
+    //             state (writes its outputs); for each middle segment j, one unit from
+    //             a zero state (its affine part) and one from the identity state with
+    //             zero values (its transition operator), neither writing outputs.
+    //             Every unit writes its final state, fp32, at index rank.
+    //   window 1: segments 1 .. nseg-1 from the initial states at index rank (fp32),
+    //             writing outputs; the last one writes the caller's final state.
+    int window = -1;         // -1: one unit per (sequence, head), no split
+    int nseg = 0;
 };
 
 // TMA tensor maps over the token rows of q, k, v, g (built on the host per call).
@@ -135,6 +147,7 @@ __device__ __forceinline__ void cp_async_wait() {
 cudaError_t launch_seqmap(const Problem& P, const SeqMap& M, int* err, cudaStream_t s);
 cudaError_t launch_fused(const Problem& P, const SeqMap& M, int* err, cudaStream_t s);
 cudaError_t launch_decode(const Problem& P, cudaStream_t s);
+cudaError_t launch_combine(const float* w0, float* sin, int N, int H, int nseg, cudaStream_t s);
 size_t fused_smem_bytes();
 
 }  // namespace kda

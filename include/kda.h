@@ -62,7 +62,8 @@ typedef enum {
     KDA_ERR_CUDA = -11,           /* another CUDA runtime error                        */
     KDA_ERR_ARG = -12,            /* scale or lower_bound outside the supported range  */
     KDA_ERR_ALIAS = -13,          /* out overlaps an input, or states alias unsafely   */
-    KDA_ERR_SCRATCH_LIMIT = -14   /* kda_fwd_noalloc: num_seqs > KDA_NOALLOC_MAX_SEQS   */
+    KDA_ERR_SCRATCH_LIMIT = -14,  /* kda_fwd_noalloc: num_seqs > KDA_NOALLOC_MAX_SEQS   */
+    KDA_ERR_SEGMENTS = -15        /* kda_fwd_segments: num_segments not possible       */
 } kda_status;
 
 /*
@@ -101,10 +102,13 @@ typedef enum {
  *   stream      cudaStream_t to run on
  *
  * q, k, v, g and out must be 16-byte aligned; out must not overlap any input.
- * Fixed-length calls use no scratch memory.  Varlen calls take
- * kda_fwd_workspace_bytes() of scratch (the longest-first sequence order)
- * from the stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on
- * `stream`); the call does not synchronise.  The first call on a device
+ * kda_fwd is kda_fwd_segments with num_segments = 0: a long fixed-length call
+ * whose B*H recurrences leave most SMs idle is cut into segments that run side
+ * by side (see kda_fwd_segments); other calls run one pass.  Varlen calls take
+ * kda_fwd_workspace_bytes() of scratch (the longest-first sequence order), and
+ * split calls that many bytes of fp32 segment states, from the stream-ordered
+ * allocator (cudaMallocAsync / cudaFreeAsync on `stream`); one-pass
+ * fixed-length calls take none.  The call does not synchronise.  The first call on a device
  * raises the release threshold of that device's default memory pool to its
  * maximum, so that freed scratch stays in the pool instead of going back to
  * the driver at every synchronisation (a process-wide setting of that pool).
@@ -114,6 +118,45 @@ int kda_fwd(const void* q, const void* k, const void* v, const void* g, const vo
             float lower_bound, const void* initial_state, int initial_state_dtype,
             void* final_state, int final_state_dtype, const int32_t* cu_seqlens,
             int num_seqs, int B, int T, int H, int K, int V, void* stream);
+
+/*
+ * kda_fwd_segments -- kda_fwd with the sequence split chosen by the caller.
+ *
+ * The recurrence is affine in the state: over a segment of tokens,
+ * S_end = P S_start + B, with P the product of the segment's transitions
+ * (I - b_t k_t k_t^T) Diag(alpha_t) and B the end state of the segment run from
+ * a zero state.  A fixed-length call cut into s segments (the n = ceil(T / 16)
+ * chunks of a sequence spread evenly: segment j holds chunks floor(j n / s) ..
+ * floor((j + 1) n / s) - 1) runs in two windows of one segment's length:
+ * window 0 runs segment 0 from the initial state and, for each middle segment,
+ * its B (from a zero state) and its P (from the identity state with zero
+ * values); a combine kernel chains S_start(j) = P_{j-1} S_start(j-1) + B_{j-1} in
+ * fp32; window 1 runs segments 1 .. s-1 from their S_start.  That is 2s - 3
+ * recurrences per (sequence, head) in window 0, s - 1 in window 1, for about
+ * 2/s of the one-pass time when they fit on the SMs.  This is the chunk-parallel
+ * stage of the pages' two-stage split ("Moonshot AI Open-Sources FlashKDA",
+ * "What makes the kernel fast": the sequential stage has far less parallelism
+ * than the token-parallel one), applied to whole segments.
+ *
+ *   num_segments  0: automatic -- the largest s whose window-0 recurrences,
+ *                    (2s - 3) B H, fit on the device's SMs, with at least 1,024
+ *                    tokens per segment; one pass when that gives s < 3
+ *                 1: one pass (the same arithmetic as kda_fwd_noalloc)
+ *                 s >= 2: s segments, at most ceil(T / 16) (KDA_ERR_SEGMENTS
+ *                    otherwise, and for num_segments > 1 with cu_seqlens, which
+ *                    always runs one pass)
+ *
+ * Other arguments, layouts and errors as kda_fwd.  Split and one-pass results
+ * differ by rounding only (both are checked against the fp64 oracle); each is
+ * deterministic.  Scratch: kda_fwd_workspace_bytes for the automatic choice;
+ * 4 * 16,384 * B * H * (3s - 4) bytes (rounded up to 256 twice) for s segments.
+ */
+int kda_fwd_segments(const void* q, const void* k, const void* v, const void* g,
+                     const void* beta, float scale, void* out, const float* A_log,
+                     const float* dt_bias, float lower_bound, const void* initial_state,
+                     int initial_state_dtype, void* final_state, int final_state_dtype,
+                     const int32_t* cu_seqlens, int num_seqs, int B, int T, int H, int K,
+                     int V, int num_segments, void* stream);
 
 /*
  * kda_fwd_host -- the same operation on HOST buffers (end-to-end entry point).
@@ -128,8 +171,9 @@ int kda_fwd(const void* q, const void* k, const void* v, const void* g, const vo
  * call with B == 1 and T >= 2048 runs in token blocks (each half of the
  * tokens still left, in whole 16-token chunks, down to 256 tokens; the state
  * carried in fp32 on the device) so that the copies in and out overlap the
- * kernel on two extra streams; its results are bit-identical to one kda_fwd
- * call on the same data.
+ * kernel on two extra streams; its results are bit-identical to one
+ * one-pass call on the same data (kda_fwd_segments with num_segments = 1,
+ * which is kda_fwd whenever kda_fwd does not split the sequence).
  */
 int kda_fwd_host(const void* q, const void* k, const void* v, const void* g,
                  const void* beta, float scale, void* out, const float* A_log,
@@ -163,7 +207,9 @@ const char* kda_status_string(int status);
 int kda_last_cuda_error(void);
 
 /* Bytes of scratch memory kda_fwd takes from the stream-ordered allocator for
- * the given problem (0 for an empty problem).  Host-only, no CUDA call. */
+ * the given problem (0 for an empty problem).  Varlen: host-only, no CUDA call.
+ * Fixed length: reads the current device's SM count, on which the automatic
+ * sequence split depends (0 when no device can be queried). */
 size_t kda_fwd_workspace_bytes(int B, int T, int H, int num_seqs, int varlen);
 
 /*
@@ -178,16 +224,18 @@ size_t kda_fwd_workspace_bytes(int B, int T, int H, int num_seqs, int varlen);
  * fixed array in the library's own device memory instead, and calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *
- * Same arguments, layouts, checks and results as kda_fwd (the caller still
- * passes every input and output buffer), plus:
+ * Same arguments, layouts and checks as kda_fwd (the caller still passes
+ * every input and output buffer).  It always runs one pass, so its results are
+ * those of kda_fwd_segments with num_segments = 1: kda_fwd's own, except on the
+ * long fixed-length calls that kda_fwd splits into segments (whose scratch
+ * would need an allocation).  Plus:
  *   - The scratch is a static device array sized for KDA_NOALLOC_MAX_SEQS
  *     sequences (about 256 KB).  Every GPU that loads this library holds one
  *     copy of it until the process exits.  Varlen calls with
  *     num_seqs > KDA_NOALLOC_MAX_SEQS return KDA_ERR_SCRATCH_LIMIT and launch
  *     nothing.  Fixed-length calls use no scratch.
  *   - The first varlen call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and caches it.
  *   - All calls on a device share the one array.  Each call rewrites the part
  *     it uses before reading it (nothing needs to start at zero), but calls
  *     whose work overlaps on the GPU -- on different streams, or from
@@ -240,7 +288,13 @@ int kda_decode(const void* q, const void* k, const void* v, const void* g, const
  * (KDA_KERNEL_*), the summed device time in milliseconds and the number of
  * launches since the last enable.  Arrays must hold KDA_NUM_KERNELS entries.
  * Returns KDA_OK, or KDA_ERR_CUDA. */
-enum { KDA_KERNEL_SEQMAP = 0, KDA_KERNEL_FUSED = 1, KDA_KERNEL_DECODE = 2, KDA_NUM_KERNELS = 3 };
+enum {
+    KDA_KERNEL_SEQMAP = 0,
+    KDA_KERNEL_FUSED = 1,
+    KDA_KERNEL_DECODE = 2,
+    KDA_KERNEL_COMBINE = 3,
+    KDA_NUM_KERNELS = 4
+};
 int kda_profile_enable(int on);
 int kda_profile_read(double* total_ms, long long* launches);
 const char* kda_kernel_name(int kernel_id);

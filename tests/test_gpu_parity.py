@@ -172,45 +172,52 @@ def test_varlen_uniform_all_heads():
 
 
 def test_long_context_state_carry():
-    """T=65536, H=32 in two 32768-token calls carrying the fp32 state equals one call,
-    and both match the oracle on every head."""
+    """T=65536, H=32 in two 32768-token calls carrying the fp32 state: one pass
+    (num_segments = 1) gives exactly the single call's result; kda_fwd (which splits
+    these 32-head calls into 3 segments) matches the oracle on every head, in one call
+    and in two."""
     import torch
     import gated_delta_rule_39_gb300 as kda
     d = synth.make_workload("carry_t65536_h32")
     x = upload(d)
     H, T = 32, 65536
-    full = torch.empty((1, T, H, 128), dtype=torch.bfloat16, device="cuda:0")
-    S_full = torch.empty((1, H, 128, 128), dtype=torch.float32, device="cuda:0")
-    kda.kda_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], d["scale"], full, x["A_log"],
-                x["dt_bias"], d["lower_bound"], final_state=S_full)
     half = T // 2
-    split = torch.empty_like(full)
-    S_mid = torch.empty_like(S_full)
-    S_end = torch.empty_like(S_full)
     sl = lambda t, a, b: t[:, a:b].contiguous()
-    o1 = torch.empty((1, half, H, 128), dtype=torch.bfloat16, device="cuda:0")
-    o2 = torch.empty_like(o1)
-    kda.kda_fwd(sl(x["q"], 0, half), sl(x["k"], 0, half), sl(x["v"], 0, half),
-                sl(x["g"], 0, half), sl(x["beta"], 0, half), d["scale"], o1, x["A_log"],
-                x["dt_bias"], d["lower_bound"], final_state=S_mid)
-    kda.kda_fwd(sl(x["q"], half, T), sl(x["k"], half, T), sl(x["v"], half, T),
-                sl(x["g"], half, T), sl(x["beta"], half, T), d["scale"], o2, x["A_log"],
-                x["dt_bias"], d["lower_bound"], initial_state=S_mid, final_state=S_end)
-    torch.cuda.synchronize()
-    split[:, :half] = o1
-    split[:, half:] = o2
-    # the two-call result equals the single pass: chunk boundaries coincide at 32768,
-    # so the arithmetic is identical
+
+    def run(fn, segs=None):
+        full = torch.empty((1, T, H, 128), dtype=torch.bfloat16, device="cuda:0")
+        S_full = torch.empty((1, H, 128, 128), dtype=torch.float32, device="cuda:0")
+        kw = {} if segs is None else {"num_segments": segs}
+        fn(x["q"], x["k"], x["v"], x["g"], x["beta"], d["scale"], full, x["A_log"],
+           x["dt_bias"], d["lower_bound"], final_state=S_full, **kw)
+        S_mid = torch.empty_like(S_full)
+        S_end = torch.empty_like(S_full)
+        o1 = torch.empty((1, half, H, 128), dtype=torch.bfloat16, device="cuda:0")
+        o2 = torch.empty_like(o1)
+        fn(sl(x["q"], 0, half), sl(x["k"], 0, half), sl(x["v"], 0, half),
+           sl(x["g"], 0, half), sl(x["beta"], 0, half), d["scale"], o1, x["A_log"],
+           x["dt_bias"], d["lower_bound"], final_state=S_mid, **kw)
+        fn(sl(x["q"], half, T), sl(x["k"], half, T), sl(x["v"], half, T),
+           sl(x["g"], half, T), sl(x["beta"], half, T), d["scale"], o2, x["A_log"],
+           x["dt_bias"], d["lower_bound"], initial_state=S_mid, final_state=S_end, **kw)
+        torch.cuda.synchronize()
+        return full, S_full, torch.cat([o1, o2], dim=1), S_end
+
+    # one pass: chunk boundaries coincide at 32768, so the arithmetic is identical
+    full, S_full, split, S_end = run(kda.kda_fwd_segments, 1)
     assert torch.equal(split, full)
     assert torch.equal(S_end, S_full)
     ro, rs = run_oracle(d)
-    e = out_error(to_f64(full), ro)
-    assert e["ok"], e
-    se = state_error(to_f64(S_full), rs)
-    assert se["ok"], se
+    r = run(kda.kda_fwd)
+    for o, s_ in [(full, S_full), (r[0], r[1]), (r[2], r[3])]:
+        e = out_error(to_f64(o), ro)
+        assert e["ok"], e
+        se = state_error(to_f64(s_), rs)
+        assert se["ok"], se
 
 
-def test_maximum_size_tail():
+@pytest.mark.parametrize("segments", [1, 0])
+def test_maximum_size_tail(segments):
     """The largest call the boundary accepts with one head: T = 2^24 - 7 tokens, so each
     token tensor holds 2^31 - 896 elements (the limit is 2^31) and the last chunk is
     ragged.  The oracle cannot replay 16.8 M tokens, but the recurrence forgets: over
@@ -218,7 +225,8 @@ def test_maximum_size_tail():
     recipe, so the outputs of the last 256 tokens and the final state equal those of
     the oracle started from a zero state on the last 512 tokens (checked here against a
     768-token window).  This covers the far end of maximal tensors, where 32-bit index
-    arithmetic would overflow first."""
+    arithmetic would overflow first.  Run in one pass and as kda_fwd runs it (split
+    into 77 segments on 152 SMs)."""
     import torch
     import gated_delta_rule_39_gb300 as kda
     T, H = (1 << 24) - 7, 1
@@ -226,9 +234,9 @@ def test_maximum_size_tail():
     d = synth.make_inputs_device(T, H, seed=31)
     out = torch.empty((1, T, H, 128), dtype=torch.bfloat16, device="cuda:0")
     fs = torch.empty((1, H, 128, 128), dtype=torch.float32, device="cuda:0")
-    kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], out,
-                torch.from_numpy(d["A_log"]).cuda(), torch.from_numpy(d["dt_bias"]).cuda(),
-                d["lower_bound"], final_state=fs)
+    kda.kda_fwd_segments(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], out,
+                         torch.from_numpy(d["A_log"]).cuda(), torch.from_numpy(d["dt_bias"]).cuda(),
+                         d["lower_bound"], final_state=fs, num_segments=segments)
     torch.cuda.synchronize()
     assert kda.kda_fwd_get_error() == 0
     tail = 256
