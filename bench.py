@@ -216,12 +216,13 @@ def roofline_of(kernel, ms, bytes_, flop, hbm, tflops, src):
 class Runner:
     """Device copies of one workload and the call sequence of one step."""
 
-    def __init__(self, d, device, stream):
+    def __init__(self, d, device, stream, segments=0):
         import torch
         import gated_delta_rule_39_gb300 as kda
         self.kda = kda
         self.d = d
         self.stream = stream
+        self.segments = segments   # 0: kda_fwd's own choice; else kda_fwd_segments
         B, T, H, _ = d["q"].shape
         self.B, self.T, self.H, self.N = B, T, H, d["N"]
 
@@ -250,17 +251,19 @@ class Runner:
 
     def step(self):
         kda, x, d = self.kda, self.x, self.d
+        seg = {} if self.segments == 0 or self.cu is not None else {"num_segments": self.segments}
+        fwd = kda.kda_fwd_segments if seg else kda.kda_fwd
         if self.calls == 1:
-            kda.kda_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], d["scale"], self.out,
-                        self.A_log, self.dt_bias, d["lower_bound"], initial_state=self.s0,
-                        final_state=self.s1, cu_seqlens=self.cu, stream=self.stream)
+            fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], d["scale"], self.out,
+                self.A_log, self.dt_bias, d["lower_bound"], initial_state=self.s0,
+                final_state=self.s1, cu_seqlens=self.cu, stream=self.stream, **seg)
             return
         for i, xp in enumerate(self.pieces):
-            kda.kda_fwd(xp["q"], xp["k"], xp["v"], xp["g"], xp["beta"], d["scale"],
-                        self.opieces[i], self.A_log, self.dt_bias, d["lower_bound"],
-                        initial_state=(self.s0 if i == 0 else self.carry),
-                        final_state=(self.s1 if i == self.calls - 1 else self.carry),
-                        stream=self.stream)
+            fwd(xp["q"], xp["k"], xp["v"], xp["g"], xp["beta"], d["scale"],
+                self.opieces[i], self.A_log, self.dt_bias, d["lower_bound"],
+                initial_state=(self.s0 if i == 0 else self.carry),
+                final_state=(self.s1 if i == self.calls - 1 else self.carry),
+                stream=self.stream, **seg)
 
 
 class DecodeRunner:
@@ -387,7 +390,7 @@ def run_cuda(args, world, rank, local, pg):
             d = synth.make_inputs(w.B, w.T, args.heads, seed=rank, init_dtype=w.init_dtype)
         else:
             d = synth.make_workload(name, seed=rank)
-        runner = Runner(d, device, stream)
+        runner = Runner(d, device, stream, args.segments)
     B, T, H, N = runner.B, runner.T, runner.H, runner.N
 
     # ---- timed region: K steps, launch timing on the launch stream -------------
@@ -494,6 +497,8 @@ def run_cuda(args, world, rank, local, pg):
                 "roofline": main["roofline"], "path_roofline": main["path_roofline"],
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": main["gpu_launches"],
                 "kernel_ms": main["kernel_ms"], "clocks": clocks}
+        if args.segments:
+            line["config"]["segments"] = args.segments
         if others:
             line["workloads"] = others
         print(json.dumps(line), flush=True)
@@ -590,6 +595,9 @@ def main():
                     help="profiling only: run the workload with this many heads instead")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="time this workload instead of the headline one (profiling)")
+    ap.add_argument("--segments", type=int, default=0,
+                    help="sequence split of fixed-length calls: 0 = kda_fwd's own choice, "
+                         "1 = one pass, s = s segments (kda_fwd_segments)")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip the nested measurements of the other workloads")
     args = ap.parse_args()
