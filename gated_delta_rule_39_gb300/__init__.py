@@ -26,8 +26,9 @@ _LIB_PATH = os.path.join(_HERE, "_lib", "libkda.so")
 
 KDA_BF16 = 0
 KDA_F32 = 1
-KDA_NUM_KERNELS = 4
-KERNEL_NAMES = ("seqmap_kernel", "fused_kernel", "decode_kernel", "combine_kernel")
+KDA_NUM_KERNELS = 6
+KERNEL_NAMES = ("seqmap_kernel", "fused_kernel", "decode_kernel", "combine_kernel",
+                "segprep_kernel", "segfinal_kernel")
 
 _lib = None
 _vp = ctypes.c_void_p

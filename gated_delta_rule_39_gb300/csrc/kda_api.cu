@@ -152,12 +152,24 @@ int plan_segments(int B, int T, int H, int requested, int sms) {
     return s >= 3 ? s : 1;
 }
 
-// window-0 end states and window-1 initial states of a split call (fp32)
-size_t split_bytes(int N, int H, int s) {
-    if (s < 2) return 0;
+// Scratch of a split call (fp32 states of every unit; see kda_split.cu): window 0's
+// initial states (reused for window 1's end states), window 0's end states, window 1's
+// initial states, and 16 zero rows of values.
+struct SplitScratch {
+    size_t init0, end0, init1, zero, total;
+};
+SplitScratch split_layout(int N, int H, int s) {
+    SplitScratch L{};
+    if (s < 2) return L;
     const size_t st = (size_t)kDim * kDim * sizeof(float) * N * H;
-    return align_up(st * (2 * s - 3)) + align_up(st * (s - 1));
+    L.init0 = 0;
+    L.end0 = align_up(st * (2 * s - 3));
+    L.init1 = L.end0 + align_up(st * (2 * s - 3));
+    L.zero = L.init1 + align_up(st * (s - 1));
+    L.total = L.zero + align_up((size_t)kChunk * H * kDim * 2);
+    return L;
 }
+size_t split_bytes(int N, int H, int s) { return split_layout(N, H, s).total; }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     if (!a || !b || na == 0 || nb == 0) return false;
@@ -488,25 +500,44 @@ int kda_fwd_segments(const void* q, const void* k, const void* v, const void* g,
     SeqMap M{};
     cudaError_t e = cudaSuccess;
     if (segs >= 2) {
-        // window 0 -> combine -> window 1, all on the caller's stream
-        const size_t st = (size_t)kDim * kDim * sizeof(float) * N * H;
-        float* w0 = reinterpret_cast<float*>(scratch);
-        float* sin = reinterpret_cast<float*>(scratch + align_up(st * (2 * segs - 3)));
+        // initial states -> window 0 -> combine -> window 1 -> final state, all on the
+        // caller's stream; every unit's states live at its own index of fp32 scratch
+        const SplitScratch L = split_layout(N, H, segs);
+        float* init0 = reinterpret_cast<float*>(scratch + L.init0);
+        float* end0 = reinterpret_cast<float*>(scratch + L.end0);
+        float* init1 = reinterpret_cast<float*>(scratch + L.init1);
+        float* end1 = init0;   // free once window 0 has run
+        auto* zero = reinterpret_cast<__nv_bfloat16*>(scratch + L.zero);
         Problem P0 = P, P1 = P;
         P0.window = 0;
         P0.nseg = segs;
-        P0.final_state = w0;
+        P0.vzero = zero;
+        P0.init_state = init0;
+        P0.init_dtype = KDA_F32;
+        P0.final_state = end0;
         P0.final_dtype = KDA_F32;
         P1.window = 1;
         P1.nseg = segs;
-        P1.init_state = sin;
+        P1.init_state = init1;
         P1.init_dtype = KDA_F32;
-        e = timed_launch(KDA_KERNEL_FUSED, s, [&] { return launch_fused(P0, M, err, s); });
+        P1.final_state = end1;
+        P1.final_dtype = KDA_F32;
+        e = cudaMemsetAsync(zero, 0, (size_t)kChunk * H * kDim * 2, s);
+        if (e == cudaSuccess)
+            e = timed_launch(KDA_KERNEL_SEGPREP, s, [&] {
+                return launch_segprep(initial_state, initial_state_dtype, init0, N, H, segs, s);
+            });
+        if (e == cudaSuccess)
+            e = timed_launch(KDA_KERNEL_FUSED, s, [&] { return launch_fused(P0, M, err, s); });
         if (e == cudaSuccess)
             e = timed_launch(KDA_KERNEL_COMBINE, s,
-                             [&] { return launch_combine(w0, sin, N, H, segs, s); });
+                             [&] { return launch_combine(end0, init1, N, H, segs, s); });
         if (e == cudaSuccess)
             e = timed_launch(KDA_KERNEL_FUSED, s, [&] { return launch_fused(P1, M, err, s); });
+        if (e == cudaSuccess)
+            e = timed_launch(KDA_KERNEL_SEGFINAL, s, [&] {
+                return launch_segfinal(end1, final_state, final_state_dtype, N, H, segs, s);
+            });
     } else {
         if (varlen) {
             M.seq_order = reinterpret_cast<int*>(scratch);
@@ -755,6 +786,8 @@ const char* kda_kernel_name(int kernel_id) {
         case KDA_KERNEL_FUSED: return "fused_kernel";
         case KDA_KERNEL_DECODE: return "decode_kernel";
         case KDA_KERNEL_COMBINE: return "combine_kernel";
+        case KDA_KERNEL_SEGPREP: return "segprep_kernel";
+        case KDA_KERNEL_SEGFINAL: return "segfinal_kernel";
         default: return "unknown";
     }
 }

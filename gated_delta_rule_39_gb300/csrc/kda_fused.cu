@@ -274,11 +274,8 @@ __device__ __forceinline__ float tf32_round(float x) {
 }
 
 struct Unit {
-    int n, h, tok_start, L, nch;
-    int nf;          // index of the final state to write, -1: none
-    int init_mode;   // 0: P.init_state[n] (or zero without one), 1: zero, 2: identity
-    bool vzero;      // values taken as zero (the v rows are not loaded)
-    bool noout;      // no outputs written
+    int n, h, tok_start, L, nch;   // n: index of the initial and final state
+    bool vzero;                    // values taken as zero (v read from 16 zero rows)
 };
 
 // ---- raw-row loads on the TMA engine (one thread) ----------------------------------
@@ -295,22 +292,22 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 }
 
 __device__ void loader(const RawMaps& TM, const Unit& U, Smem& S, int* err) {
-    const CUtensorMap* maps[4] = {&TM.q, &TM.k, &TM.v, &TM.g};
+    const CUtensorMap* maps[4] = {&TM.q, &TM.k, U.vzero ? &TM.vz : &TM.v, &TM.g};
     int c = 0;   // chunks issued
     for (; c < U.nch; ++c) {
         const int slot = c % kRaw;
         if (c >= kRaw && !mbar_wait(&S.raw_empty[slot], (unsigned)(((c / kRaw) - 1) & 1), err))
             break;
         const uint32_t full = smem_u32(&S.raw_full[slot]);
-        tc::mbar_arrive_expect_tx(full, U.vzero ? kRawBytes - kRawBytes / 4 : kRawBytes);
+        tc::mbar_arrive_expect_tx(full, kRawBytes);
         const int row = U.tok_start + c * kChunk;
+        const int vrow = U.vzero ? 0 : row;   // zero values: the same 16 zero rows each chunk
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            if (t == 2 && U.vzero) continue;   // zero values: the producers use 0
+        for (int t = 0; t < 4; ++t)
 #pragma unroll
             for (int half = 0; half < 2; ++half)
-                tma_load_3d(smem_u32(S.raw[slot].x[t][half]), maps[t], 64 * half, U.h, row, full);
-        }
+                tma_load_3d(smem_u32(S.raw[slot].x[t][half]), maps[t], 64 * half, U.h,
+                            t == 2 ? vrow : row, full);
     }
     // Do not let the CTA exit while copies it issued are still landing.  Each slot has at
     // most one copy in flight (the next one waits for raw_empty), so the last issues of
@@ -357,7 +354,7 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
                     };
                     rq[i] = ld(0);
                     rk[i] = ld(1);
-                    rv[i] = U.vzero ? 0u : ld(2);
+                    rv[i] = ld(2);
                     rg[i] = ld(3);
                 }
             }
@@ -847,18 +844,13 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
     const int v = 32 * ew + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * ew) << 16);   // this warp's lane quarter
     const size_t sbase = ((size_t)U.n * P.H + U.h) * kDim * kDim + v;   // + c * kDim
-    const size_t fbase = ((size_t)max(U.nf, 0) * P.H + U.h) * kDim * kDim + v;
-    const bool write_final = P.final_state != nullptr && U.nf >= 0;
-    // element (key c, value v) of the initial state
-    const auto init_at = [&](int c) -> float {
-        if (U.init_mode == 2) return c == v ? 1.0f : 0.0f;
-        return (U.init_mode == 0 && P.init_state) ? state_in(P, sbase + (size_t)c * kDim) : 0.0f;
-    };
     bool ok = true;
 
     if (U.nch == 0) {   // no tokens: the final state is the initial state
-        if (write_final)
-            for (int c = 0; c < kDim; ++c) state_out(P, fbase + (size_t)c * kDim, init_at(c));
+        if (P.final_state)
+            for (int c = 0; c < kDim; ++c)
+                state_out(P, sbase + (size_t)c * kDim,
+                          P.init_state ? state_in(P, sbase + (size_t)c * kDim) : 0.0f);
         return;
     }
     // initial state S0 into buffer 0, then S0 Diag(2^G_last of chunk 0) into buffer 1
@@ -866,7 +858,10 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
     for (int piece = 0; piece < 4; ++piece) {
         uint32_t x[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = __float_as_uint(init_at(32 * piece + i));
+        for (int i = 0; i < 32; ++i) {
+            const int c = 32 * piece + i;
+            x[i] = __float_as_uint(P.init_state ? state_in(P, sbase + (size_t)c * kDim) : 0.0f);
+        }
         tc::st32(tl + TM_S + 32 * piece, x);
     }
     tc::wait_st();
@@ -912,7 +907,7 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
             tc::wait_st();
             tc::fence_before_sync();
             mbar_arrive(&S.scaled);
-        } else if (write_final) {
+        } else if (P.final_state) {
 #pragma unroll 1
             for (int piece = 0; piece < 4; ++piece) {
                 uint32_t x[32];
@@ -920,11 +915,11 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
                 tc::wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    state_out(P, fbase + (size_t)(32 * piece + i) * kDim, __uint_as_float(x[i]));
+                    state_out(P, sbase + (size_t)(32 * piece + i) * kDim, __uint_as_float(x[i]));
             }
         }
         // outputs of chunk c - 1: O^T lane v, column t = token
-        if (!U.noout) {
+        {
             uint32_t o[16];
             tc::ld16(tl + TM_UO + 32u * uob, o);
             tc::wait_ld();
@@ -953,32 +948,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     Unit U;
     U.h = blockIdx.x % P.H;
     const int rank = blockIdx.x / P.H;
-    U.init_mode = 0;
     U.vzero = false;
-    U.noout = false;
     if (P.window >= 0) {
-        // sequence split (fixed length): the unit's sequence, segment and kind
+        // sequence split (fixed length): the unit's sequence, segment and kind.  Its
+        // initial state (prepared on the host side: the caller's, zero or identity) and
+        // its final state are at index rank of fp32 scratch.
         const int per = P.window == 0 ? 2 * P.nseg - 3 : P.nseg - 1;
         const int seq = rank / per, vj = rank % per;
-        int j = vj;                               // segment
-        U.n = rank;
-        U.nf = rank;
-        if (P.window == 0) {
-            if (vj == 0) {
-                U.n = seq;                        // the caller's initial state
-            } else if (vj <= P.nseg - 2) {
-                U.init_mode = 1;                  // affine part: zero initial state
-                U.noout = true;
-            } else {
-                j = vj - (P.nseg - 2);            // transition operator: identity state,
-                U.init_mode = 2;                  // zero values
-                U.vzero = true;
-                U.noout = true;
-            }
-        } else {
-            j = vj + 1;
-            U.nf = (j == P.nseg - 1) ? seq : -1;  // the caller's final state
+        int j = P.window == 0 ? vj : vj + 1;      // segment
+        if (P.window == 0 && vj > P.nseg - 2) {
+            j = vj - (P.nseg - 2);                // transition operator: zero values
+            U.vzero = true;
         }
+        U.n = rank;
         const long long nchk = (P.T + kChunk - 1) / kChunk;
         const int c0 = (int)((long long)j * nchk / P.nseg);
         const int c1 = (int)((long long)(j + 1) * nchk / P.nseg);
@@ -994,7 +976,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         U.tok_start = P.cu_seqlens[U.n];
         U.L = P.cu_seqlens[U.n + 1] - U.tok_start;
     }
-    if (P.window < 0) U.nf = U.n;
     U.nch = (U.L + kChunk - 1) / kChunk;
 
     if (threadIdx.x == 0) {
@@ -1111,9 +1092,9 @@ cudaError_t launch_fused(const Problem& P, const SeqMap& M, int* err, cudaStream
     if (rows > 0) {
         cudaError_t e = encode_rows(&TM.q, P.q, P.H, rows);
         if (e == cudaSuccess) e = encode_rows(&TM.k, P.k, P.H, rows);
-        // v is not read by units with zero values; a window-0 launch still has some
-        // units that read it
         if (e == cudaSuccess) e = encode_rows(&TM.v, P.v, P.H, rows);
+        // 16 zero rows for the units with zero values (window 0 of a split call)
+        if (e == cudaSuccess && P.vzero) e = encode_rows(&TM.vz, P.vzero, P.H, kChunk);
         if (e == cudaSuccess) e = encode_rows(&TM.g, P.g, P.H, rows);
         if (e != cudaSuccess) return e;
     }   // else no tokens: the loader issues nothing

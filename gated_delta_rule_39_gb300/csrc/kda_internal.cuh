@@ -52,21 +52,23 @@ struct Problem {
     int H;
     // Sequence split of fixed-length calls (window >= 0; see kda_split.cu).  Every
     // sequence's n = ceil(T / 16) chunks are cut into nseg segments: segment j holds
-    // chunks floor(j n / nseg) .. floor((j + 1) n / nseg) - 1.
-    //   window 0: 2 nseg - 3 units per sequence: segment 0 from the caller's initial
-    //             state (writes its outputs); for each middle segment j, one unit from
-    //             a zero state (its affine part) and one from the identity state with
-    //             zero values (its transition operator), neither writing outputs.
-    //             Every unit writes its final state, fp32, at index rank.
-    //   window 1: segments 1 .. nseg-1 from the initial states at index rank (fp32),
-    //             writing outputs; the last one writes the caller's final state.
+    // chunks floor(j n / nseg) .. floor((j + 1) n / nseg) - 1.  Unit `rank` of a window
+    // reads its initial state and writes its final state at index rank (fp32).
+    //   window 0: 2 nseg - 3 units per sequence: segment 0, then for each middle
+    //             segment j its affine part and its transition operator (whose values
+    //             are zero: v is read from the 16 zero rows at `vzero`).
+    //   window 1: segments 1 .. nseg-1.
+    // Every unit writes its outputs; those of window 0's middle units are overwritten
+    // by window 1.
     int window = -1;         // -1: one unit per (sequence, head), no split
     int nseg = 0;
+    const __nv_bfloat16* vzero = nullptr;   // [16][H][128] zeros (window 0)
 };
 
 // TMA tensor maps over the token rows of q, k, v, g (built on the host per call).
 struct RawMaps {
     CUtensorMap q, k, v, g;
+    CUtensorMap vz;   // zero rows (sequence split, window 0)
 };
 
 // Scratch written by the varlen sequence map, read by the fused kernel.
@@ -148,6 +150,10 @@ cudaError_t launch_seqmap(const Problem& P, const SeqMap& M, int* err, cudaStrea
 cudaError_t launch_fused(const Problem& P, const SeqMap& M, int* err, cudaStream_t s);
 cudaError_t launch_decode(const Problem& P, cudaStream_t s);
 cudaError_t launch_combine(const float* w0, float* sin, int N, int H, int nseg, cudaStream_t s);
+cudaError_t launch_segprep(const void* init, int init_dtype, float* w0init, int N, int H, int nseg,
+                           cudaStream_t s);
+cudaError_t launch_segfinal(const float* w1final, void* final_state, int final_dtype, int N, int H,
+                            int nseg, cudaStream_t s);
 size_t fused_smem_bytes();
 
 }  // namespace kda

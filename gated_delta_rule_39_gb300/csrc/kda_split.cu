@@ -24,8 +24,12 @@
 // ("Moonshot AI Open-Sources FlashKDA", "What makes the kernel fast": the
 // sequential stage has far less parallelism than the token-parallel one).
 //
-// This file holds the combine step: one CTA per (sequence, head), fp32 products
-// of 128 x 128 matrices on CUDA cores (the chain is s - 2 products long).
+// This file holds the steps around the two windows: the initial states of window 0
+// (the caller's, zero, identity; fp32), the combine step (one CTA per (sequence,
+// head), fp32 products of 128 x 128 matrices on CUDA cores, a chain of s - 2), and
+// the copy of the last segment's end state into the caller's final state.  Each
+// unit of a window reads and writes its states at its own index, so the fused
+// kernel's epilogue is the same as for a one-pass call.
 #include <atomic>
 
 #include "kda_internal.cuh"
@@ -36,6 +40,8 @@ namespace {
 
 constexpr int kCombThreads = 256;   // 16 x 16 threads, an 8 x 8 output tile each
 constexpr int kPad = 132;           // row stride of the transposed operator (floats)
+constexpr int kCopyThreads = 256;
+constexpr size_t kKV = (size_t)kDim * kDim;   // elements of one state
 
 struct CombSmem {
     float pt[kDim][kPad];   // P_{j-1} transposed: pt[k][r] = P[r][k]
@@ -52,7 +58,6 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __re
     const int h = blockIdx.x % H, seq = blockIdx.x / H;
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
     const int per0 = 2 * nseg - 3, per1 = nseg - 1;
-    constexpr size_t kKV = (size_t)kDim * kDim;
     const auto w0_at = [&](int unit) { return w0 + ((size_t)(seq * per0 + unit) * H + h) * kKV; };
     const auto sin_at = [&](int j) { return sin + ((size_t)(seq * per1 + j - 1) * H + h) * kKV; };
 
@@ -115,7 +120,80 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __re
     }
 }
 
+__device__ __forceinline__ float4 load4(const void* base, int dtype, size_t idx) {
+    if (dtype == KDA_F32) return *reinterpret_cast<const float4*>(static_cast<const float*>(base) + idx);
+    const uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + idx);
+    return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                       __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+}
+
+// Window 0's initial states, unit rank = seq (2s - 3) + vj: vj = 0 the caller's state
+// (zero without one), 1 .. s-2 zero (affine parts), s-1 .. 2s-4 identity (transition
+// operators).  One CTA per (unit, head).
+__global__ void __launch_bounds__(kCopyThreads) segprep_kernel(const void* __restrict__ init,
+                                                              int init_dtype,
+                                                              float* __restrict__ w0init, int H,
+                                                              int nseg) {
+    const int h = blockIdx.x % H, rank = blockIdx.x / H;
+    const int per = 2 * nseg - 3, seq = rank / per, vj = rank % per;
+    float4* dst = reinterpret_cast<float4*>(w0init + (size_t)blockIdx.x * kKV);
+    const size_t src = ((size_t)seq * H + h) * kKV;
+    for (int i = threadIdx.x; i < (int)(kKV / 4); i += kCopyThreads) {
+        float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (vj == 0) {
+            if (init) x = load4(init, init_dtype, src + 4 * (size_t)i);
+        } else if (vj > nseg - 2) {
+            const int r = (4 * i) >> 7, c = (4 * i) & 127;   // element (r, c .. c + 3)
+            x.x = r == c ? 1.0f : 0.0f;
+            x.y = r == c + 1 ? 1.0f : 0.0f;
+            x.z = r == c + 2 ? 1.0f : 0.0f;
+            x.w = r == c + 3 ? 1.0f : 0.0f;
+        }
+        dst[i] = x;
+    }
+}
+
+// The caller's final state from window 1's last unit of each sequence.
+__global__ void __launch_bounds__(kCopyThreads) segfinal_kernel(const float* __restrict__ w1final,
+                                                               void* __restrict__ final_state,
+                                                               int final_dtype, int H, int nseg) {
+    const int h = blockIdx.x % H, seq = blockIdx.x / H;
+    const int rank = seq * (nseg - 1) + nseg - 2;
+    const float4* src = reinterpret_cast<const float4*>(w1final + ((size_t)rank * H + h) * kKV);
+    const size_t dst = ((size_t)seq * H + h) * kKV;
+    for (int i = threadIdx.x; i < (int)(kKV / 4); i += kCopyThreads) {
+        const float4 x = src[i];
+        if (final_dtype == KDA_F32) {
+            reinterpret_cast<float4*>(static_cast<float*>(final_state) + dst)[i] = x;
+        } else {
+            const __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y);
+            const __nv_bfloat162 b = __floats2bfloat162_rn(x.z, x.w);
+            uint2 raw;
+            raw.x = *reinterpret_cast<const uint32_t*>(&a);
+            raw.y = *reinterpret_cast<const uint32_t*>(&b);
+            reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(final_state) + dst)[i] = raw;
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_segprep(const void* init, int init_dtype, float* w0init, int N, int H, int nseg,
+                           cudaStream_t s) {
+    const long long ctas = (long long)N * H * (2 * nseg - 3);
+    if (ctas == 0) return cudaSuccess;
+    segprep_kernel<<<(unsigned)ctas, kCopyThreads, 0, s>>>(init, init_dtype, w0init, H, nseg);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_segfinal(const float* w1final, void* final_state, int final_dtype, int N, int H,
+                            int nseg, cudaStream_t s) {
+    const long long ctas = (long long)N * H;
+    if (ctas == 0 || final_state == nullptr) return cudaSuccess;
+    segfinal_kernel<<<(unsigned)ctas, kCopyThreads, 0, s>>>(w1final, final_state, final_dtype, H,
+                                                           nseg);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const float* w0, float* sin, int N, int H, int nseg, cudaStream_t s) {
     const long long ctas = (long long)N * H;

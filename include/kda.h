@@ -149,7 +149,9 @@ int kda_fwd(const void* q, const void* k, const void* v, const void* g, const vo
  * Other arguments, layouts and errors as kda_fwd.  Split and one-pass results
  * differ by rounding only (both are checked against the fp64 oracle); each is
  * deterministic.  Scratch: kda_fwd_workspace_bytes for the automatic choice;
- * 4 * 16,384 * B * H * (3s - 4) bytes (rounded up to 256 twice) for s segments.
+ * for s segments 65,536 * B * H * (5s - 7) + 4,096 * H bytes, each of its four
+ * parts rounded up to 256 (fp32 initial and end states of every segment's runs
+ * and 16 zero rows of values).
  */
 int kda_fwd_segments(const void* q, const void* k, const void* v, const void* g,
                      const void* beta, float scale, void* out, const float* A_log,
@@ -293,7 +295,9 @@ enum {
     KDA_KERNEL_FUSED = 1,
     KDA_KERNEL_DECODE = 2,
     KDA_KERNEL_COMBINE = 3,
-    KDA_NUM_KERNELS = 4
+    KDA_KERNEL_SEGPREP = 4,
+    KDA_KERNEL_SEGFINAL = 5,
+    KDA_NUM_KERNELS = 6
 };
 int kda_profile_enable(int on);
 int kda_profile_read(double* total_ms, long long* launches);

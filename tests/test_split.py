@@ -120,7 +120,8 @@ def test_automatic_split_on_few_heads():
     prof = kda.kda_profile_read()
     kda.kda_profile_enable(False)
     assert prof["fused_kernel"][1] == 2 and prof["combine_kernel"][1] == 1
-    assert kda.kda_fwd_workspace_bytes(1, 4096, 4) == 4 * 128 * 128 * 4 * (5 + 3)
+    assert prof["segprep_kernel"][1] == 1 and prof["segfinal_kernel"][1] == 1
+    assert kda.kda_fwd_workspace_bytes(1, 4096, 4) == 65536 * 4 * (5 * 4 - 7) + 4096 * 4
     _check(d, out, fs)
 
 
@@ -138,6 +139,7 @@ def test_many_heads_run_one_pass():
     prof = kda.kda_profile_read()
     kda.kda_profile_enable(False)
     assert prof["fused_kernel"][1] == 1 and prof["combine_kernel"][1] == 0
+    assert prof["segprep_kernel"][1] == 0
     one = _run(d, 1, x=x)
     assert torch.equal(out, one[0]) and torch.equal(fs, one[1])
 
