@@ -180,7 +180,7 @@ def ncu_traffic(kernel: str, workload: str | None = None):
 # The other workloads of the pages' benchmark reported in the same line (each a
 # nested object with its own timing, roofline and CPU-oracle sample).
 OTHER_WORKLOADS = ("prefill_t8192_h64", "varlen_mixed_t8192_h96", "varlen_uniform_8x1024_h96",
-                   "carry_t65536_h32")
+                   "carry_t65536_h32", "varlen_short_20000_h16")
 
 
 def algorithmic_work(d, calls):
@@ -191,10 +191,14 @@ def algorithmic_work(d, calls):
     th = B * T * H
     s0 = d.get("initial_state")
     init_b = 0 if s0 is None else (2 if s0.dtype == np.uint16 else 4)
+    w = d.get("workload")
+    fd = "f32" if w is None else w.final_dtype
+    write_b = 0 if fd is None else (4 if fd == "f32" else 2)
     state_bytes = 0
     for i in range(calls):
         read_b = init_b if i == 0 else 4      # later calls read the carried fp32 state
-        state_bytes += N * H * K * V * (read_b + 4)
+        last = i == calls - 1
+        state_bytes += N * H * K * V * (read_b + (write_b if last else 4))
     return BYTES_PER_TH * th + state_bytes, FLOP_PER_TH * th, th
 
 
@@ -239,8 +243,11 @@ class Runner:
         cu = d.get("cu_seqlens")
         self.cu = None if cu is None else torch.from_numpy(cu.astype(np.int32)).to(device)
         self.out = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=device)
-        self.s1 = torch.empty((self.N, H, K, V), dtype=torch.float32, device=device)
         w = d.get("workload")
+        fd = "f32" if w is None else w.final_dtype   # None: the call writes no final state
+        self.s1 = (None if fd is None else
+                   torch.empty((self.N, H, K, V), device=device,
+                               dtype=torch.float32 if fd == "f32" else torch.bfloat16))
         self.calls = w.carry_calls if w is not None else 1
         if self.calls > 1:   # one sequence cut into `calls` pieces, the state carried
             L = T // self.calls

@@ -157,6 +157,11 @@ static_assert(kRawBytes == 16384, "four tensors x 16 rows x 256 bytes");
 struct ProdShared {
     float Akk[2][kChunk * AK_LD];                  // A_kk (before diag(b)) per chunk parity
 };
+constexpr int kUnitRing = 8;   // unit indices the loader may publish ahead of the roles
+// warps that read each published unit index: epilogue 4, MMA 1, solver 1, A products 2,
+// w 2, producers 8 (every warp but the loader's)
+constexpr int kUnitReaders = 18;
+
 struct Smem {
     Stage st[kRing];
     EarlySlot early[kEarly];
@@ -176,6 +181,10 @@ struct Smem {
                                          // and the chunk's O|U MMAs complete (commit)
     unsigned long long epi_done;         // epilogue finished with tensor memory
     unsigned long long drain;            // the MMA thread's exit drain (one commit)
+    // persistent calls: the units this CTA takes, in order (loader -> every role)
+    unsigned long long unit_full[kUnitRing];    // the loader wrote unit[slot]
+    unsigned long long unit_empty[kUnitRing];   // every consumer warp has read it
+    int unit[kUnitRing][6];                     // n, h, tok_start, L, nch (-1: none), vzero
     uint32_t tmem_base;
 };
 
@@ -278,6 +287,89 @@ struct Unit {
     bool vzero;                    // values taken as zero (v read from 16 zero rows)
 };
 
+// Unit `id` of a launch (id = rank * H + h): its head, tokens and state index.
+__device__ __forceinline__ Unit unit_at(const Problem& P, const SeqMap& M, int id) {
+    Unit U;
+    U.h = id % P.H;
+    const int rank = id / P.H;
+    U.vzero = false;
+    if (P.window >= 0) {
+        // sequence split (fixed length): the unit's sequence, segment and kind.  Its
+        // initial state (prepared on the host side: the caller's, zero or identity) and
+        // its final state are at index rank of fp32 scratch.
+        const int per = P.window == 0 ? 2 * P.nseg - 3 : P.nseg - 1;
+        const int seq = rank / per, vj = rank % per;
+        int j = P.window == 0 ? vj : vj + 1;      // segment
+        if (P.window == 0 && vj > P.nseg - 2) {
+            j = vj - (P.nseg - 2);                // transition operator: zero values
+            U.vzero = true;
+        }
+        U.n = rank;
+        const long long nchk = (P.T + kChunk - 1) / kChunk;
+        const int c0 = (int)((long long)j * nchk / P.nseg);
+        const int c1 = (int)((long long)(j + 1) * nchk / P.nseg);
+        U.tok_start = seq * P.T + c0 * kChunk;
+        U.L = min(c1 * kChunk, P.T) - c0 * kChunk;
+    } else if (P.cu_seqlens == nullptr) {
+        U.n = rank;
+        U.tok_start = rank * P.T;
+        U.L = P.T;
+    } else {
+        U.n = M.seq_order[rank];
+        U.tok_start = P.cu_seqlens[U.n];
+        U.L = P.cu_seqlens[U.n + 1] - U.tok_start;
+    }
+    U.nch = (U.L + kChunk - 1) / kChunk;
+    return U;
+}
+
+// Persistent calls: the CTA's k-th unit.  The loader takes the next unit of the whole
+// launch from a device counter (units in longest-first order, so this is list
+// scheduling, longest first), decodes it and publishes it in slot k of the unit ring;
+// every other warp copies it from there, so no role reads the sequence map itself.  A
+// slot is free again once every reader has copied it, so the loader can run at most
+// kUnitRing units ahead of the slowest role's current unit.  nch = -1: no more units.
+__device__ bool publish_unit(const Problem& P, const SeqMap& M, Smem& S, int k, int* err, Unit& U) {
+    const int slot = k % kUnitRing;
+    if (k >= kUnitRing &&
+        !mbar_wait(&S.unit_empty[slot], (unsigned)(((k / kUnitRing) - 1) & 1), err))
+        return false;
+    const int id = atomicAdd(M.counter, 1);
+    if (id < P.N * P.H) {
+        U = unit_at(P, M, id);
+    } else {
+        U = Unit{};
+        U.nch = -1;
+    }
+    volatile int* w = S.unit[slot];
+    w[0] = U.n;
+    w[1] = U.h;
+    w[2] = U.tok_start;
+    w[3] = U.L;
+    w[4] = U.nch;
+    w[5] = U.vzero;
+    mbar_arrive(&S.unit_full[slot]);   // release: the unit is visible to the readers
+    return U.nch >= 0;
+}
+// A reader's k-th unit; false: none, or a wait gave up.  whole_warp: all 32 lanes call it
+// and lane 0 releases the slot; otherwise the one calling thread does.
+__device__ bool read_unit(Smem& S, int k, int* err, bool whole_warp, Unit& U) {
+    const int slot = k % kUnitRing;
+    bool ok = mbar_wait(&S.unit_full[slot], (unsigned)((k / kUnitRing) & 1), err);
+    if (whole_warp) ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return false;
+    const volatile int* r = S.unit[slot];
+    U.n = r[0];
+    U.h = r[1];
+    U.tok_start = r[2];
+    U.L = r[3];
+    U.nch = r[4];
+    U.vzero = r[5] != 0;
+    if (whole_warp) __syncwarp();
+    if (!whole_warp || (threadIdx.x & 31) == 0) mbar_arrive(&S.unit_empty[slot]);
+    return U.nch >= 0;
+}
+
 // ---- raw-row loads on the TMA engine (one thread) ----------------------------------
 // Tensor maps over q, k, v, g viewed as [rows][H][128] bf16 (rows = B*T tokens).
 // Rows past the end of the tensor are zero-filled; rows past the end of a
@@ -291,12 +383,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-__device__ void loader(const RawMaps& TM, const Unit& U, Smem& S, int* err) {
+// One unit's chunks; g0 = this CTA's chunks before it (ring slots and barrier phases
+// continue across the units of a persistent CTA).  Returns the chunks issued.
+__device__ __forceinline__ int loader_unit(const RawMaps& TM, const Unit& U, Smem& S, int* err,
+                                           int g0) {
     const CUtensorMap* maps[4] = {&TM.q, &TM.k, U.vzero ? &TM.vz : &TM.v, &TM.g};
     int c = 0;   // chunks issued
     for (; c < U.nch; ++c) {
-        const int slot = c % kRaw;
-        if (c >= kRaw && !mbar_wait(&S.raw_empty[slot], (unsigned)(((c / kRaw) - 1) & 1), err))
+        const int g = g0 + c;
+        const int slot = g % kRaw;
+        if (g >= kRaw && !mbar_wait(&S.raw_empty[slot], (unsigned)(((g / kRaw) - 1) & 1), err))
             break;
         const uint32_t full = smem_u32(&S.raw_full[slot]);
         tc::mbar_arrive_expect_tx(full, kRawBytes);
@@ -309,18 +405,38 @@ __device__ void loader(const RawMaps& TM, const Unit& U, Smem& S, int* err) {
                 tma_load_3d(smem_u32(S.raw[slot].x[t][half]), maps[t], 64 * half, U.h,
                             t == 2 ? vrow : row, full);
     }
+    return c;
+}
+
+template <bool kP>
+__device__ void loader(const Problem& P, const SeqMap& M, const RawMaps& TM, const Unit& U0,
+                       Smem& S, int* err) {
+    int n = 0;   // chunks issued
+    if constexpr (!kP) {
+        n = loader_unit(TM, U0, S, err, 0);
+    } else {
+        for (int k = 0;; ++k) {
+            Unit U;
+            if (!publish_unit(P, M, S, k, err, U)) break;
+            const int done = loader_unit(TM, U, S, err, n);
+            n += done;
+            if (done < U.nch) break;   // a wait gave up
+        }
+    }
     // Do not let the CTA exit while copies it issued are still landing.  Each slot has at
     // most one copy in flight (the next one waits for raw_empty), so the last issues of
     // the slots are the only phases that may be pending; also after a wait gave up.
-    const int first = c > kRaw ? c - kRaw : 0;
-    for (int i = first; i < c; ++i)
+    const int first = n > kRaw ? n - kRaw : 0;
+    for (int i = first; i < n; ++i)
         mbar_wait(&S.raw_full[i % kRaw], (unsigned)((i / kRaw) & 1), err, KDA_DRAIN_LIMIT);
 }
 
 // ---- token-parallel stage: producer warp w, channels 16w .. 16w+15 ----------------
 // Lane (pi, j) = (lane & 7, lane >> 3) holds channels c0 = 16w + 2 pi, c0 + 1 over rows
 // 4j .. 4j+3 of the chunk.
-__device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lane, int* err) {
+// One unit's chunks (g0 as for the loader); false if a wait gave up.
+__device__ __forceinline__ bool produce_unit(const Problem& P, const Unit& U, Smem& S, int w, int lane,
+                                             int* err, int g0) {
     const int pi = lane & 7, j = lane >> 3;
     const int c0 = 16 * w + 2 * pi;
     const int r0 = 4 * j;
@@ -334,11 +450,12 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
     const int chunk16 = 2 * (w & 3) + (pi >> 2);
     const int inoff = 4 * (pi & 3);
     for (int c = 0; c < U.nch; ++c) {
+        const int g = g0 + c;
         {
             const int len = min(kChunk, U.L - c * kChunk);
-            const int rslot = c % kRaw;
-            bool ok = mbar_wait(&S.raw_full[rslot], (unsigned)((c / kRaw) & 1), err);
-            if (!__all_sync(0xffffffffu, ok)) return;
+            const int rslot = g % kRaw;
+            bool ok = mbar_wait(&S.raw_full[rslot], (unsigned)((g / kRaw) & 1), err);
+            if (!__all_sync(0xffffffffu, ok)) return false;
             uint32_t rq[4], rk[4], rv[4], rg[4];
             {
                 const RawSlot& R = S.raw[rslot];
@@ -362,10 +479,10 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
             // thread's generic-proxy reads before it, then release the slot.
             tc::fence_proxy_async_smem();
             mbar_arrive(&S.raw_empty[rslot]);
-            const int slot = c % kRing;
+            const int slot = g % kRing;
             Stage& st = S.st[slot];
-            if (c >= kRing) ok = mbar_wait(&S.empty[slot], (unsigned)(((c / kRing) - 1) & 1), err);
-            if (!__all_sync(0xffffffffu, ok)) return;
+            if (g >= kRing) ok = mbar_wait(&S.empty[slot], (unsigned)(((g / kRing) - 1) & 1), err);
+            if (!__all_sync(0xffffffffu, ok)) return false;
 
             // gates lower_bound * sigmoid(exp(A_log) (g + dt_bias)), base 2; rows past the
             // sequence end decay by nothing
@@ -400,12 +517,12 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
 
             // decay factors and operand tiles
             // the early slot of this parity: both A-product warps are done with chunk c - 2
-            if (c >= kEarly)
-                ok = mbar_wait(&S.e_free[c & 1], (unsigned)(((c - kEarly) >> 1) & 1), err);
-            if (!__all_sync(0xffffffffu, ok)) return;
+            if (g >= kEarly)
+                ok = mbar_wait(&S.e_free[g & 1], (unsigned)(((g - kEarly) >> 1) & 1), err);
+            if (!__all_sync(0xffffffffu, ok)) return false;
             unsigned char* x = reinterpret_cast<unsigned char*>(st.x);
-            unsigned char* kge = reinterpret_cast<unsigned char*>(S.early[c & 1].kg);
-            unsigned char* ki = reinterpret_cast<unsigned char*>(S.early[c & 1].ki);
+            unsigned char* kge = reinterpret_cast<unsigned char*>(S.early[g & 1].kg);
+            unsigned char* ki = reinterpret_cast<unsigned char*>(S.early[g & 1].ki);
             float kd0[4], kd1[4];
             __half v0[4], v1[4];
 #pragma unroll
@@ -449,6 +566,23 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
             mbar_arrive(&S.kq_ready[slot]);
         }
     }
+    return true;
+}
+
+template <bool kP>
+__device__ void produce(const Problem& P, const SeqMap& M, const Unit& U0, Smem& S, int w, int lane,
+                        int* err) {
+    if constexpr (!kP) {
+        produce_unit(P, U0, S, w, lane, err, 0);
+    } else {
+        int g = 0;
+        for (int k = 0;; ++k) {
+            Unit U;
+            if (!read_unit(S, k, err, true, U)) return;
+            if (!produce_unit(P, U, S, w, lane, err, g)) return;
+            g += U.nch;
+        }
+    }
 }
 
 // ---- decay-ratio products (A-product warps) ----------------------------------------
@@ -457,18 +591,20 @@ __device__ void produce(const Problem& P, const Unit& U, Smem& S, int w, int lan
 // swizzled operand tiles (an 8 x 8 b16 matrix = 8 rows x 4 fp32).  Four independent
 // accumulators per warp (two n-tiles x two channel halves) keep the MMA chains short;
 // the halves are added in a fixed order.
-__device__ void aprod(const Unit& U, Smem& S, int which, int lane, int* err) {
+__device__ __forceinline__ bool aprod_unit(const Unit& U, Smem& S, int which, int lane, int* err,
+                                           int g0) {
     ProdShared& PS = S.pr;
     const int g = lane >> 2, t = lane & 3;
     const int m = lane >> 3, i8 = lane & 7;   // ldmatrix: matrix and row this lane addresses
 
     for (int c = 0; c < U.nch; ++c) {
-        const int par = c & 1, slot = c % kRing;
-        bool ok = mbar_wait(&S.kq_ready[slot], (unsigned)((c / kRing) & 1), err);
-        // A_kk buffer of this parity: the solver is done with chunk c - 2
-        if (which == 0 && c >= 2)
-            ok = ok && mbar_wait(&S.t_ready[(c - 2) % kRing], (unsigned)(((c - 2) / kRing) & 1), err);
-        if (!__all_sync(0xffffffffu, ok)) return;
+        const int ck = g0 + c;   // chunk of the CTA
+        const int par = ck & 1, slot = ck % kRing;
+        bool ok = mbar_wait(&S.kq_ready[slot], (unsigned)((ck / kRing) & 1), err);
+        // A_kk buffer of this parity: the solver is done with the chunk two before
+        if (which == 0 && ck >= 2)
+            ok = ok && mbar_wait(&S.t_ready[(ck - 2) % kRing], (unsigned)(((ck - 2) / kRing) & 1), err);
+        if (!__all_sync(0xffffffffu, ok)) return false;
         Stage& st = S.st[slot];
         // A operand: K 2^G (early slot) or Q 2^G (rows 0-15 of the x tile)
         const unsigned char* xa = which ? reinterpret_cast<const unsigned char*>(st.x)
@@ -517,17 +653,36 @@ __device__ void aprod(const Unit& U, Smem& S, int which, int lane, int* err) {
             mbar_arrive(&S.a_ready[par]);
         }
     }
+    return true;
+}
+
+template <bool kP>
+__device__ void aprod(const Problem& P, const SeqMap& M, const Unit& U0, Smem& S, int which, int lane,
+                      int* err) {
+    if constexpr (!kP) {
+        aprod_unit(U0, S, which, lane, err, 0);
+    } else {
+        int g = 0;
+        for (int k = 0;; ++k) {
+            Unit U;
+            if (!read_unit(S, k, err, true, U)) return;
+            if (!aprod_unit(U, S, which, lane, err, g)) return;
+            g += U.nch;
+        }
+    }
 }
 
 // ---- w warps: -w = -T diag(b)(K 2^G) for channels 64 which .. + 63 -------------------
 // fp16 m16n8k16 MMAs: A = T diag(b) (row-major fp16), B = K 2^G (fp16 [token][channel]);
 // the result, negated and rounded to tf32, fills rows 16-31 of the x tile.
-__device__ void wcalc(const Unit& U, Smem& S, int which, int lane, int* err) {
+__device__ __forceinline__ bool wcalc_unit(const Unit& U, Smem& S, int which, int lane, int* err,
+                                           int g0) {
     const int g = lane >> 2, t = lane & 3;
     for (int c = 0; c < U.nch; ++c) {
-        const int slot = c % kRing;
-        const bool ok = mbar_wait(&S.t_ready[slot], (unsigned)((c / kRing) & 1), err);
-        if (!__all_sync(0xffffffffu, ok)) return;
+        const int ck = g0 + c;   // chunk of the CTA
+        const int slot = ck % kRing;
+        const bool ok = mbar_wait(&S.t_ready[slot], (unsigned)((ck / kRing) & 1), err);
+        if (!__all_sync(0xffffffffu, ok)) return false;
         Stage& st = S.st[slot];
         unsigned char* x = reinterpret_cast<unsigned char*>(st.x);
         uint32_t ta[4];
@@ -553,6 +708,23 @@ __device__ void wcalc(const Unit& U, Smem& S, int which, int lane, int* err) {
         }
         tc::fence_proxy_async_smem();   // -w is read by the chain's MMA
         mbar_arrive(&S.full[slot]);
+    }
+    return true;
+}
+
+template <bool kP>
+__device__ void wcalc(const Problem& P, const SeqMap& M, const Unit& U0, Smem& S, int which, int lane,
+                      int* err) {
+    if constexpr (!kP) {
+        wcalc_unit(U0, S, which, lane, err, 0);
+    } else {
+        int g = 0;
+        for (int k = 0;; ++k) {
+            Unit U;
+            if (!read_unit(S, k, err, true, U)) return;
+            if (!wcalc_unit(U, S, which, lane, err, g)) return;
+            g += U.nch;
+        }
     }
 }
 
@@ -632,7 +804,8 @@ __device__ __noinline__ void solve_substitution(const float* akk, float bl, int 
     }
 }
 
-__device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* err) {
+__device__ __forceinline__ bool solve_unit(const Problem& P, const Unit& U, Smem& S, int lane, int* err,
+                                           int g0) {
     ProdShared& PS = S.pr;
     const int g = lane >> 2, t = lane & 3;
     // beta logits in windows of 64 tokens (4 chunks), the next window loaded one
@@ -655,10 +828,11 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
         const float lw = __shfl_sync(0xffffffffu, (c & 2) ? bw1 : bw0, 16 * (c & 1) + (lane & 15));
         // b of row `lane & 15`; rows past the sequence end get b = 0 (their T row is e_i)
         const float bl = ((lane & 15) < len) ? sigmoid_fast(lw) : 0.0f;
-        const int par = c & 1;
-        const bool ok = mbar_wait(&S.a_ready[par], (unsigned)((c >> 1) & 1), err);
-        if (!__all_sync(0xffffffffu, ok)) return;
-        Stage& st = S.st[c % kRing];
+        const int ck = g0 + c;   // chunk of the CTA
+        const int par = ck & 1;
+        const bool ok = mbar_wait(&S.a_ready[par], (unsigned)((ck >> 1) & 1), err);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        Stage& st = S.st[ck % kRing];
         const float* akk = PS.Akk[par];
         unsigned char* tbt = reinterpret_cast<unsigned char*>(st.tbt);
         // A = diag(b) A_kk strictly lower, in accumulator layout (rows g, g + 8; columns
@@ -730,7 +904,23 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
-        mbar_arrive(&S.t_ready[c % kRing]);
+        mbar_arrive(&S.t_ready[ck % kRing]);
+    }
+    return true;
+}
+
+template <bool kP>
+__device__ void solve(const Problem& P, const SeqMap& M, const Unit& U0, Smem& S, int lane, int* err) {
+    if constexpr (!kP) {
+        solve_unit(P, U0, S, lane, err, 0);
+    } else {
+        int g = 0;
+        for (int k = 0;; ++k) {
+            Unit U;
+            if (!read_unit(S, k, err, true, U)) return;
+            if (!solve_unit(P, U, S, lane, err, g)) return;
+            g += U.nch;
+        }
     }
 }
 
@@ -743,7 +933,10 @@ __device__ void solve(const Problem& P, const Unit& U, Smem& S, int lane, int* e
 //                                              epilogue into the other state buffer)
 //   O    += U^T A_qk^T
 // The state and U are read from tensor memory as fp32 A operands (kind::tf32).
-__device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
+// One unit's chunks; g0 as for the loader, ui = this CTA's units with tokens before it.
+// Returns the chunks whose MMAs and commits were all issued (fewer if a wait gave up).
+__device__ __forceinline__ int mma_unit(const Unit& U, Smem& S, uint32_t tmem, int* err, int g0,
+                                        int ui) {
     constexpr uint32_t id_u = tc::idesc_f16_f32(128, 16);
     constexpr uint32_t id_s = tc::idesc_tf32_f32(128, 32);
     constexpr uint32_t id_k = tc::idesc_tf32_f32(128, 128);
@@ -756,16 +949,17 @@ __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
     const uint64_t d_aqk = tc::smem_desc(smem_u32(S.st[0].aqk), 128, AQ_SBO, tc::kSwizzleNone);
     int c = 0;
     for (; c < U.nch; ++c) {
-        const int slot = c % kRing;
+        const int g = g0 + c;   // chunk of the CTA (the state and [O|U] buffers go by c)
+        const int slot = g % kRing;
         const uint64_t so = (uint64_t)((slot * sizeof(Stage)) >> 4);
         const uint32_t sc = tmem + TM_S + 128u * (c & 1);
         const uint32_t sn = tmem + TM_S + 128u * ((c + 1) & 1);
         const uint32_t uo = tmem + TM_UO + 32u * (c % 3);
-        if (!mbar_wait(&S.full[slot], (unsigned)((c / kRing) & 1), err)) break;
+        if (!mbar_wait(&S.full[slot], (unsigned)((g / kRing) & 1), err)) break;
         if (c == 0) {
-            if (!mbar_wait(&S.init_ready, 0u, err)) break;
+            if (!mbar_wait(&S.init_ready, (unsigned)(ui & 1), err)) break;
         } else {
-            if (!mbar_wait(&S.s_done, (unsigned)((c - 1) & 1), err)) break;
+            if (!mbar_wait(&S.s_done, (unsigned)((g - 1) & 1), err)) break;
         }
         tc::fence_after_sync();
         // [O|U] = S^T [Q 2^G ; -w]^T over the 16 key-channel steps (the first one starts
@@ -780,7 +974,7 @@ __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
         // one wait for both the [O|U] MMAs and the epilogue's rescale: a wait costs
         // this thread ~100 cycles even on a completed barrier
         tc::commit(smem_u32(&S.scaled));
-        if (!mbar_wait(&S.scaled, (unsigned)(c & 1), err)) {
+        if (!mbar_wait(&S.scaled, (unsigned)(g & 1), err)) {
             // the [O|U] MMAs of this chunk were issued and committed: drain them below
             break;
         }
@@ -792,6 +986,26 @@ __device__ void mma_issuer(const Unit& U, Smem& S, uint32_t tmem, int* err) {
         }
         tc::commit(smem_u32(&S.s_done));
         tc::commit(smem_u32(&S.empty[slot]));
+    }
+    return c;
+}
+
+template <bool kP>
+__device__ void mma_issuer(const Problem& P, const SeqMap& M, const Unit& U0, Smem& S,
+                           uint32_t tmem, int* err) {
+    int c = 0;   // chunks of this CTA whose commits were all issued
+    if constexpr (!kP) {
+        c = mma_unit(U0, S, tmem, err, 0, 0);
+    } else {
+        int ui = 0;
+        for (int k = 0;; ++k) {
+            Unit U;
+            if (!read_unit(S, k, err, false, U)) break;
+            const int done = mma_unit(U, S, tmem, err, c, ui);
+            c += done;
+            if (done < U.nch) break;   // a wait gave up
+            if (U.nch > 0) ++ui;
+        }
     }
     // Every MMA this thread issued completes before the CTA goes on to release tensor
     // memory and exit, also after a wait gave up part-way through a chunk: one more
@@ -839,8 +1053,9 @@ __device__ __forceinline__ void scale32(uint32_t (&x)[32], const float* gc) {
     }
 }
 
-__device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem, int ew,
-                         int lane, int* err) {
+// One unit; g0 as for the loader.  Returns false if a wait gave up.
+__device__ __forceinline__ bool epilogue_unit(const Problem& P, const Unit& U, Smem& S,
+                                              uint32_t tmem, int ew, int lane, int* err, int g0) {
     const int v = 32 * ew + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * ew) << 16);   // this warp's lane quarter
     const size_t sbase = ((size_t)U.n * P.H + U.h) * kDim * kDim + v;   // + c * kDim
@@ -851,7 +1066,7 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
             for (int c = 0; c < kDim; ++c)
                 state_out(P, sbase + (size_t)c * kDim,
                           P.init_state ? state_in(P, sbase + (size_t)c * kDim) : 0.0f);
-        return;
+        return true;
     }
     // initial state S0 into buffer 0, then S0 Diag(2^G_last of chunk 0) into buffer 1
 #pragma unroll 1
@@ -867,14 +1082,14 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
     tc::wait_st();
     tc::fence_before_sync();
     mbar_arrive(&S.init_ready);
-    ok = mbar_wait(&S.full[0], 0u, err);
-    if (!__all_sync(0xffffffffu, ok)) return;
+    ok = mbar_wait(&S.full[g0 % kRing], (unsigned)((g0 / kRing) & 1), err);
+    if (!__all_sync(0xffffffffu, ok)) return false;
 #pragma unroll 1
     for (int piece = 0; piece < 4; ++piece) {
         uint32_t x[32];
         tc::ld32(tl + TM_S + 32 * piece, x);
         tc::wait_ld();
-        scale32(x, S.st[0].gc + 32 * piece);
+        scale32(x, S.st[g0 % kRing].gc + 32 * piece);
         tc::st32(tl + TM_S + 128 + 32 * piece, x);
     }
     tc::wait_st();
@@ -882,15 +1097,15 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
     mbar_arrive(&S.scaled);
 
     // slot / phase of chunk c in the operand ring, and the [O|U] buffer of chunk c - 1
-    int slot = 1 % kRing, phase = (1 / kRing) & 1, uob = 0;
+    int slot = (g0 + 1) % kRing, phase = ((g0 + 1) / kRing) & 1, uob = 0;
     __nv_bfloat16* out = P.out + ((size_t)U.tok_start * P.H + U.h) * kDim + v;
     const size_t out_step = (size_t)P.H * kDim;   // elements between consecutive tokens
     for (int c = 1; c <= U.nch; ++c) {
         // chunk c - 1 finished: its end state is in buffer c & 1
-        ok = mbar_wait(&S.s_done, (unsigned)((c - 1) & 1), err);
+        ok = mbar_wait(&S.s_done, (unsigned)((g0 + c - 1) & 1), err);
         const bool more = c < U.nch;
         if (more) ok = ok && mbar_wait(&S.full[slot], (unsigned)phase, err);
-        if (!__all_sync(0xffffffffu, ok)) return;
+        if (!__all_sync(0xffffffffu, ok)) return false;
         tc::fence_after_sync();
         const uint32_t sc = tl + TM_S + 128u * (c & 1);
         if (more) {
@@ -935,8 +1150,29 @@ __device__ void epilogue(const Problem& P, const Unit& U, Smem& S, uint32_t tmem
         }
         if (++uob == 3) uob = 0;
     }
+    return true;
 }
 
+template <bool kP>
+__device__ void epilogue(const Problem& P, const SeqMap& M, const Unit& U0, Smem& S, uint32_t tmem,
+                         int ew, int lane, int* err) {
+    if constexpr (!kP) {
+        epilogue_unit(P, U0, S, tmem, ew, lane, err, 0);
+    } else {
+        int g = 0;
+        for (int k = 0;; ++k) {
+            Unit U;
+            if (!read_unit(S, k, err, true, U)) return;
+            if (!epilogue_unit(P, U, S, tmem, ew, lane, err, g)) return;
+            g += U.nch;
+        }
+    }
+}
+
+// kP: persistent (a grid of at most one CTA per SM takes the units from a device
+// counter, longest first); otherwise one CTA per unit.  Every unit's arithmetic is the
+// same either way.
+template <bool kP>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_kernel(Problem P, SeqMap M, const __grid_constant__ RawMaps TM, int* err) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -946,37 +1182,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     Unit U;
-    U.h = blockIdx.x % P.H;
-    const int rank = blockIdx.x / P.H;
-    U.vzero = false;
-    if (P.window >= 0) {
-        // sequence split (fixed length): the unit's sequence, segment and kind.  Its
-        // initial state (prepared on the host side: the caller's, zero or identity) and
-        // its final state are at index rank of fp32 scratch.
-        const int per = P.window == 0 ? 2 * P.nseg - 3 : P.nseg - 1;
-        const int seq = rank / per, vj = rank % per;
-        int j = P.window == 0 ? vj : vj + 1;      // segment
-        if (P.window == 0 && vj > P.nseg - 2) {
-            j = vj - (P.nseg - 2);                // transition operator: zero values
-            U.vzero = true;
-        }
-        U.n = rank;
-        const long long nchk = (P.T + kChunk - 1) / kChunk;
-        const int c0 = (int)((long long)j * nchk / P.nseg);
-        const int c1 = (int)((long long)(j + 1) * nchk / P.nseg);
-        U.tok_start = seq * P.T + c0 * kChunk;
-        U.L = min(c1 * kChunk, P.T) - c0 * kChunk;
-    } else if (P.cu_seqlens == nullptr) {
-        U.n = rank;
-        U.tok_start = rank * P.T;
-        U.L = P.T;
-    } else {
+    if constexpr (kP) {
         if (!*M.valid) return;  // malformed cu_seqlens: write nothing (CTA-uniform)
-        U.n = M.seq_order[rank];
-        U.tok_start = P.cu_seqlens[U.n];
-        U.L = P.cu_seqlens[U.n + 1] - U.tok_start;
+        U = Unit{};
+    } else {
+        U.h = blockIdx.x % P.H;
+        const int rank = blockIdx.x / P.H;
+        U.vzero = false;
+        if (P.window >= 0) {
+            // sequence split (fixed length): the unit's sequence, segment and kind.  Its
+            // initial state (prepared on the host side: the caller's, zero or identity) and
+            // its final state are at index rank of fp32 scratch.
+            const int per = P.window == 0 ? 2 * P.nseg - 3 : P.nseg - 1;
+            const int seq = rank / per, vj = rank % per;
+            int j = P.window == 0 ? vj : vj + 1;      // segment
+            if (P.window == 0 && vj > P.nseg - 2) {
+                j = vj - (P.nseg - 2);                // transition operator: zero values
+                U.vzero = true;
+            }
+            U.n = rank;
+            const long long nchk = (P.T + kChunk - 1) / kChunk;
+            const int c0 = (int)((long long)j * nchk / P.nseg);
+            const int c1 = (int)((long long)(j + 1) * nchk / P.nseg);
+            U.tok_start = seq * P.T + c0 * kChunk;
+            U.L = min(c1 * kChunk, P.T) - c0 * kChunk;
+        } else if (P.cu_seqlens == nullptr) {
+            U.n = rank;
+            U.tok_start = rank * P.T;
+            U.L = P.T;
+        } else {
+            if (!*M.valid) return;  // malformed cu_seqlens: write nothing (CTA-uniform)
+            U.n = M.seq_order[rank];
+            U.tok_start = P.cu_seqlens[U.n];
+            U.L = P.cu_seqlens[U.n + 1] - U.tok_start;
+        }
+        U.nch = (U.L + kChunk - 1) / kChunk;
     }
-    U.nch = (U.L + kChunk - 1) / kChunk;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRing; ++s) {
@@ -998,6 +1239,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&S.raw_full[s], 1);                 // loader's arrive + TMA bytes
             mbar_init(&S.raw_empty[s], kProdThreads);     // every producer thread
         }
+        if (kP) {
+            for (int s = 0; s < kUnitRing; ++s) {
+                mbar_init(&S.unit_full[s], 1);               // the loader
+                mbar_init(&S.unit_empty[s], kUnitReaders);   // one arrival per reading warp
+            }
+        }
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     tc::fence_proxy_async_smem();
@@ -1012,11 +1259,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const Role role = role_of(warp);
     if (role == kEpi) {
-        epilogue(P, U, S, tmem, warp, lane, err);
+        epilogue<kP>(P, M, U, S, tmem, warp, lane, err);
         tc::fence_before_sync();
         mbar_arrive(&S.epi_done);
     } else if (role == kMma) {
-        if (lane == 0) mma_issuer(U, S, tmem, err);
+        if (lane == 0) mma_issuer<kP>(P, M, U, S, tmem, err);
         __syncwarp();
         // free tensor memory once the epilogue is done with it (after a timeout the
         // epilogue stops at its next wait, so a longer limit than a pipeline wait's)
@@ -1026,21 +1273,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     } else if (role == kSolve) {
-        solve(P, U, S, lane, err);
+        solve<kP>(P, M, U, S, lane, err);
     } else if (role == kAprod0 || role == kAprod1) {
-        aprod(U, S, role == kAprod1, lane, err);
+        aprod<kP>(P, M, U, S, role == kAprod1, lane, err);
     } else if (role == kW0 || role == kW1) {
-        wcalc(U, S, role == kW1, lane, err);
+        wcalc<kP>(P, M, U, S, role == kW1, lane, err);
     } else if (role == kLoad) {
-        if (lane == 0) loader(TM, U, S, err);
+        if (lane == 0) loader<kP>(P, M, TM, U, S, err);
     } else {
-        produce(P, U, S, prod_index(warp), lane, err);
+        produce<kP>(P, M, U, S, prod_index(warp), lane, err);
     }
 }
 
 // per-device flag: the kernel attribute below is set once (setting it is idempotent,
 // so two threads racing on a first call both succeed)
 std::atomic<bool> g_attr_set[64];
+std::atomic<int> g_sms[64];   // SM count per device, 0 until read
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -1077,14 +1325,24 @@ cudaError_t launch_fused(const Problem& P, const SeqMap& M, int* err, cudaStream
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !g_attr_set[dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(fused_kernel,
+        cudaError_t e = cudaFuncSetAttribute(fused_kernel<false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fused_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_sms[dev].store(sms, std::memory_order_relaxed);
         g_attr_set[dev].store(true, std::memory_order_release);
     }
     const long long per = P.window == 0 ? 2LL * P.nseg - 3 : P.window == 1 ? P.nseg - 1LL : 1LL;
     const long long ctas = (long long)P.N * P.H * per;
     if (ctas == 0) return cudaSuccess;
+    // more varlen units than SMs, and a unit counter given: one persistent CTA per SM
+    const int sms = (dev >= 0 && dev < 64) ? g_sms[dev].load(std::memory_order_relaxed) : 0;
+    const bool persist = P.cu_seqlens != nullptr && M.counter != nullptr && sms > 0 && ctas > sms;
     // total token rows: B*T (fixed length, N = B sequences of T) or T (varlen, B = 1)
     const long long rows = (P.cu_seqlens == nullptr) ? (long long)P.N * P.T : (long long)P.T;
     RawMaps TM;
@@ -1098,7 +1356,10 @@ cudaError_t launch_fused(const Problem& P, const SeqMap& M, int* err, cudaStream
         if (e == cudaSuccess) e = encode_rows(&TM.g, P.g, P.H, rows);
         if (e != cudaSuccess) return e;
     }   // else no tokens: the loader issues nothing
-    fused_kernel<<<(unsigned)ctas, kThreads, smem, s>>>(P, M, TM, err);
+    if (persist)
+        fused_kernel<true><<<(unsigned)sms, kThreads, smem, s>>>(P, M, TM, err);
+    else
+        fused_kernel<false><<<(unsigned)ctas, kThreads, smem, s>>>(P, M, TM, err);
     return cudaGetLastError();
 }
 

@@ -75,6 +75,7 @@ struct RawMaps {
 struct SeqMap {
     int* seq_order;     // [N] sequences, longest first
     int* valid;         // [1] 1 if cu_seqlens passed validation
+    int* counter = nullptr;   // [1] next unit of a persistent launch (zeroed by the map)
 };
 
 // Device error word helpers.

@@ -133,7 +133,10 @@ __global__ void __launch_bounds__(kThreads) seqmap_kernel(Problem P, SeqMap M, i
         for (int n = threadIdx.x; n < N; n += kThreads)
             M.seq_order[n] = (int)(keys[n] & 0xFFFFFFFFull);
     }
-    if (threadIdx.x == 0) *M.valid = 1;
+    if (threadIdx.x == 0) {
+        *M.valid = 1;
+        if (M.counter) *M.counter = 0;   // the fused kernel's persistent CTAs count from 0
+    }
 }
 
 // per-device flag: the kernel attribute below is set once (setting it is idempotent,

@@ -104,8 +104,13 @@ typedef enum {
  * q, k, v, g and out must be 16-byte aligned; out must not overlap any input.
  * kda_fwd is kda_fwd_segments with num_segments = 0: a long fixed-length call
  * whose B*H recurrences leave most SMs idle is cut into segments that run side
- * by side (see kda_fwd_segments); other calls run one pass.  Varlen calls take
- * kda_fwd_workspace_bytes() of scratch (the longest-first sequence order), and
+ * by side (see kda_fwd_segments); other calls run one pass.  A varlen call with
+ * more (sequence, head) recurrences than SMs, whose sequences average at most 256
+ * tokens, runs one persistent CTA per SM that takes the recurrences longest first
+ * from a device counter and carries its pipeline from one to the next (results
+ * bit-identical to one CTA per recurrence).  Varlen calls take
+ * kda_fwd_workspace_bytes() of scratch (the longest-first sequence order, a
+ * validity flag and that counter), and
  * split calls that many bytes of fp32 segment states, from the stream-ordered
  * allocator (cudaMallocAsync / cudaFreeAsync on `stream`); one-pass
  * fixed-length calls take none.  The call does not synchronise.  The first call on a device

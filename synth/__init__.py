@@ -51,7 +51,7 @@ class Workload:
     B: int = 1
     K: int = 128
     V: int = 128
-    lengths: str | None = None  # None = fixed length; "mixed12" or "uniform8x1024"
+    lengths: str | None = None  # None = fixed length; "mixed12", "uniform8x1024", "short20000"
     init_dtype: str | None = None   # None, "bf16" or "f32"
     final_dtype: str | None = "f32"
     carry_calls: int = 1        # >1: the sequence is processed in this many calls
@@ -79,7 +79,25 @@ WORKLOADS = {
     "carry_t65536_h32": Workload(
         "carry_t65536_h32", T=65536, H=32, carry_calls=2,
         description="B=1 T=65536 H=32 as two 32768-token calls carrying an fp32 state"),
+    "varlen_short_20000_h16": Workload(
+        "varlen_short_20000_h16", T=160000, H=16, lengths="short20000", final_dtype=None,
+        description="20,000 sequences of 0-16 tokens (uniform, summing to 160,000) "
+                    "packed, H=16, no states: many short prompts in one call"),
 }
+
+
+def short_lengths(rng: np.random.Generator, n: int = 20000, total: int = 160000,
+                  hi: int = 16) -> np.ndarray:
+    """n lengths uniform in [0, hi], then moved one token at a time (a random sequence
+    that still has room) until they sum to ``total``."""
+    lens = rng.integers(0, hi + 1, size=n).astype(np.int64)
+    while lens.sum() != total:
+        i = int(rng.integers(n))
+        if lens.sum() < total and lens[i] < hi:
+            lens[i] += 1
+        elif lens.sum() > total and lens[i] > 0:
+            lens[i] -= 1
+    return lens
 
 
 def mixed_lengths(rng: np.random.Generator, n: int = 12, total: int = 8192,
@@ -142,7 +160,7 @@ def make_inputs(B: int, T: int, H: int, K: int = 128, V: int = 128, seed: int = 
         N = B
     elif isinstance(lengths, str):
         assert B == 1
-        N = {"mixed12": 12, "uniform8x1024": 8}[lengths]
+        N = {"mixed12": 12, "uniform8x1024": 8, "short20000": 20000}[lengths]
     else:
         assert B == 1
         N = len(lengths)
@@ -164,6 +182,8 @@ def make_inputs(B: int, T: int, H: int, K: int = 128, V: int = 128, seed: int = 
     elif lengths == "uniform8x1024":
         assert T % N == 0
         cu = cu_from_lengths(np.full(N, T // N, np.int64))
+    elif lengths == "short20000":
+        cu = cu_from_lengths(short_lengths(rng, n=N, total=T))
     elif lengths is not None:
         cu = cu_from_lengths(lengths)
         assert int(cu[-1]) == T

@@ -371,3 +371,44 @@ def test_profile_counts_launches():
     kda.kda_profile_enable(False)
     assert prof["seqmap_kernel"][1] == 2 and prof["fused_kernel"][1] == 2
     assert all(ms > 0 for ms, n in prof.values() if n)
+
+
+@pytest.mark.parametrize("N,H,lo,hi", [(2000, 2, 0, 40), (300, 3, 100, 400), (160, 1, 0, 0)])
+def test_persistent_schedule_equals_one_cta_per_unit(N, H, lo, hi):
+    """Varlen calls with more (sequence, head) units than SMs run persistent CTAs that
+    take units from a device counter, longest first, with their pipelines carried from
+    unit to unit; kda_fwd_noalloc always runs one CTA per unit.  The arithmetic of every
+    unit is the same, so the results are bit-identical (here with empty sequences, one
+    chunk, many chunks, ragged ends, and a call of empty sequences only)."""
+    import torch
+    import gated_delta_rule_39_gb300 as kda
+    rng = np.random.default_rng(N + H)
+    lens = [int(x) for x in rng.integers(lo, hi + 1, size=N)]
+    T = sum(lens)
+    d = synth.make_inputs(1, T, H, seed=N, lengths=lens, init_dtype="f32")
+    x = upload(d)
+    res = []
+    for fn in (kda.kda_fwd, kda.kda_fwd_noalloc):
+        out = torch.full((1, T, H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        fs = torch.full((N, H, 128, 128), float("nan"), device="cuda")
+        fn(x["q"], x["k"], x["v"], x["g"], x["beta"], d["scale"], out, x["A_log"], x["dt_bias"],
+           d["lower_bound"], initial_state=x["initial_state"], final_state=fs,
+           cu_seqlens=x["cu_seqlens"])
+        torch.cuda.synchronize()
+        assert kda.kda_fwd_get_error() == 0
+        res.append((out, fs))
+    assert torch.equal(res[0][0], res[1][0]) or T == 0
+    assert torch.equal(res[0][1], res[1][1])
+    if T > 0 and N * H <= 900:
+        ro, rs = run_oracle(d)
+        e = out_error(to_f64(res[0][0]), ro)
+        assert e["ok"], e
+        assert state_error(to_f64(res[0][1]), rs)["ok"]
+
+
+def test_varlen_short_20000_sampled_heads():
+    """The many-short-prompts workload at full size (20,000 sequences of 0-16 tokens,
+    16 heads, 320,000 units: the persistent schedule) against the oracle on three
+    heads, every sequence of each."""
+    d = synth.make_workload("varlen_short_20000_h16")
+    _check(d, heads=[0, 7, 15], final_dtype=None, tag="short20000")

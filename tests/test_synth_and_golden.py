@@ -69,3 +69,13 @@ def test_golden_fixture_matches_oracle():
             assert out[int(r[1]), int(r[2])] == pytest.approx(float(r[3]), rel=1e-12, abs=1e-15)
         elif r[0] == "state":
             assert S[int(r[1]), int(r[2])] == pytest.approx(float(r[3]), rel=1e-12, abs=1e-15)
+
+
+def test_short_lengths_recipe():
+    """20,000 lengths in [0, 16] summing to 160,000, the same for the same seed."""
+    a = synth.short_lengths(np.random.default_rng(5))
+    b = synth.short_lengths(np.random.default_rng(5))
+    assert a.shape == (20000,) and a.sum() == 160000
+    assert a.min() >= 0 and a.max() <= 16 and (a == 0).any() and (a == 16).any()
+    assert np.array_equal(a, b)
+    assert synth.WORKLOADS["varlen_short_20000_h16"].final_dtype is None
