@@ -17,6 +17,11 @@ Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``)
     point symmetry and its monotonicity.
   * ``kda_fwd`` -- ``kda_gate`` + sigmoid(beta) + ``kda_recurrence``; pinned by
     equality with those pieces called separately.
+  * ``kda_bwd`` (``kda_oracle_bwd.c``, a library of its own) -- the reverse
+    pass of ``kda_fwd``; pinned by central finite differences of ``kda_fwd``
+    along random directions of every input, element-wise differences on small
+    sizes, and equality with PyTorch autograd through an independently written
+    fp64 token recurrence (``tests/test_oracle_bwd.py``).
   * equality of the oracle's numbers with FlashKDA's own kernel outputs:
     parity unpinned (the pages print no output values).
 
@@ -36,7 +41,10 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kda_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "_build", "libkda_oracle.so")
+_BWD_SRC = os.path.join(_HERE, "kda_oracle_bwd.c")
+_BWD_LIB_PATH = os.path.join(_HERE, "_build", "libkda_oracle_bwd.so")
 _lib = None
+_bwd_lib = None
 
 _dp = ctypes.POINTER(ctypes.c_double)
 _lp = ctypes.POINTER(ctypes.c_long)
@@ -201,6 +209,63 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"kda_oracle_recurrence rejected its arguments (code {rc})")
         return out, Sf
+
+
+def build_bwd(force: bool = False) -> str:
+    """Compile the backward oracle ``kda_oracle_bwd.c`` (same flags as the forward)."""
+    return build(force=force, src=_BWD_SRC, out=_BWD_LIB_PATH)
+
+
+def kda_bwd(q, k, v, g, beta, scale: float, A_log, dt_bias, lower_bound: float, dout,
+            initial_state=None, dfinal=None, cu_seqlens=None, heads=None, n_threads=None):
+    """Gradients of a loss L = sum(dout * out) + sum(dfinal * final_state) of ``kda_fwd``
+    in fp64.  Shapes as ``kda_fwd``; dout [B, T, H, V]; dfinal optional [N, H, K, V].
+    Returns a dict: dq, dk, dg [B, T, H, K]; dv [B, T, H, V]; dbeta [B, T, H];
+    dA_log [H]; dt_bias [H, K] (as "ddt_bias"); d_initial_state [N, H, K, V] (the
+    gradient with respect to the initial state, also when none was given: zero).
+    Entries of heads outside ``heads`` are NaN (dA_log, ddt_bias: 0)."""
+    global _bwd_lib
+    if _bwd_lib is None:
+        lib = ctypes.CDLL(build_bwd())
+        lib.kda_oracle_bwd.restype = ctypes.c_int
+        lib.kda_oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_double, _dp, _dp,
+                                       ctypes.c_double, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
+                                       _dp, _dp, _dp, _dp, _lp, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, _ip, ctypes.c_int,
+                                       ctypes.c_int]
+        _bwd_lib = lib
+    q64, k64, v64, g64, b64, do64 = (_f64(x) for x in (q, k, v, g, beta, dout))
+    B, T, H, K = q64.shape
+    V = v64.shape[-1]
+    assert k64.shape == q64.shape and g64.shape == q64.shape
+    assert v64.shape == (B, T, H, V) and b64.shape == (B, T, H) and do64.shape == v64.shape
+    if cu_seqlens is not None:
+        assert B == 1
+    ss, N = _seq_start(B * T, cu_seqlens, B)
+    hsel, nsel = _heads(heads, H)
+    S0 = _f64(initial_state)
+    dST = _f64(dfinal)
+    for x in (S0, dST):
+        if x is not None:
+            assert x.shape == (N, H, K, V)
+    r = {"dq": np.full((B, T, H, K), np.nan), "dk": np.full((B, T, H, K), np.nan),
+         "dg": np.full((B, T, H, K), np.nan), "dv": np.full((B, T, H, V), np.nan),
+         "dbeta": np.full((B, T, H), np.nan), "d_initial_state": np.full((N, H, K, V), np.nan)}
+    dA_u = np.zeros((N, H))
+    ddt_u = np.zeros((N, H, K))
+    A = _f64(A_log)
+    dtb = _f64(dt_bias)
+    rc = _bwd_lib.kda_oracle_bwd(
+        _ptr(q64), _ptr(k64), _ptr(v64), _ptr(g64), _ptr(b64), float(scale), _ptr(A), _ptr(dtb),
+        float(lower_bound), _ptr(S0), _ptr(do64), _ptr(dST), _ptr(r["dq"]), _ptr(r["dk"]),
+        _ptr(r["dv"]), _ptr(r["dg"]), _ptr(r["dbeta"]), _ptr(dA_u), _ptr(ddt_u),
+        _ptr(r["d_initial_state"]), _ptr(ss, _lp), N, H, K, V, _ptr(hsel, _ip), nsel,
+        n_threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"kda_oracle_bwd rejected its arguments (code {rc})")
+    r["dA_log"] = dA_u.sum(axis=0)
+    r["ddt_bias"] = ddt_u.sum(axis=0)
+    return r
 
 
 def get() -> Oracle:
