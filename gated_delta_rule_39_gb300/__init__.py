@@ -14,7 +14,7 @@ import ctypes
 import os
 
 __all__ = ["KdaError", "kda_fwd", "kda_fwd_segments", "kda_fwd_host", "kda_fwd_noalloc",
-           "kda_decode",
+           "kda_decode", "kda_bwd", "kda_bwd_workspace_bytes",
            "kda_fwd_get_error", "kda_status_string",
            "kda_last_cuda_error",
            "kda_fwd_workspace_bytes", "kda_profile_enable", "kda_profile_read",
@@ -26,9 +26,10 @@ _LIB_PATH = os.path.join(_HERE, "_lib", "libkda.so")
 
 KDA_BF16 = 0
 KDA_F32 = 1
-KDA_NUM_KERNELS = 6
+KDA_NUM_KERNELS = 9
 KERNEL_NAMES = ("seqmap_kernel", "fused_kernel", "decode_kernel", "combine_kernel",
-                "segprep_kernel", "segfinal_kernel")
+                "segprep_kernel", "segfinal_kernel", "bwd_kernel", "bwd_finish_kernel",
+                "bwd_reduce_kernel")
 
 _lib = None
 _vp = ctypes.c_void_p
@@ -79,6 +80,13 @@ def declare(lib):
                                ctypes.c_float, _vp, ctypes.c_int, _vp, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp]
     lib.kda_decode.restype = ctypes.c_int
+    lib.kda_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_float,
+                            _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                            _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                            ctypes.c_int, ctypes.c_int, _vp]
+    lib.kda_bwd.restype = ctypes.c_int
+    lib.kda_bwd_workspace_bytes.argtypes = [ctypes.c_int] * 5
+    lib.kda_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.kda_fwd_get_error.argtypes = [_vp]
     lib.kda_fwd_get_error.restype = ctypes.c_int
     lib.kda_last_cuda_error.argtypes = []
@@ -310,6 +318,51 @@ def kda_fwd_host(q, k, v, g, beta, scale: float, out, A_log, dt_bias, lower_boun
             _ptr(cu_seqlens), N if cu_seqlens is not None else 0, B, T, H, K, V, s)
     if rc != 0:
         raise KdaError(rc, "kda_fwd_host")
+
+
+def kda_bwd(q, k, v, g, beta, scale: float, A_log, dt_bias, lower_bound: float, d_out,
+            initial_state=None, d_final_state=None, cu_seqlens=None, stream=None,
+            d_initial_state: bool = True) -> dict:
+    """Gradients of a loss with respect to the forward pass's inputs, on CUDA tensors
+    (asynchronous on ``stream``).  d_out: bf16 [B, T, H, 128] = dL/d(out);
+    d_final_state: optional fp32 [N, H, 128, 128] = dL/d(final state).  Other arguments
+    as ``kda_fwd``.  Returns fp32 tensors: dq, dk, dg [B, T, H, 128], dv [B, T, H, 128],
+    dbeta [B, T, H], dA_log [H], ddt_bias [H, 128] and (unless d_initial_state is
+    False) d_initial_state [N, H, 128, 128]."""
+    import torch
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("kda_bwd takes CUDA tensors")
+    B, T, H, K, V, N = _marshal(q, k, v, g, beta, d_out, A_log, dt_bias, initial_state, None,
+                                cu_seqlens, dev)
+    if d_final_state is not None:
+        _check(d_final_state, "d_final_state", torch.float32, (N, H, K, V), dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    r = {"dq": torch.empty((B, T, H, K), **f32), "dk": torch.empty((B, T, H, K), **f32),
+         "dv": torch.empty((B, T, H, V), **f32), "dg": torch.empty((B, T, H, K), **f32),
+         "dbeta": torch.empty((B, T, H), **f32), "dA_log": torch.empty((H,), **f32),
+         "ddt_bias": torch.empty((H, K), **f32)}
+    if d_initial_state:
+        r["d_initial_state"] = torch.empty((N, H, K, V), **f32)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    s = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    with torch.cuda.device(dev):
+        rc = load_library().kda_bwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(A_log),
+            _ptr(dt_bias), float(lower_bound), _ptr(initial_state), _state_dtype(initial_state),
+            _ptr(d_out), _ptr(d_final_state), _ptr(r["dq"]), _ptr(r["dk"]), _ptr(r["dv"]),
+            _ptr(r["dg"]), _ptr(r["dbeta"]), _ptr(r["dA_log"]), _ptr(r["ddt_bias"]),
+            _ptr(r.get("d_initial_state")), _ptr(cu_seqlens),
+            N if cu_seqlens is not None else 0, B, T, H, K, V, s)
+    if rc != 0:
+        raise KdaError(rc, "kda_bwd")
+    return r
+
+
+def kda_bwd_workspace_bytes(B: int, T: int, H: int, num_seqs: int = 0,
+                            varlen: bool = False) -> int:
+    return int(load_library().kda_bwd_workspace_bytes(B, T, H, num_seqs, int(varlen)))
 
 
 def kda_fwd_get_error(stream=None) -> int:

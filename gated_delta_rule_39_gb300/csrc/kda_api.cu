@@ -223,6 +223,49 @@ int validate(const void* q, const void* k, const void* v, const void* g, const v
     return KDA_OK;
 }
 
+// Host-side checks of kda_bwd; no CUDA call.
+int validate_bwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                 float scale, const float* A_log, const float* dt_bias, float lower_bound,
+                 const void* s0, int s0_dtype, const void* dout, const float* dfinal,
+                 const float* const* outs, const float* d_init, const int32_t* cu, int num_seqs,
+                 int B, int T, int H, int K, int V) {
+    if (K != kDim || V != kDim) return KDA_ERR_UNSUPPORTED_DIM;
+    if (B < 1 || T < 0 || H < 1) return KDA_ERR_SHAPE;
+    if (cu && (B != 1 || num_seqs < 1)) return KDA_ERR_SHAPE;
+    const long long tok = (long long)B * T;
+    if (tok * H * kDim >= (1LL << 31)) return KDA_ERR_SHAPE;
+    const int N = cu ? num_seqs : B;
+    if ((long long)N * H * kDim * kDim >= (1LL << 40)) return KDA_ERR_SHAPE;
+    if (!A_log || !dt_bias || !outs[5] || !outs[6]) return KDA_ERR_NULL;   // dA_log, ddt_bias
+    if (tok > 0) {
+        if (!q || !k || !v || !g || !beta || !dout) return KDA_ERR_NULL;
+        for (int i = 0; i < 5; ++i)
+            if (!outs[i]) return KDA_ERR_NULL;
+    }
+    if (s0 && s0_dtype != KDA_BF16 && s0_dtype != KDA_F32) return KDA_ERR_DTYPE;
+    if (!std::isfinite(scale)) return KDA_ERR_ARG;
+    if (!(lower_bound >= kLowerBoundMin && lower_bound <= 0.0f)) return KDA_ERR_ARG;
+    for (const void* p : {q, k, v, g, dout, static_cast<const void*>(outs[2]),
+                          static_cast<const void*>(d_init)})
+        if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return KDA_ERR_ALIGN;
+    // outputs (fp32) must not overlap the inputs or each other
+    const size_t n_row = (size_t)tok * H * kDim, n_s = (size_t)N * H * kDim * kDim;
+    const void* in_p[] = {q, k, v, g, dout, beta, s0, dfinal, A_log, dt_bias};
+    const size_t in_n[] = {n_row * 2, n_row * 2, n_row * 2, n_row * 2, n_row * 2,
+                           (size_t)tok * H * 2, n_s * (s0_dtype == KDA_F32 ? 4 : 2), n_s * 4,
+                           (size_t)H * 4, (size_t)H * kDim * 4};
+    const void* out_p[] = {outs[0], outs[1], outs[2], outs[3], outs[4], outs[5], outs[6], d_init};
+    const size_t out_n[] = {n_row * 4, n_row * 4, n_row * 4, n_row * 4, (size_t)tok * H * 4,
+                            (size_t)H * 4, (size_t)H * kDim * 4, n_s * 4};
+    for (int o = 0; o < 8; ++o) {
+        for (int i = 0; i < 10; ++i)
+            if (overlaps(out_p[o], out_n[o], in_p[i], in_n[i])) return KDA_ERR_ALIAS;
+        for (int o2 = o + 1; o2 < 8; ++o2)
+            if (overlaps(out_p[o], out_n[o], out_p[o2], out_n[o2])) return KDA_ERR_ALIAS;
+    }
+    return KDA_OK;
+}
+
 // Host-side checks of kda_decode; no CUDA call.
 int validate_decode(const void* q, const void* k, const void* v, const void* g, const void* beta,
                     float scale, const void* out, const float* A_log, const float* dt_bias,
@@ -711,6 +754,96 @@ int kda_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
     return KDA_OK;
 }
 
+int kda_bwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+            float scale, const float* A_log, const float* dt_bias, float lower_bound,
+            const void* initial_state, int initial_state_dtype, const void* d_out,
+            const float* d_final_state, float* dq, float* dk, float* dv, float* dg, float* dbeta,
+            float* dA_log, float* ddt_bias, float* d_initial_state, const int32_t* cu_seqlens,
+            int num_seqs, int B, int T, int H, int K, int V, void* stream) {
+    const float* outs[7] = {dq, dk, dv, dg, dbeta, dA_log, ddt_bias};
+    int rc = validate_bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state,
+                          initial_state_dtype, d_out, d_final_state, outs, d_initial_state,
+                          cu_seqlens, num_seqs, B, T, H, K, V);
+    if (rc != KDA_OK) return rc;
+    int dev = 0;
+    int* err = nullptr;
+    rc = device_setup(&dev, &err);
+    if (rc != KDA_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool varlen = cu_seqlens != nullptr;
+    const int N = varlen ? num_seqs : B;
+    const long long rows = (long long)B * T;
+    size_t n_ck, n_fw, n_part, n_blk;
+    const size_t floats = bwd_scratch_floats(N, rows, H, &n_ck, &n_fw, &n_part, &n_blk);
+    const size_t map_bytes = scratch_bytes(N, varlen);
+    unsigned char* scratch = nullptr;
+    const cudaError_t ea = cudaMallocAsync(reinterpret_cast<void**>(&scratch),
+                                           map_bytes + floats * sizeof(float), s);
+    if (ea != cudaSuccess) return cuda_fail(KDA_ERR_ALLOC, ea);
+    BwdProblem P{};
+    P.q = static_cast<const __nv_bfloat16*>(q);
+    P.k = static_cast<const __nv_bfloat16*>(k);
+    P.v = static_cast<const __nv_bfloat16*>(v);
+    P.g = static_cast<const __nv_bfloat16*>(g);
+    P.beta = static_cast<const __nv_bfloat16*>(beta);
+    P.dout = static_cast<const __nv_bfloat16*>(d_out);
+    P.scale = scale;
+    P.A_log = A_log;
+    P.dt_bias = dt_bias;
+    P.lower_bound = lower_bound;
+    P.init_state = initial_state;
+    P.init_dtype = initial_state_dtype;
+    P.dfinal = d_final_state;
+    P.dq = dq;
+    P.dk = dk;
+    P.dv = dv;
+    P.dg = dg;
+    P.dbeta = dbeta;
+    P.dA_log = dA_log;
+    P.ddt_bias = ddt_bias;
+    P.d_init = d_initial_state;
+    P.cu_seqlens = cu_seqlens;
+    P.N = N;
+    P.T = T;
+    P.H = H;
+    float* f = reinterpret_cast<float*>(scratch + map_bytes);
+    P.ck = f;
+    P.fw = f + n_ck;
+    P.part = P.fw + n_fw;
+    P.blk = P.part + n_part;
+    cudaError_t e = cudaSuccess;
+    const int* valid = nullptr;
+    if (varlen) {   // validate cu_seqlens on the device (the sequence map's check)
+        Problem FP{};
+        FP.cu_seqlens = cu_seqlens;
+        FP.N = N;
+        FP.T = T;
+        FP.H = H;
+        SeqMap M{};
+        M.seq_order = reinterpret_cast<int*>(scratch);
+        M.valid = M.seq_order + N;
+        valid = M.valid;
+        e = timed_launch(KDA_KERNEL_SEQMAP, s, [&] { return launch_seqmap(FP, M, err, s); });
+    }
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_BWD, s, [&] { return launch_bwd_main(P, valid, s); });
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_BWD_FINISH, s, [&] { return launch_bwd_finish(P, rows, valid, s); });
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_BWD_REDUCE, s, [&] { return launch_bwd_reduce(P, rows, valid, s); });
+    cudaFreeAsync(scratch, s);
+    if (e != cudaSuccess) return cuda_fail(KDA_ERR_LAUNCH, e);
+    return KDA_OK;
+}
+
+size_t kda_bwd_workspace_bytes(int B, int T, int H, int num_seqs, int varlen) {
+    if (B < 1 || T < 0 || H < 1) return 0;
+    const int N = varlen ? num_seqs : B;
+    size_t a, b, c, d;
+    return scratch_bytes(N, varlen != 0) +
+           bwd_scratch_floats(N, (long long)B * T, H, &a, &b, &c, &d) * sizeof(float);
+}
+
 int kda_decode(const void* q, const void* k, const void* v, const void* g, const void* beta,
                float scale, void* out, const float* A_log, const float* dt_bias, float lower_bound,
                const void* state_in, int state_in_dtype, void* state_out, int state_out_dtype,
@@ -799,6 +932,9 @@ const char* kda_kernel_name(int kernel_id) {
         case KDA_KERNEL_COMBINE: return "combine_kernel";
         case KDA_KERNEL_SEGPREP: return "segprep_kernel";
         case KDA_KERNEL_SEGFINAL: return "segfinal_kernel";
+        case KDA_KERNEL_BWD: return "bwd_kernel";
+        case KDA_KERNEL_BWD_FINISH: return "bwd_finish_kernel";
+        case KDA_KERNEL_BWD_REDUCE: return "bwd_reduce_kernel";
         default: return "unknown";
     }
 }

@@ -65,6 +65,23 @@ struct Problem {
     const __nv_bfloat16* vzero = nullptr;   // [16][H][128] zeros (window 0)
 };
 
+// ---- backward pass (kda_bwd.cu) ----------------------------------------------------
+struct BwdProblem {
+    const __nv_bfloat16 *q, *k, *v, *g, *beta, *dout;
+    float scale;
+    const float* A_log;
+    const float* dt_bias;
+    float lower_bound;
+    const void* init_state;   // or nullptr (zero)
+    int init_dtype;
+    const float* dfinal;      // dL/d(final state) [N][H][K][V], or nullptr (zero)
+    float *dq, *dk, *dv, *dg, *dbeta, *dA_log, *ddt_bias;
+    float* d_init;            // dL/d(initial state) [N][H][K][V], or nullptr (not written)
+    const int* cu_seqlens;    // or nullptr: N sequences of T tokens
+    int N, T, H;
+    float *ck, *fw, *part, *blk;   // scratch (bwd_scratch_floats)
+};
+
 // TMA tensor maps over the token rows of q, k, v, g (built on the host per call).
 struct RawMaps {
     CUtensorMap q, k, v, g;
@@ -156,5 +173,12 @@ cudaError_t launch_segprep(const void* init, int init_dtype, float* w0init, int 
 cudaError_t launch_segfinal(const float* w1final, void* final_state, int final_dtype, int N, int H,
                             int nseg, cudaStream_t s);
 size_t fused_smem_bytes();
+size_t bwd_scratch_floats(int N, long long rows, int H, size_t* ck, size_t* fw, size_t* part,
+                          size_t* blk);
+cudaError_t launch_bwd_main(const BwdProblem& P, const int* valid, cudaStream_t s);
+cudaError_t launch_bwd_finish(const BwdProblem& P, long long rows, const int* valid,
+                              cudaStream_t s);
+cudaError_t launch_bwd_reduce(const BwdProblem& P, long long rows, const int* valid,
+                              cudaStream_t s);
 
 }  // namespace kda

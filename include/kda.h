@@ -190,6 +190,46 @@ int kda_fwd_host(const void* q, const void* k, const void* v, const void* g,
                  void* stream);
 
 /*
+ * kda_bwd -- the backward pass: gradients of a scalar loss L with respect to the
+ * forward pass's inputs, given dL/d(out) and, optionally, dL/d(final state).
+ *
+ * No counterpart on the pages (the pages' library is forward-only: "Moonshot AI
+ * Open-Sources FlashKDA", "Limitations before you integrate").  It differentiates
+ * the recurrence above exactly (reverse order of its steps, token by token, in fp32):
+ * with x = exp(A_log)(g + dt_bias), a = exp(lower_bound sigmoid(x)), b = sigmoid(beta),
+ * S' = Diag(a) S, r = S'^T k, d = b (v - r), S = S' + k d^T, o = scale S^T q.
+ *
+ *   inputs      q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state
+ *               (+ dtype), cu_seqlens, num_seqs, B, T, H, K, V: as kda_fwd
+ *   d_out       bf16 [B, T, H, V]: dL/d(out)
+ *   d_final_state  fp32 [N, H, K, V]: dL/d(final state), or NULL (zero)
+ *   outputs (fp32): dq, dk, dg [B, T, H, K]; dv [B, T, H, V]; dbeta [B, T, H];
+ *               dA_log [H]; ddt_bias [H, K] (summed over all sequences and tokens);
+ *               d_initial_state [N, H, K, V] or NULL (not written); it is the
+ *               gradient with respect to the initial state also when none is given.
+ *
+ * Outputs must not overlap the inputs or each other (KDA_ERR_ALIAS); q, k, v, g,
+ * d_out, dv and d_initial_state must be 16-byte aligned.  Scratch:
+ * kda_bwd_workspace_bytes() from the stream-ordered allocator (state checkpoints every
+ * 16 tokens, each token's d and v - r, per-slice partial sums; about 13 KB per token
+ * and head).  Asynchronous on `stream`; a malformed cu_seqlens sets KDA_ERR_BAD_SEQLENS
+ * in the error word and writes nothing.  Results are deterministic (fixed summation
+ * order).  The work: 8 CTAs per (sequence, head), each owning 16 value columns of the
+ * state, on CUDA cores; then a kernel that sums their partial dq, dk and decay
+ * gradients and applies the activations, and one that sums dA_log and ddt_bias.
+ */
+int kda_bwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+            float scale, const float* A_log, const float* dt_bias, float lower_bound,
+            const void* initial_state, int initial_state_dtype, const void* d_out,
+            const float* d_final_state, float* dq, float* dk, float* dv, float* dg,
+            float* dbeta, float* dA_log, float* ddt_bias, float* d_initial_state,
+            const int32_t* cu_seqlens, int num_seqs, int B, int T, int H, int K, int V,
+            void* stream);
+
+/* Bytes of scratch kda_bwd takes from the stream-ordered allocator (host-only). */
+size_t kda_bwd_workspace_bytes(int B, int T, int H, int num_seqs, int varlen);
+
+/*
  * kda_fwd_get_error -- synchronise `stream`, then return and clear the current
  * device's error word: KDA_OK, KDA_ERR_BAD_SEQLENS or KDA_ERR_DEVICE_TIMEOUT
  * (or KDA_ERR_CUDA if the synchronisation itself failed).  There is one word
@@ -302,7 +342,10 @@ enum {
     KDA_KERNEL_COMBINE = 3,
     KDA_KERNEL_SEGPREP = 4,
     KDA_KERNEL_SEGFINAL = 5,
-    KDA_NUM_KERNELS = 6
+    KDA_KERNEL_BWD = 6,
+    KDA_KERNEL_BWD_FINISH = 7,
+    KDA_KERNEL_BWD_REDUCE = 8,
+    KDA_NUM_KERNELS = 9
 };
 int kda_profile_enable(int on);
 int kda_profile_read(double* total_ms, long long* launches);
