@@ -42,6 +42,16 @@ C = 16
 # plus, per (sequence, head), the initial state read and the final state write.
 FLOP_PER_TH = 6 * K * V + 2 * C * (3 * K + 2 * V)
 BYTES_PER_TH = 4 * 2 * 128 + 2 + 2 * 128
+# Backward pass (kda_bwd), token-level reverse of the recurrence on CUDA cores, per
+# (token, head): the forward step it recomputes (S' = Diag(a) S, r = S'^T k, S += k d^T:
+# 5KV) and the reverse step (dS += q dO^T, dq, dd, dk, dS', dk += S' dr, da, dS = a dS':
+# 15KV) -- 20KV flop; bytes: q, k, v, g, dO and beta read (bf16), dq, dk, dv, dg and
+# dbeta written (fp32).  It is bound by fp32 CUDA-core arithmetic: the peak is 152 SMs
+# x 128 fp32 lanes x 2 flop (a multiply-add) x 2.07 GHz.
+BWD_FLOP_PER_TH = 20 * K * V
+BWD_BYTES_PER_TH = 5 * 2 * 128 + 2 + 4 * 4 * 128 + 4
+ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+BWD_WORKLOAD = "bwd_prefill_t8192_h96"
 # The fused kernel does the whole path, so its algorithmic work is the path's.
 KERNEL_FLOP_PER_TH = {"fused_kernel": FLOP_PER_TH}
 KERNEL_BYTES_PER_TH = {"fused_kernel": BYTES_PER_TH}
@@ -202,9 +212,15 @@ def algorithmic_work(d, calls):
     return BYTES_PER_TH * th + state_bytes, FLOP_PER_TH * th, th
 
 
-def roofline_of(kernel, ms, bytes_, flop, hbm, tflops, src):
+def roofline_of(kernel, ms, bytes_, flop, hbm, tflops, src, alu=False):
     t_hbm = bytes_ / (hbm * 1e9)
     t_tc = flop / (tflops * 1e12)
+    if alu and flop / (ALU_TFLOPS * 1e12) >= t_hbm:
+        roof = {"bound": "alu", "achieved": flop / (ms * 1e-3) / 1e12, "peak": ALU_TFLOPS,
+                "unit": "TFLOP/s", "frac": flop / (ms * 1e-3) / 1e12 / ALU_TFLOPS,
+                "kernel": kernel, "kernel_ms": ms,
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz"}
+        return roof
     if t_tc >= t_hbm:
         roof = {"bound": "tensor", "achieved": flop / (ms * 1e-3) / 1e12, "peak": tflops,
                 "unit": "TFLOP/s"}
@@ -308,6 +324,56 @@ class DecodeRunner:
 DECODE_WORKLOAD = "decode_n256_h96"
 
 
+class BwdRunner:
+    """One kda_bwd call on the headline workload's inputs, a seeded dL/d(out) and
+    dL/d(final state); outputs allocated once."""
+
+    def __init__(self, d, device, stream, seed):
+        import ctypes
+        import torch
+        import synth
+        import gated_delta_rule_39_gb300 as kda
+        self.kda = kda
+        self.lib = kda.load_library()
+        self.d = d
+        self.stream = stream
+        B, T, H, _ = d["q"].shape
+        self.B, self.T, self.H, self.N = B, T, H, d["N"]
+        self.calls = 1
+
+        def bf16(bits):
+            return (torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
+                    .view(torch.bfloat16))
+
+        rng = np.random.default_rng(seed + 1000)
+        self.x = {n: bf16(d[n]) for n in ("q", "k", "v", "g", "beta")}
+        self.x["dout"] = bf16(synth.f32_to_bf16_bits(rng.standard_normal(d["v"].shape,
+                                                                          dtype=np.float32)))
+        self.dfinal = torch.from_numpy(rng.standard_normal((self.N, H, K, V), dtype=np.float32)).to(device)
+        self.A_log = torch.from_numpy(d["A_log"]).to(device)
+        self.dt_bias = torch.from_numpy(d["dt_bias"]).to(device)
+        s0 = d.get("initial_state")
+        self.s0 = None if s0 is None else (bf16(s0) if s0.dtype == np.uint16
+                                           else torch.from_numpy(s0).to(device))
+        f32 = dict(dtype=torch.float32, device=device)
+        self.o = [torch.empty((B, T, H, K), **f32), torch.empty((B, T, H, K), **f32),
+                  torch.empty((B, T, H, V), **f32), torch.empty((B, T, H, K), **f32),
+                  torch.empty((B, T, H), **f32), torch.empty((H,), **f32),
+                  torch.empty((H, K), **f32), torch.empty((self.N, H, K, V), **f32)]
+        p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+        self.args = ([p(self.x[n]) for n in ("q", "k", "v", "g", "beta")] +
+                     [ctypes.c_float(d["scale"]), p(self.A_log), p(self.dt_bias),
+                      ctypes.c_float(d["lower_bound"]), p(self.s0),
+                      0 if s0 is None or s0.dtype == np.uint16 else 1, p(self.x["dout"]),
+                      p(self.dfinal)] + [p(t) for t in self.o] +
+                     [None, 0, B, T, H, K, V, ctypes.c_void_p(stream.cuda_stream)])
+
+    def step(self):
+        rc = self.lib.kda_bwd(*self.args)
+        if rc != 0:
+            raise RuntimeError(f"kda_bwd failed: {self.kda.kda_status_string(rc)}")
+
+
 def make_decode_inputs(seed):
     import synth
     return synth.make_inputs(256, 1, 96, seed=seed, init_dtype="f32")
@@ -345,7 +411,7 @@ def timed_steps(runner, steps, warmup, pg=None, device=None, sampler=None):
     return elapsed_ms, prof
 
 
-def workload_line(name, d, elapsed_ms, prof, steps, world, calls, decode=False):
+def workload_line(name, d, elapsed_ms, prof, steps, world, calls, decode=False, bwd=False):
     """Throughput and roofline of one workload from its timing."""
     hbm, tflops, src = peaks()
     B, T, H, _ = d["q"].shape
@@ -353,13 +419,18 @@ def workload_line(name, d, elapsed_ms, prof, steps, world, calls, decode=False):
     if decode:   # the state is read and written in fp32 once per (sequence, head)
         bytes_ = B * H * (BYTES_PER_TH + K * V * (4 + 4))
         flop = B * H * 8 * K * V   # decay, S'^T k, update, S^T q: 4 multiply-adds per element
+    if bwd:      # initial state read, dL/d(final state) read, d(initial state) written
+        s0 = d.get("initial_state")
+        init_b = 0 if s0 is None else (2 if s0.dtype == np.uint16 else 4)
+        bytes_ = th * BWD_BYTES_PER_TH + d["N"] * H * K * V * (init_b + 4 + 4)
+        flop = th * BWD_FLOP_PER_TH
     tokens_per_step = B * T
     dom = max(prof, key=lambda n: prof[n][0])
     # the dominant kernel's device time per step (a split call launches it twice)
     dom_ms = prof[dom][0] / steps
     ms_per_step = elapsed_ms / steps
-    roof = (roofline_of(dom, dom_ms, bytes_, flop, hbm, tflops, src)
-            if dom in ("fused_kernel", "decode_kernel") else None)
+    roof = (roofline_of(dom, dom_ms, bytes_, flop, hbm, tflops, src, alu=bwd)
+            if dom in ("fused_kernel", "decode_kernel", "bwd_kernel") else None)
     if roof is not None:
         roof["traffic"] = ncu_traffic(dom, name)
     t_roof = max(bytes_ / (hbm * 1e9), flop / (tflops * 1e12))
@@ -482,6 +553,21 @@ def run_cuda(args, world, rank, local, pg):
         others[DECODE_WORKLOAD] = rec
         del drun
         torch.cuda.empty_cache()
+        # the backward pass over the headline workload (dL/d(out) and dL/d(final state)
+        # drawn with the rank's seed)
+        brun = BwdRunner(d, device, stream, rank)
+        bsteps = max(3, args.steps // 4)
+        ems, bprof = timed_steps(brun, bsteps, 3, pg, device)
+        ems = max_over_ranks(pg, ems, device)
+        rec = workload_line(BWD_WORKLOAD, d, ems, bprof, bsteps, world, 1, bwd=True)
+        rec["steps"], rec["warmup"] = bsteps, 3
+        rec["config"] = {"inputs": WORKLOAD, "d_out": "bf16 N(0,1)", "d_final_state": "f32 N(0,1)",
+                         "entry_point": "kda_bwd", "outputs": "fp32 gradients"}
+        if world == 1 and not args.no_cpu_baseline:
+            rec["cpu_baseline"] = cpu_baseline_bwd(brun, target_s=args.cpu_seconds / 4)
+        others[BWD_WORKLOAD] = rec
+        del brun
+        torch.cuda.empty_cache()
 
     if rank == 0:
         if args.heads:
@@ -543,6 +629,43 @@ def cpu_baseline(d, workload: str = WORKLOAD, target_s: float = 12.0):
             "sample": f"{n_heads} of {H} heads x {d['q'].shape[0] * T} tokens of {workload}; "
                       f"tokens/s counts "
                       f"a token as all {H} heads ({t:.1f} s)"}
+
+
+def cpu_baseline_bwd(brun, target_s: float = 3.0):
+    """Time the fp64 backward oracle on a subset of heads of the backward's inputs."""
+    import oracle
+    d = brun.d
+    H = d["q"].shape[2]
+    T = d["q"].shape[1]
+    threads = oracle.default_threads()
+    dout = brun.x["dout"].view(torch_int16()).cpu().numpy().view(np.uint16)
+    dfinal = brun.dfinal.cpu().numpy()
+
+    def run(heads):
+        t0 = time.perf_counter()
+        oracle.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], d["A_log"],
+                       d["dt_bias"], d["lower_bound"], dout, initial_state=d.get("initial_state"),
+                       dfinal=dfinal, cu_seqlens=d.get("cu_seqlens"), heads=heads,
+                       n_threads=threads)
+        return time.perf_counter() - t0
+
+    probe = min(H, threads)
+    t_probe = run(list(range(probe)))
+    n_heads = int(min(H, max(probe, round(probe * target_s / max(t_probe, 1e-3)))))
+    if n_heads > probe:
+        t = run(list(range(n_heads)))
+    else:
+        n_heads, t = probe, t_probe
+    tokens_equiv = d["q"].shape[0] * T * n_heads / H
+    return {"value": tokens_equiv / t, "unit": "tokens/s", "cores": min(threads, n_heads),
+            "kind": "oracle",
+            "sample": f"backward of {n_heads} of {H} heads x {d['q'].shape[0] * T} tokens; "
+                      f"tokens/s counts a token as all {H} heads ({t:.1f} s)"}
+
+
+def torch_int16():
+    import torch
+    return torch.int16
 
 
 def run_reference(args, world, rank, local, pg):

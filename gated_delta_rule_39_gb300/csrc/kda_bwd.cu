@@ -16,12 +16,15 @@
 //
 // The value columns of the state are independent recurrences (k, a and b are shared),
 // so the work is cut into 8 slices of 16 value columns per (sequence, head), one CTA
-// each: thread (key c, half h) holds S[c][16 s + 8 h .. + 7].  Phase 1 runs the slice
-// forward, storing its state every 16 tokens and each token's d and v - r; phase 2
-// walks the chunks backwards, rebuilds the chunk's states from the checkpoint
-// (element-wise, with the stored d) into shared memory, and runs the reverse steps.
-// dq, dk, da and db sum over value columns: each slice writes its partial sums, and a
-// second kernel adds the 8 slices in a fixed order and applies the activations.
+// each: thread (column j, key block b) holds S[8 b .. 8 b + 7][16 s + j], so a warp
+// holds all 128 keys of two columns and the sums over keys (r = S'^T k, dd = dS^T k)
+// are four shuffles.  Each block of 8 token rows is staged in shared memory at once.
+// Phase 1 runs the slice forward, storing its state every 8 tokens and each token's
+// d and v - r; phase 2 walks the blocks backwards, rebuilds the block's states from the
+// checkpoint (element-wise, with the stored d) into shared memory, and runs the
+// reverse steps.  dq, dk, da and db sum over value columns: within a warp by a
+// shuffle, over the 8 warps in shared memory every 2 tokens, and over the 8 slices by
+// a second kernel (all in a fixed order), which also applies the activations.
 // This is a token-by-token pass on CUDA cores; a chunked pass on tensor cores, as the
 // forward is, would be much faster.
 #include <atomic>
@@ -36,41 +39,32 @@ constexpr int kSlices = 8;          // value slices per (sequence, head)
 constexpr int kSliceV = kDim / kSlices;   // 16 value columns
 constexpr int kBwdThreads = 256;    // 128 keys x 2 halves of 8 columns
 constexpr int kPart = 388;          // partial sums per (row, head, slice): dq, dk, da [128], db
+constexpr int kGroup = 2;           // tokens whose per-warp partial sums wait in shared memory
+constexpr int kBC = 8;              // tokens per checkpoint (and per staged block of rows):
+                                    // small enough for two CTAs per SM
 
 struct BwdSmem {
-    float st[kChunk][kBwdThreads][8];   // S_{t-1} of each token of the chunk, per thread
-    float red[2][8][kSliceV];           // warp partials of the key reductions (two buffers)
+    float4 st[kBC][2][kBwdThreads];     // S_{t-1} of each token of the block: a thread's 8
+                                        // values as two float4 planes (no bank conflicts)
+    float a[kBC][kDim];                  // the block's decays
+    float kk[kBC][kDim];                 // keys
+    float qq[kBC][kDim];                 // queries (reverse phase)
+    float vv[kBC][kSliceV];             // the slice's values (forward) or dL/d(out) (reverse)
+    float fw[kBC][2 * kSliceV];         // d and v - r of the slice (reverse)
+    float b[kBC];                       // sigmoid(beta)
+    // reverse: per-warp sums over the warp's two columns of dq, dk, da (128 keys each)
+    // and db, for a group of 4 tokens; summed over the 8 warps once per group
+    float grp[kGroup][8][3 * kDim + 4];
 };
 
 __device__ __forceinline__ float bf(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
 
-// x[e] summed over the 128 keys (threads of the same half), for this thread's 8 columns
-__device__ __forceinline__ void key_sum(float (&x)[8], BwdSmem& S, int buf, int warp, int lane) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        float y = x[e];
-        y += __shfl_xor_sync(0xffffffffu, y, 2);
-        y += __shfl_xor_sync(0xffffffffu, y, 4);
-        y += __shfl_xor_sync(0xffffffffu, y, 8);
-        y += __shfl_xor_sync(0xffffffffu, y, 16);
-        x[e] = y;
-    }
-    if (lane < 2) {
-        float* r = &S.red[buf][warp][8 * lane];
-        *reinterpret_cast<float4*>(r) = make_float4(x[0], x[1], x[2], x[3]);
-        *reinterpret_cast<float4*>(r + 4) = make_float4(x[4], x[5], x[6], x[7]);
-    }
-    __syncthreads();
-    const int hv = lane & 1;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = 0.0f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-        const float4 p = *reinterpret_cast<const float4*>(&S.red[buf][w][8 * hv]);
-        const float4 q = *reinterpret_cast<const float4*>(&S.red[buf][w][8 * hv + 4]);
-        x[0] += p.x; x[1] += p.y; x[2] += p.z; x[3] += p.w;
-        x[4] += q.x; x[5] += q.y; x[6] += q.z; x[7] += q.w;
-    }
+__device__ __forceinline__ void load4_bf16(const __nv_bfloat16* p, float (&x)[4]) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(p);
+    x[0] = __uint_as_float(raw.x << 16);
+    x[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(raw.y << 16);
+    x[3] = __uint_as_float(raw.y & 0xFFFF0000u);
 }
 
 __device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float (&x)[8]) {
@@ -93,178 +87,248 @@ __device__ __forceinline__ float decay(const BwdProblem& P, size_t row, int h, i
     return expf(P.lower_bound * sigm(x));
 }
 
-// Checkpoint slot of chunk c of sequence n (first token bos): distinct for every
-// (n, c) of a call, below N + rows / 16 + 1.
+// Checkpoint slot of block c (of 8 tokens) of sequence n (first token bos): distinct for
+// every (n, c) of a call, below N + rows / 8 + 1.
 __device__ __forceinline__ long long ck_slot(int n, long long bos, int c) {
-    return (long long)n + c + bos / kChunk;
+    return (long long)n + c + bos / kBC;
 }
 
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(BwdProblem P, const int* valid) {
+// A block's token rows into shared memory, all threads at once (one memory latency
+// per 8 tokens): keys and decays (and queries on the way back), the slice's 16 values
+// (or dL/d(out)), b, and on the way back the stored d and v - r.  Rows past the
+// sequence's end are not read.
+__device__ __forceinline__ void stage(const BwdProblem& P, BwdSmem& S, long long row0, int len,
+                                      int h, int col0, float eA, bool reverse,
+                                      const float* fw0, size_t fw_step) {
+    const int tid = threadIdx.x;
+    {   // 8 rows x 128 channels: thread = (row, 4 channels)
+        const int i = tid >> 5, c4 = 4 * (tid & 31);
+        if (i < len) {
+            const size_t rk = ((size_t)(row0 + i) * P.H + h) * kDim + c4;
+            float kx[4], gx[4], a[4];
+            load4_bf16(P.k + rk, kx);
+            load4_bf16(P.g + rk, gx);
+            const float* db = P.dt_bias + (size_t)h * kDim + c4;   // 4-byte aligned only
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[e] = expf(P.lower_bound * sigm(eA * (gx[e] + db[e])));
+            *reinterpret_cast<float4*>(&S.a[i][c4]) = make_float4(a[0], a[1], a[2], a[3]);
+            *reinterpret_cast<float4*>(&S.kk[i][c4]) = make_float4(kx[0], kx[1], kx[2], kx[3]);
+            if (reverse) {
+                float qx[4];
+                load4_bf16(P.q + rk, qx);
+                *reinterpret_cast<float4*>(&S.qq[i][c4]) = make_float4(qx[0], qx[1], qx[2], qx[3]);
+            }
+        }
+    }
+    if (tid < 2 * kBC) {   // the slice's 16 columns of v (or dO): thread = (row, 8 columns)
+        const int i = tid >> 1, hv = tid & 1;
+        if (i < len) {
+            const size_t rv = ((size_t)(row0 + i) * P.H + h) * kDim + col0 + 8 * hv;
+            float x[8];
+            load8_bf16(reverse ? P.dout + rv : P.v + rv, x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) S.vv[i][8 * hv + e] = x[e];
+        }
+    } else if (tid < 3 * kBC) {   // b of each row
+        const int i = tid - 2 * kBC;
+        if (i < len) S.b[i] = sigm(bf(P.beta, (size_t)(row0 + i) * P.H + h));
+    } else if (reverse && tid >= 128 && tid < 128 + 8 * kBC) {   // d and v - r: (row, 4 floats)
+        const int i = (tid - 128) >> 3, f4 = 4 * ((tid - 128) & 7);
+        if (i < len)
+            *reinterpret_cast<float4*>(&S.fw[i][f4]) =
+                *reinterpret_cast<const float4*>(fw0 + (size_t)i * fw_step + f4);
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const int* valid) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     BwdSmem& S = *reinterpret_cast<BwdSmem*>(smem_raw);
     if (valid && !*valid) return;   // malformed cu_seqlens: the sequence map says so
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int key = tid >> 1, hv = tid & 1;
     const int slice = blockIdx.x % kSlices;
     const int h = (blockIdx.x / kSlices) % P.H;
     const int n = blockIdx.x / (kSlices * P.H);
     const long long bos = P.cu_seqlens ? P.cu_seqlens[n] : (long long)n * P.T;
     const int L = P.cu_seqlens ? P.cu_seqlens[n + 1] - P.cu_seqlens[n] : P.T;
-    const int nch = (L + kChunk - 1) / kChunk;
-    const int col = kSliceV * slice + 8 * hv;                  // first of this thread's columns
+    const int nch = (L + kBC - 1) / kBC;
+    const int col0 = kSliceV * slice;
     const float eA = expf(P.A_log[h]);
-    const size_t sidx = (((size_t)n * P.H + h) * kDim + key) * kDim + col;   // state element
+    const size_t fw_step = (size_t)P.H * kSlices * (2 * kSliceV);           // between rows
     const auto fw_at = [&](size_t row) {   // d (16) and v - r (16) of this slice at a row
         return P.fw + ((row * P.H + h) * kSlices + slice) * (2 * kSliceV);
     };
-    const auto ck_at = [&](int c) {
-        return P.ck + ((ck_slot(n, bos, c) * P.H + h) * kSlices + slice) * (kDim * kSliceV) +
-               key * kSliceV + 8 * hv;
-    };
 
     // ---- phase 1: forward over the slice, checkpoints and per-token d, v - r ----------
-    float st[8];
+    // Here thread (column jv = tid / 16, key block kb = tid % 16) holds S[8 kb .. + 7][jv]:
+    // a warp holds all 128 keys of two columns, so r = S'^T k is a sum over 16 lanes
+    // (four shuffles, no barrier per token).
+    {
+        const int jv = tid >> 4, kb = tid & 15, k0 = 8 * kb;
+        float st[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        float x = 0.0f;
-        if (P.init_state)
-            x = P.init_dtype == KDA_F32 ? static_cast<const float*>(P.init_state)[sidx + e]
-                                        : __bfloat162float(static_cast<const __nv_bfloat16*>(P.init_state)[sidx + e]);
-        st[e] = x;
-    }
-    int buf = 0;
-    for (int c = 0; c < nch; ++c) {
-        float* ck = ck_at(c);
-        *reinterpret_cast<float4*>(ck) = make_float4(st[0], st[1], st[2], st[3]);
-        *reinterpret_cast<float4*>(ck + 4) = make_float4(st[4], st[5], st[6], st[7]);
-        const int len = min(kChunk, L - c * kChunk);
-        for (int i = 0; i < len; ++i) {
-            const size_t row = bos + (size_t)c * kChunk + i;
-            const float a = decay(P, row, h, key, eA);
-            const float kk = bf(P.k, (row * P.H + h) * kDim + key);
-            const float b = sigm(bf(P.beta, row * P.H + h));
-            float vv[8], r[8];
-            load8_bf16(P.v + (row * P.H + h) * kDim + col, vv);
+        for (int e = 0; e < 8; ++e) {
+            float x = 0.0f;
+            if (P.init_state) {
+                const size_t si = (((size_t)n * P.H + h) * kDim + k0 + e) * kDim + col0 + jv;
+                x = P.init_dtype == KDA_F32 ? static_cast<const float*>(P.init_state)[si]
+                                            : __bfloat162float(static_cast<const __nv_bfloat16*>(P.init_state)[si]);
+            }
+            st[e] = x;
+        }
+        for (int c = 0; c < nch; ++c) {
+            // checkpoint [key][16 columns] of the slice (read back by thread (key, half))
+            float* ck = P.ck + ((ck_slot(n, bos, c) * P.H + h) * kSlices + slice) * (kDim * kSliceV);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                st[e] *= a;
-                r[e] = st[e] * kk;
-            }
-            key_sum(r, S, buf, warp, lane);
-            buf ^= 1;
-            float d[8];
+            for (int e = 0; e < 8; ++e) ck[(k0 + e) * kSliceV + jv] = st[e];
+            const int len = min(kBC, L - c * kBC);
+            const long long row0 = bos + (long long)c * kBC;
+            stage(P, S, row0, len, h, col0, eA, false, nullptr, 0);
+            for (int i = 0; i < len; ++i) {
+                const float4 a0 = *reinterpret_cast<const float4*>(&S.a[i][k0]);
+                const float4 a1 = *reinterpret_cast<const float4*>(&S.a[i][k0 + 4]);
+                const float4 q0 = *reinterpret_cast<const float4*>(&S.kk[i][k0]);
+                const float4 q1 = *reinterpret_cast<const float4*>(&S.kk[i][k0 + 4]);
+                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float kk[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                float r = 0.0f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                d[e] = b * (vv[e] - r[e]);
-                st[e] = fmaf(kk, d[e], st[e]);
+                for (int e = 0; e < 8; ++e) {
+                    st[e] *= a[e];
+                    r = fmaf(st[e], kk[e], r);
+                }
+                r += __shfl_xor_sync(0xffffffffu, r, 1);
+                r += __shfl_xor_sync(0xffffffffu, r, 2);
+                r += __shfl_xor_sync(0xffffffffu, r, 4);
+                r += __shfl_xor_sync(0xffffffffu, r, 8);
+                const float vr = S.vv[i][jv] - r;
+                const float d = S.b[i] * vr;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) st[e] = fmaf(kk[e], d, st[e]);
+                if (kb == 0) {   // lanes 0 and 16: this column's d and v - r
+                    float* f = fw_at(row0 + i);
+                    f[jv] = d;
+                    f[kSliceV + jv] = vr;
+                }
             }
-            if (key == 0) {   // threads 0 and 1: the 16 columns of the slice
-                float* f = fw_at(row) + 8 * hv;
-                *reinterpret_cast<float4*>(f) = make_float4(d[0], d[1], d[2], d[3]);
-                *reinterpret_cast<float4*>(f + 4) = make_float4(d[4], d[5], d[6], d[7]);
-                float* g = fw_at(row) + kSliceV + 8 * hv;
-                *reinterpret_cast<float4*>(g) = make_float4(vv[0] - r[0], vv[1] - r[1], vv[2] - r[2], vv[3] - r[3]);
-                *reinterpret_cast<float4*>(g + 4) = make_float4(vv[4] - r[4], vv[5] - r[5], vv[6] - r[6], vv[7] - r[7]);
-            }
+            __syncthreads();   // the staged rows are replaced by the next block's
         }
     }
-    __syncthreads();   // the per-token d and v - r are read by other threads below
+    __syncthreads();   // checkpoints, d and v - r are read by other threads below
 
-    // ---- phase 2: reverse ------------------------------------------------------------
+    // ---- phase 2: reverse, in the same layout: thread (column jv, keys 8 kb .. + 7) ----
+    const int jv = tid >> 4, kb = tid & 15, k0 = 8 * kb;
     float dS[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) dS[e] = P.dfinal ? P.dfinal[sidx + e] : 0.0f;
+    for (int e = 0; e < 8; ++e)
+        dS[e] = P.dfinal ? P.dfinal[(((size_t)n * P.H + h) * kDim + k0 + e) * kDim + col0 + jv] : 0.0f;
     for (int c = nch - 1; c >= 0; --c) {
-        const int len = min(kChunk, L - c * kChunk);
-        {   // rebuild the chunk's states S_{t-1} from the checkpoint (element-wise)
-            const float* ck = ck_at(c);
-            const float4 c0 = *reinterpret_cast<const float4*>(ck);
-            const float4 c1 = *reinterpret_cast<const float4*>(ck + 4);
-            float s[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        const int len = min(kBC, L - c * kBC);
+        const long long row0 = bos + (long long)c * kBC;
+        stage(P, S, row0, len, h, col0, eA, true, fw_at(row0), fw_step);
+        {   // rebuild the block's states S_{t-1} from the checkpoint (element-wise)
+            const float* ck = P.ck + ((ck_slot(n, bos, c) * P.H + h) * kSlices + slice) * (kDim * kSliceV);
+            float sv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sv[e] = ck[(k0 + e) * kSliceV + jv];
             for (int i = 0; i < len; ++i) {
-                const size_t row = bos + (size_t)c * kChunk + i;
-                *reinterpret_cast<float4*>(&S.st[i][tid][0]) = make_float4(s[0], s[1], s[2], s[3]);
-                *reinterpret_cast<float4*>(&S.st[i][tid][4]) = make_float4(s[4], s[5], s[6], s[7]);
-                const float a = decay(P, row, h, key, eA);
-                const float kk = bf(P.k, (row * P.H + h) * kDim + key);
-                const float* f = fw_at(row) + 8 * hv;
-                const float4 d0 = *reinterpret_cast<const float4*>(f);
-                const float4 d1 = *reinterpret_cast<const float4*>(f + 4);
-                const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+                S.st[i][0][tid] = make_float4(sv[0], sv[1], sv[2], sv[3]);
+                S.st[i][1][tid] = make_float4(sv[4], sv[5], sv[6], sv[7]);
+                const float d = S.fw[i][jv];
+                const float4 a0 = *reinterpret_cast<const float4*>(&S.a[i][k0]);
+                const float4 a1 = *reinterpret_cast<const float4*>(&S.a[i][k0 + 4]);
+                const float4 k0v = *reinterpret_cast<const float4*>(&S.kk[i][k0]);
+                const float4 k1v = *reinterpret_cast<const float4*>(&S.kk[i][k0 + 4]);
+                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float kk[8] = {k0v.x, k0v.y, k0v.z, k0v.w, k1v.x, k1v.y, k1v.z, k1v.w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) s[e] = fmaf(kk, d[e], a * s[e]);
+                for (int e = 0; e < 8; ++e) sv[e] = fmaf(kk[e], d, a[e] * sv[e]);
             }
         }
-        // (each thread reads only its own rebuilt states and its own key's decay)
+        // (each thread reads only its own rebuilt states)
         for (int i = len - 1; i >= 0; --i) {
-            const size_t row = bos + (size_t)c * kChunk + i;
-            const size_t rk = (row * P.H + h) * kDim;
-            const float a = decay(P, row, h, key, eA);
-            const float kk = bf(P.k, rk + key), qq = bf(P.q, rk + key);
-            const float b = sigm(bf(P.beta, row * P.H + h));
-            float dout[8];
-            load8_bf16(P.dout + rk + col, dout);
-            const float* f = fw_at(row) + 8 * hv;
-            const float4 d0 = *reinterpret_cast<const float4*>(f);
-            const float4 d1 = *reinterpret_cast<const float4*>(f + 4);
-            const float4 w0 = *reinterpret_cast<const float4*>(f + kSliceV);
-            const float4 w1 = *reinterpret_cast<const float4*>(f + kSliceV + 4);
-            const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-            const float vr[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            float sp[8], sprev[8];
-            {
-                const float4 p0 = *reinterpret_cast<const float4*>(&S.st[i][tid][0]);
-                const float4 p1 = *reinterpret_cast<const float4*>(&S.st[i][tid][4]);
-                sprev[0] = p0.x; sprev[1] = p0.y; sprev[2] = p0.z; sprev[3] = p0.w;
-                sprev[4] = p1.x; sprev[5] = p1.y; sprev[6] = p1.z; sprev[7] = p1.w;
-            }
-            float dq = 0.0f, dk = 0.0f, da = 0.0f;
-            float dd[8];
+            const int gi = (len - 1 - i) % kGroup;   // slot of this token in its group
+            const float4 a0 = *reinterpret_cast<const float4*>(&S.a[i][k0]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&S.a[i][k0 + 4]);
+            const float4 k0v = *reinterpret_cast<const float4*>(&S.kk[i][k0]);
+            const float4 k1v = *reinterpret_cast<const float4*>(&S.kk[i][k0 + 4]);
+            const float4 q0 = *reinterpret_cast<const float4*>(&S.qq[i][k0]);
+            const float4 q1 = *reinterpret_cast<const float4*>(&S.qq[i][k0 + 4]);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float kk[8] = {k0v.x, k0v.y, k0v.z, k0v.w, k1v.x, k1v.y, k1v.z, k1v.w};
+            const float qq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            const float d = S.fw[i][jv], vr = S.fw[i][kSliceV + jv];
+            const float dout = S.vv[i][jv], b = S.b[i];
+            const float4 p0 = S.st[i][0][tid];
+            const float4 p1 = S.st[i][1][tid];
+            const float sprev[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            float sp[8], dq[8], dk[8], da[8];
+            float dd = 0.0f;
+            const float sdo = P.scale * dout;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                sp[e] = a * sprev[e];
-                const float snow = fmaf(kk, d[e], sp[e]);
-                dS[e] = fmaf(P.scale * qq, dout[e], dS[e]);
-                dq = fmaf(snow, dout[e], dq);
-                dk = fmaf(dS[e], d[e], dk);
-                dd[e] = dS[e] * kk;
+                sp[e] = a[e] * sprev[e];
+                dq[e] = fmaf(kk[e], d, sp[e]) * dout;   // S_t dO (scale applied at the end)
+                dS[e] = fmaf(qq[e], sdo, dS[e]);
+                dk[e] = dS[e] * d;
+                dd = fmaf(dS[e], kk[e], dd);
             }
-            key_sum(dd, S, buf, warp, lane);
-            buf ^= 1;
-            float db = 0.0f;
+            dd += __shfl_xor_sync(0xffffffffu, dd, 1);   // dd = dS^T k over the 128 keys
+            dd += __shfl_xor_sync(0xffffffffu, dd, 2);
+            dd += __shfl_xor_sync(0xffffffffu, dd, 4);
+            dd += __shfl_xor_sync(0xffffffffu, dd, 8);
+            const float dr = -b * dd;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                db = fmaf(dd[e], vr[e], db);
-                const float dr = -b * dd[e];
-                const float dsp = fmaf(kk, dr, dS[e]);
-                dk = fmaf(sp[e], dr, dk);
-                da = fmaf(dsp, sprev[e], da);
-                dS[e] = a * dsp;
+                const float dsp = fmaf(kk[e], dr, dS[e]);
+                dk[e] = fmaf(sp[e], dr, dk[e]);
+                da[e] = dsp * sprev[e];
+                dS[e] = a[e] * dsp;
             }
-            if (key == 0) {   // dv of the slice's 16 columns
-                float* o = P.dv + rk + col;
-                *reinterpret_cast<float4*>(o) = make_float4(b * dd[0], b * dd[1], b * dd[2], b * dd[3]);
-                *reinterpret_cast<float4*>(o + 4) = make_float4(b * dd[4], b * dd[5], b * dd[6], b * dd[7]);
+            float db = dd * vr;
+            const size_t row = row0 + i;
+            if (kb == 0) P.dv[(row * P.H + h) * kDim + col0 + jv] = b * dd;
+            // the warp's two columns (lanes l and l ^ 16) added, then kept for the group
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                dq[e] += __shfl_xor_sync(0xffffffffu, dq[e], 16);
+                dk[e] += __shfl_xor_sync(0xffffffffu, dk[e], 16);
+                da[e] += __shfl_xor_sync(0xffffffffu, da[e], 16);
             }
-            // the two halves of a key: add their partial sums
-            dq += __shfl_xor_sync(0xffffffffu, dq, 1);
-            dk += __shfl_xor_sync(0xffffffffu, dk, 1);
-            da += __shfl_xor_sync(0xffffffffu, da, 1);
-            db += __shfl_xor_sync(0xffffffffu, db, 1);
-            float* part = P.part + ((row * P.H + h) * kSlices + slice) * kPart;
-            if (hv == 0) {
-                part[key] = P.scale * dq;
-                part[kDim + key] = dk;
-                part[2 * kDim + key] = da;
+            db += __shfl_xor_sync(0xffffffffu, db, 16);
+            if (lane < 16) {
+                float* gp = S.grp[gi][warp];
+                *reinterpret_cast<float4*>(gp + k0) = make_float4(dq[0], dq[1], dq[2], dq[3]);
+                *reinterpret_cast<float4*>(gp + k0 + 4) = make_float4(dq[4], dq[5], dq[6], dq[7]);
+                *reinterpret_cast<float4*>(gp + kDim + k0) = make_float4(dk[0], dk[1], dk[2], dk[3]);
+                *reinterpret_cast<float4*>(gp + kDim + k0 + 4) = make_float4(dk[4], dk[5], dk[6], dk[7]);
+                *reinterpret_cast<float4*>(gp + 2 * kDim + k0) = make_float4(da[0], da[1], da[2], da[3]);
+                *reinterpret_cast<float4*>(gp + 2 * kDim + k0 + 4) = make_float4(da[4], da[5], da[6], da[7]);
+                if (lane == 0) gp[3 * kDim] = db;
             }
-            if (tid == 0) part[3 * kDim] = db;
+            if (gi == kGroup - 1 || i == 0) {
+                // the group's tokens (rows row .. row + gi): sum the 8 warps in order and
+                // write this slice's partial sums
+                __syncthreads();
+                for (int g = 0; g <= gi; ++g) {
+                    const size_t grow = row + gi - g;   // slot g holds the g-th token walked
+                    float* out = P.part + ((grow * P.H + h) * kSlices + slice) * kPart;
+                    for (int e = tid; e < 3 * kDim + 1; e += kBwdThreads) {
+                        float sum = 0.0f;
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) sum += S.grp[g][w][e];
+                        out[e] = e < kDim ? P.scale * sum : sum;
+                    }
+                }
+                __syncthreads();
+            }
         }
-        __syncthreads();   // the chunk's rebuilt states are overwritten by the next one
+        __syncthreads();   // the block's staged rows and states are replaced by the next one
     }
     if (P.d_init) {
-        float* o = P.d_init + sidx;
-        *reinterpret_cast<float4*>(o) = make_float4(dS[0], dS[1], dS[2], dS[3]);
-        *reinterpret_cast<float4*>(o + 4) = make_float4(dS[4], dS[5], dS[6], dS[7]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            P.d_init[(((size_t)n * P.H + h) * kDim + k0 + e) * kDim + col0 + jv] = dS[e];
     }
 }
 
@@ -337,7 +401,7 @@ std::atomic<bool> g_bwd_attr[64];
 
 size_t bwd_scratch_floats(int N, long long rows, int H, size_t* ck, size_t* fw, size_t* part,
                           size_t* blk) {
-    const long long slots = N + rows / kChunk + 1;
+    const long long slots = N + rows / kBC + 1;
     *ck = (size_t)slots * H * kSlices * kDim * kSliceV;
     *fw = (size_t)rows * H * kSlices * 2 * kSliceV;
     *part = (size_t)rows * H * kSlices * kPart;
