@@ -59,24 +59,6 @@ struct BwdSmem {
 
 __device__ __forceinline__ float bf(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
 
-__device__ __forceinline__ void load4_bf16(const __nv_bfloat16* p, float (&x)[4]) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(p);
-    x[0] = __uint_as_float(raw.x << 16);
-    x[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-    x[2] = __uint_as_float(raw.y << 16);
-    x[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-}
-
-__device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float (&x)[8]) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        x[2 * i] = __uint_as_float(w[i] << 16);
-        x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-}
-
 __device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 // the decay of key channel c at token row t, and x (the sigmoid's argument)
@@ -93,52 +75,109 @@ __device__ __forceinline__ long long ck_slot(int n, long long bos, int c) {
     return (long long)n + c + bos / kBC;
 }
 
-// A block's token rows into shared memory, all threads at once (one memory latency
-// per 8 tokens): keys and decays (and queries on the way back), the slice's 16 values
-// (or dL/d(out)), b, and on the way back the stored d and v - r.  Rows past the
-// sequence's end are not read.
-__device__ __forceinline__ void stage(const BwdProblem& P, BwdSmem& S, long long row0, int len,
-                                      int h, int col0, float eA, bool reverse,
-                                      const float* fw0, size_t fw_step) {
+// Position of key channel c in the staged rows and in the per-warp column sums: the 8
+// keys of key block kb = c / 8 sit in two planes, keys 0-3 at 4 kb and keys 4-7 at
+// 64 + 4 kb, so that the 16 key blocks of a warp read or write 16 consecutive float4 per
+// plane (no bank conflicts).  kkey is the inverse.
+__device__ __forceinline__ int kpos(int c) { return ((c & 4) << 4) + ((c >> 3) << 2) + (c & 3); }
+__device__ __forceinline__ int kkey(int p) { return ((p & 63) >> 2) * 8 + ((p >> 6) << 2) + (p & 3); }
+
+// A block's raw token rows, loaded into registers one block ahead of their use, so that
+// their memory latency overlaps the block before: keys, gate inputs (and queries on the
+// way back) as thread (row, 4 channels); in x, the slice's 16 values or dL/d(out)
+// (threads 0-15, 8 columns each), the beta logit (threads 16-23) or the stored d and
+// v - r on the way back (threads 128-191, 4 floats each).  Rows past the sequence's end
+// are not read.
+struct Rows {
+    uint2 k, g, q;
+    uint4 x;
+};
+
+__device__ __forceinline__ void fetch(const BwdProblem& P, Rows& R, long long row0, int len,
+                                      int h, int col0, bool reverse, const float* fw0,
+                                      size_t fw_step) {
     const int tid = threadIdx.x;
-    {   // 8 rows x 128 channels: thread = (row, 4 channels)
-        const int i = tid >> 5, c4 = 4 * (tid & 31);
-        if (i < len) {
-            const size_t rk = ((size_t)(row0 + i) * P.H + h) * kDim + c4;
-            float kx[4], gx[4], a[4];
-            load4_bf16(P.k + rk, kx);
-            load4_bf16(P.g + rk, gx);
-            const float* db = P.dt_bias + (size_t)h * kDim + c4;   // 4-byte aligned only
+    const int i = tid >> 5, c4 = 4 * (tid & 31);
+    if (i < len) {
+        const size_t rk = ((size_t)(row0 + i) * P.H + h) * kDim + c4;
+        R.k = *reinterpret_cast<const uint2*>(P.k + rk);
+        R.g = *reinterpret_cast<const uint2*>(P.g + rk);
+        if (reverse) R.q = *reinterpret_cast<const uint2*>(P.q + rk);
+    }
+    if (tid < 2 * kBC) {
+        const int r = tid >> 1, hv = tid & 1;
+        if (r < len) {
+            const size_t rv = ((size_t)(row0 + r) * P.H + h) * kDim + col0 + 8 * hv;
+            R.x = *reinterpret_cast<const uint4*>(reverse ? P.dout + rv : P.v + rv);
+        }
+    } else if (tid < 3 * kBC) {
+        const int r = tid - 2 * kBC;
+        if (r < len) R.x.x = __float_as_uint(bf(P.beta, (size_t)(row0 + r) * P.H + h));
+    } else if (reverse && tid >= 128 && tid < 128 + 8 * kBC) {
+        const int r = (tid - 128) >> 3, f4 = 4 * ((tid - 128) & 7);
+        if (r < len) R.x = *reinterpret_cast<const uint4*>(fw0 + (size_t)r * fw_step + f4);
+    }
+}
+
+__device__ __forceinline__ void unpack4(uint2 w, float (&x)[4]) {
+    x[0] = __uint_as_float(w.x << 16);
+    x[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(w.y << 16);
+    x[3] = __uint_as_float(w.y & 0xFFFF0000u);
+}
+
+// The fetched rows into shared memory (decays and b formed on the way), then a barrier.
+// dtb: dt_bias of the thread's 4 channels.
+__device__ __forceinline__ void commit(BwdSmem& S, const Rows& R, int len, float eA,
+                                       float lower_bound, const float (&dtb)[4], bool reverse) {
+    const int tid = threadIdx.x;
+    const int i = tid >> 5, p = kpos(4 * (tid & 31));
+    if (i < len) {
+        float kx[4], gx[4], a[4];
+        unpack4(R.k, kx);
+        unpack4(R.g, gx);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) a[e] = expf(P.lower_bound * sigm(eA * (gx[e] + db[e])));
-            *reinterpret_cast<float4*>(&S.a[i][c4]) = make_float4(a[0], a[1], a[2], a[3]);
-            *reinterpret_cast<float4*>(&S.kk[i][c4]) = make_float4(kx[0], kx[1], kx[2], kx[3]);
-            if (reverse) {
-                float qx[4];
-                load4_bf16(P.q + rk, qx);
-                *reinterpret_cast<float4*>(&S.qq[i][c4]) = make_float4(qx[0], qx[1], qx[2], qx[3]);
-            }
+        for (int e = 0; e < 4; ++e) a[e] = expf(lower_bound * sigm(eA * (gx[e] + dtb[e])));
+        *reinterpret_cast<float4*>(&S.a[i][p]) = make_float4(a[0], a[1], a[2], a[3]);
+        *reinterpret_cast<float4*>(&S.kk[i][p]) = make_float4(kx[0], kx[1], kx[2], kx[3]);
+        if (reverse) {
+            float qx[4];
+            unpack4(R.q, qx);
+            *reinterpret_cast<float4*>(&S.qq[i][p]) = make_float4(qx[0], qx[1], qx[2], qx[3]);
         }
     }
-    if (tid < 2 * kBC) {   // the slice's 16 columns of v (or dO): thread = (row, 8 columns)
-        const int i = tid >> 1, hv = tid & 1;
-        if (i < len) {
-            const size_t rv = ((size_t)(row0 + i) * P.H + h) * kDim + col0 + 8 * hv;
-            float x[8];
-            load8_bf16(reverse ? P.dout + rv : P.v + rv, x);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) S.vv[i][8 * hv + e] = x[e];
+    if (tid < 2 * kBC) {
+        const int r = tid >> 1, hv = tid & 1;
+        if (r < len) {
+            float lo[4], hi[4];
+            unpack4(make_uint2(R.x.x, R.x.y), lo);
+            unpack4(make_uint2(R.x.z, R.x.w), hi);
+            *reinterpret_cast<float4*>(&S.vv[r][8 * hv]) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<float4*>(&S.vv[r][8 * hv + 4]) = make_float4(hi[0], hi[1], hi[2], hi[3]);
         }
-    } else if (tid < 3 * kBC) {   // b of each row
-        const int i = tid - 2 * kBC;
-        if (i < len) S.b[i] = sigm(bf(P.beta, (size_t)(row0 + i) * P.H + h));
-    } else if (reverse && tid >= 128 && tid < 128 + 8 * kBC) {   // d and v - r: (row, 4 floats)
-        const int i = (tid - 128) >> 3, f4 = 4 * ((tid - 128) & 7);
-        if (i < len)
-            *reinterpret_cast<float4*>(&S.fw[i][f4]) =
-                *reinterpret_cast<const float4*>(fw0 + (size_t)i * fw_step + f4);
+    } else if (tid < 3 * kBC) {
+        const int r = tid - 2 * kBC;
+        if (r < len) S.b[r] = sigm(__uint_as_float(R.x.x));
+    } else if (reverse && tid >= 128 && tid < 128 + 8 * kBC) {
+        const int r = (tid - 128) >> 3, f4 = 4 * ((tid - 128) & 7);
+        if (r < len)
+            *reinterpret_cast<float4*>(&S.fw[r][f4]) =
+                make_float4(__uint_as_float(R.x.x), __uint_as_float(R.x.y),
+                            __uint_as_float(R.x.z), __uint_as_float(R.x.w));
     }
     __syncthreads();
+}
+
+__device__ __forceinline__ void ld_planes(const float* row, int pk, float (&x)[8]) {
+    const float4 u = *reinterpret_cast<const float4*>(row + pk);
+    const float4 w = *reinterpret_cast<const float4*>(row + 64 + pk);
+    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    x[4] = w.x; x[5] = w.y; x[6] = w.z; x[7] = w.w;
+}
+
+__device__ __forceinline__ void st_planes(float* row, int pk, const float (&x)[8]) {
+    *reinterpret_cast<float4*>(row + pk) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(row + 64 + pk) = make_float4(x[4], x[5], x[6], x[7]);
 }
 
 __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const int* valid) {
@@ -158,13 +197,20 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
     const auto fw_at = [&](size_t row) {   // d (16) and v - r (16) of this slice at a row
         return P.fw + ((row * P.H + h) * kSlices + slice) * (2 * kSliceV);
     };
+    const auto ck_at = [&](int c) {        // checkpoint of block c: [key][16 columns]
+        return P.ck + ((ck_slot(n, bos, c) * P.H + h) * kSlices + slice) * (kDim * kSliceV);
+    };
+    float dtb[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dtb[e] = P.dt_bias[(size_t)h * kDim + 4 * (tid & 31) + e];
+    // Thread (column jv = tid / 16, key block kb = tid % 16) holds S[8 kb .. + 7][jv] in
+    // both phases: a warp holds all 128 keys of two columns, so r = S'^T k and dd = dS^T k
+    // are sums over 16 lanes (four shuffles, no barrier per token).
+    const int jv = tid >> 4, kb = tid & 15, k0 = 8 * kb, pk = 4 * kb;
+    Rows R{};
 
     // ---- phase 1: forward over the slice, checkpoints and per-token d, v - r ----------
-    // Here thread (column jv = tid / 16, key block kb = tid % 16) holds S[8 kb .. + 7][jv]:
-    // a warp holds all 128 keys of two columns, so r = S'^T k is a sum over 16 lanes
-    // (four shuffles, no barrier per token).
     {
-        const int jv = tid >> 4, kb = tid & 15, k0 = 8 * kb;
         float st[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -176,21 +222,20 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
             }
             st[e] = x;
         }
+        if (nch > 0) fetch(P, R, bos, min(kBC, L), h, col0, false, nullptr, 0);
         for (int c = 0; c < nch; ++c) {
-            // checkpoint [key][16 columns] of the slice (read back by thread (key, half))
-            float* ck = P.ck + ((ck_slot(n, bos, c) * P.H + h) * kSlices + slice) * (kDim * kSliceV);
+            float* ck = ck_at(c);
 #pragma unroll
             for (int e = 0; e < 8; ++e) ck[(k0 + e) * kSliceV + jv] = st[e];
             const int len = min(kBC, L - c * kBC);
             const long long row0 = bos + (long long)c * kBC;
-            stage(P, S, row0, len, h, col0, eA, false, nullptr, 0);
+            commit(S, R, len, eA, P.lower_bound, dtb, false);
+            if (c + 1 < nch)
+                fetch(P, R, row0 + kBC, min(kBC, L - (c + 1) * kBC), h, col0, false, nullptr, 0);
             for (int i = 0; i < len; ++i) {
-                const float4 a0 = *reinterpret_cast<const float4*>(&S.a[i][k0]);
-                const float4 a1 = *reinterpret_cast<const float4*>(&S.a[i][k0 + 4]);
-                const float4 q0 = *reinterpret_cast<const float4*>(&S.kk[i][k0]);
-                const float4 q1 = *reinterpret_cast<const float4*>(&S.kk[i][k0 + 4]);
-                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float kk[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                float a[8], kk[8];
+                ld_planes(S.a[i], pk, a);
+                ld_planes(S.kk[i], pk, kk);
                 float r = 0.0f;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -214,49 +259,51 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
             __syncthreads();   // the staged rows are replaced by the next block's
         }
     }
-    __syncthreads();   // checkpoints, d and v - r are read by other threads below
+    __syncthreads();   // d and v - r are read by other threads below
 
-    // ---- phase 2: reverse, in the same layout: thread (column jv, keys 8 kb .. + 7) ----
-    const int jv = tid >> 4, kb = tid & 15, k0 = 8 * kb;
-    float dS[8];
+    // ---- phase 2: reverse, block by block from the last ---------------------------------
+    float dS[8], ckn[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e)
         dS[e] = P.dfinal ? P.dfinal[(((size_t)n * P.H + h) * kDim + k0 + e) * kDim + col0 + jv] : 0.0f;
+    if (nch > 0) {
+        const long long row0 = bos + (long long)(nch - 1) * kBC;
+        fetch(P, R, row0, L - (nch - 1) * kBC, h, col0, true, fw_at(row0), fw_step);
+        const float* ck = ck_at(nch - 1);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ckn[e] = ck[(k0 + e) * kSliceV + jv];   // written by this thread
+    }
     for (int c = nch - 1; c >= 0; --c) {
         const int len = min(kBC, L - c * kBC);
         const long long row0 = bos + (long long)c * kBC;
-        stage(P, S, row0, len, h, col0, eA, true, fw_at(row0), fw_step);
-        {   // rebuild the block's states S_{t-1} from the checkpoint (element-wise)
-            const float* ck = P.ck + ((ck_slot(n, bos, c) * P.H + h) * kSlices + slice) * (kDim * kSliceV);
-            float sv[8];
+        commit(S, R, len, eA, P.lower_bound, dtb, true);
+        float sv[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) sv[e] = ck[(k0 + e) * kSliceV + jv];
-            for (int i = 0; i < len; ++i) {
-                S.st[i][0][tid] = make_float4(sv[0], sv[1], sv[2], sv[3]);
-                S.st[i][1][tid] = make_float4(sv[4], sv[5], sv[6], sv[7]);
-                const float d = S.fw[i][jv];
-                const float4 a0 = *reinterpret_cast<const float4*>(&S.a[i][k0]);
-                const float4 a1 = *reinterpret_cast<const float4*>(&S.a[i][k0 + 4]);
-                const float4 k0v = *reinterpret_cast<const float4*>(&S.kk[i][k0]);
-                const float4 k1v = *reinterpret_cast<const float4*>(&S.kk[i][k0 + 4]);
-                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float kk[8] = {k0v.x, k0v.y, k0v.z, k0v.w, k1v.x, k1v.y, k1v.z, k1v.w};
+        for (int e = 0; e < 8; ++e) sv[e] = ckn[e];
+        if (c > 0) {   // the block before is whole
+            fetch(P, R, row0 - kBC, kBC, h, col0, true, fw_at(row0 - kBC), fw_step);
+            const float* ck = ck_at(c - 1);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) sv[e] = fmaf(kk[e], d, a[e] * sv[e]);
-            }
+            for (int e = 0; e < 8; ++e) ckn[e] = ck[(k0 + e) * kSliceV + jv];
         }
-        // (each thread reads only its own rebuilt states)
+        // rebuild the block's states S_{t-1} from the checkpoint (element-wise, the same
+        // arithmetic as phase 1; each thread reads back only its own states)
+        for (int i = 0; i < len; ++i) {
+            S.st[i][0][tid] = make_float4(sv[0], sv[1], sv[2], sv[3]);
+            S.st[i][1][tid] = make_float4(sv[4], sv[5], sv[6], sv[7]);
+            const float d = S.fw[i][jv];
+            float a[8], kk[8];
+            ld_planes(S.a[i], pk, a);
+            ld_planes(S.kk[i], pk, kk);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sv[e] = fmaf(kk[e], d, a[e] * sv[e]);
+        }
         for (int i = len - 1; i >= 0; --i) {
             const int gi = (len - 1 - i) % kGroup;   // slot of this token in its group
-            const float4 a0 = *reinterpret_cast<const float4*>(&S.a[i][k0]);
-            const float4 a1 = *reinterpret_cast<const float4*>(&S.a[i][k0 + 4]);
-            const float4 k0v = *reinterpret_cast<const float4*>(&S.kk[i][k0]);
-            const float4 k1v = *reinterpret_cast<const float4*>(&S.kk[i][k0 + 4]);
-            const float4 q0 = *reinterpret_cast<const float4*>(&S.qq[i][k0]);
-            const float4 q1 = *reinterpret_cast<const float4*>(&S.qq[i][k0 + 4]);
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float kk[8] = {k0v.x, k0v.y, k0v.z, k0v.w, k1v.x, k1v.y, k1v.z, k1v.w};
-            const float qq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            float a[8], kk[8], qq[8];
+            ld_planes(S.a[i], pk, a);
+            ld_planes(S.kk[i], pk, kk);
+            ld_planes(S.qq[i], pk, qq);
             const float d = S.fw[i][jv], vr = S.fw[i][kSliceV + jv];
             const float dout = S.vv[i][jv], b = S.b[i];
             const float4 p0 = S.st[i][0][tid];
@@ -298,17 +345,14 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
             db += __shfl_xor_sync(0xffffffffu, db, 16);
             if (lane < 16) {
                 float* gp = S.grp[gi][warp];
-                *reinterpret_cast<float4*>(gp + k0) = make_float4(dq[0], dq[1], dq[2], dq[3]);
-                *reinterpret_cast<float4*>(gp + k0 + 4) = make_float4(dq[4], dq[5], dq[6], dq[7]);
-                *reinterpret_cast<float4*>(gp + kDim + k0) = make_float4(dk[0], dk[1], dk[2], dk[3]);
-                *reinterpret_cast<float4*>(gp + kDim + k0 + 4) = make_float4(dk[4], dk[5], dk[6], dk[7]);
-                *reinterpret_cast<float4*>(gp + 2 * kDim + k0) = make_float4(da[0], da[1], da[2], da[3]);
-                *reinterpret_cast<float4*>(gp + 2 * kDim + k0 + 4) = make_float4(da[4], da[5], da[6], da[7]);
+                st_planes(gp, pk, dq);
+                st_planes(gp + kDim, pk, dk);
+                st_planes(gp + 2 * kDim, pk, da);
                 if (lane == 0) gp[3 * kDim] = db;
             }
             if (gi == kGroup - 1 || i == 0) {
                 // the group's tokens (rows row .. row + gi): sum the 8 warps in order and
-                // write this slice's partial sums
+                // write this slice's partial sums in key order
                 __syncthreads();
                 for (int g = 0; g <= gi; ++g) {
                     const size_t grow = row + gi - g;   // slot g holds the g-th token walked
@@ -317,7 +361,8 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
                         float sum = 0.0f;
 #pragma unroll
                         for (int w = 0; w < 8; ++w) sum += S.grp[g][w][e];
-                        out[e] = e < kDim ? P.scale * sum : sum;
+                        const int sec = e >> 7;   // dq, dk, da, db
+                        out[sec * kDim + kkey(e & (kDim - 1))] = sec == 0 ? P.scale * sum : sum;
                     }
                 }
                 __syncthreads();

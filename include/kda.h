@@ -211,7 +211,7 @@ int kda_fwd_host(const void* q, const void* k, const void* v, const void* g,
  * Outputs must not overlap the inputs or each other (KDA_ERR_ALIAS); q, k, v, g,
  * d_out, dv and d_initial_state must be 16-byte aligned.  Scratch:
  * kda_bwd_workspace_bytes() from the stream-ordered allocator (state checkpoints every
- * 16 tokens, each token's d and v - r, per-slice partial sums; about 13 KB per token
+ * 8 tokens, each token's d and v - r, per-slice partial sums; about 21 KB per token
  * and head).  Asynchronous on `stream`; a malformed cu_seqlens sets KDA_ERR_BAD_SEQLENS
  * in the error word and writes nothing.  Results are deterministic (fixed summation
  * order).  The work: 8 CTAs per (sequence, head), each owning 16 value columns of the
