@@ -168,16 +168,51 @@ __device__ __forceinline__ void commit(BwdSmem& S, const Rows& R, int len, float
     __syncthreads();
 }
 
-__device__ __forceinline__ void ld_planes(const float* row, int pk, float (&x)[8]) {
-    const float4 u = *reinterpret_cast<const float4*>(row + pk);
-    const float4 w = *reinterpret_cast<const float4*>(row + 64 + pk);
-    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
-    x[4] = w.x; x[5] = w.y; x[6] = w.z; x[7] = w.w;
+// Packed fp32 pairs (one instruction for two lanes' worth of arithmetic), each with an
+// explicit round-to-nearest so that no multiply and add are fused behind the code's
+// back: phase 2 replays phase 1's state updates and must get the same bits.
+__device__ __forceinline__ unsigned long long pk2(float2 a) {
+    unsigned long long x;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    return x;
+}
+__device__ __forceinline__ float2 upk2(unsigned long long x) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(x));
+    return r;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    unsigned long long z;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(z) : "l"(pk2(a)), "l"(pk2(b)));
+    return upk2(z);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    unsigned long long z;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(z) : "l"(pk2(a)), "l"(pk2(b)));
+    return upk2(z);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    unsigned long long z;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(z) : "l"(pk2(a)), "l"(pk2(b)), "l"(pk2(c)));
+    return upk2(z);
+}
+__device__ __forceinline__ float2 dup2(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float2 shfl16(float2 a) {
+    return make_float2(__shfl_xor_sync(0xffffffffu, a.x, 16), __shfl_xor_sync(0xffffffffu, a.y, 16));
 }
 
-__device__ __forceinline__ void st_planes(float* row, int pk, const float (&x)[8]) {
-    *reinterpret_cast<float4*>(row + pk) = make_float4(x[0], x[1], x[2], x[3]);
-    *reinterpret_cast<float4*>(row + 64 + pk) = make_float4(x[4], x[5], x[6], x[7]);
+// A thread's 8 keys of a staged row (or of a column-sum row) as 4 pairs: keys 8 kb + 0-3
+// from the first plane, 4-7 from the second.
+__device__ __forceinline__ void ld_planes(const float* row, int pk, float2 (&x)[4]) {
+    const float4 u = *reinterpret_cast<const float4*>(row + pk);
+    const float4 w = *reinterpret_cast<const float4*>(row + 64 + pk);
+    x[0] = make_float2(u.x, u.y); x[1] = make_float2(u.z, u.w);
+    x[2] = make_float2(w.x, w.y); x[3] = make_float2(w.z, w.w);
+}
+
+__device__ __forceinline__ void st_planes(float* row, int pk, const float2 (&x)[4]) {
+    *reinterpret_cast<float4*>(row + pk) = make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
+    *reinterpret_cast<float4*>(row + 64 + pk) = make_float4(x[2].x, x[2].y, x[3].x, x[3].y);
 }
 
 __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const int* valid) {
@@ -211,7 +246,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
 
     // ---- phase 1: forward over the slice, checkpoints and per-token d, v - r ----------
     {
-        float st[8];
+        float2 st[4];   // keys k0 + 2e, k0 + 2e + 1
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             float x = 0.0f;
@@ -220,28 +255,31 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
                 x = P.init_dtype == KDA_F32 ? static_cast<const float*>(P.init_state)[si]
                                             : __bfloat162float(static_cast<const __nv_bfloat16*>(P.init_state)[si]);
             }
-            st[e] = x;
+            if (e & 1) st[e >> 1].y = x; else st[e >> 1].x = x;
         }
         if (nch > 0) fetch(P, R, bos, min(kBC, L), h, col0, false, nullptr, 0);
         for (int c = 0; c < nch; ++c) {
             float* ck = ck_at(c);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ck[(k0 + e) * kSliceV + jv] = st[e];
+            for (int e = 0; e < 4; ++e) {
+                ck[(k0 + 2 * e) * kSliceV + jv] = st[e].x;
+                ck[(k0 + 2 * e + 1) * kSliceV + jv] = st[e].y;
+            }
             const int len = min(kBC, L - c * kBC);
             const long long row0 = bos + (long long)c * kBC;
             commit(S, R, len, eA, P.lower_bound, dtb, false);
             if (c + 1 < nch)
                 fetch(P, R, row0 + kBC, min(kBC, L - (c + 1) * kBC), h, col0, false, nullptr, 0);
             for (int i = 0; i < len; ++i) {
-                float a[8], kk[8];
+                float2 a[4], kk[4], r2 = make_float2(0.0f, 0.0f);
                 ld_planes(S.a[i], pk, a);
                 ld_planes(S.kk[i], pk, kk);
-                float r = 0.0f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    st[e] *= a[e];
-                    r = fmaf(st[e], kk[e], r);
+                for (int e = 0; e < 4; ++e) {
+                    st[e] = mul2(st[e], a[e]);
+                    r2 = fma2(st[e], kk[e], r2);
                 }
+                float r = r2.x + r2.y;
                 r += __shfl_xor_sync(0xffffffffu, r, 1);
                 r += __shfl_xor_sync(0xffffffffu, r, 2);
                 r += __shfl_xor_sync(0xffffffffu, r, 4);
@@ -249,7 +287,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
                 const float vr = S.vv[i][jv] - r;
                 const float d = S.b[i] * vr;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) st[e] = fmaf(kk[e], d, st[e]);
+                for (int e = 0; e < 4; ++e) st[e] = fma2(kk[e], dup2(d), st[e]);
                 if (kb == 0) {   // lanes 0 and 16: this column's d and v - r
                     float* f = fw_at(row0 + i);
                     f[jv] = d;
@@ -262,10 +300,14 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
     __syncthreads();   // d and v - r are read by other threads below
 
     // ---- phase 2: reverse, block by block from the last ---------------------------------
-    float dS[8], ckn[8];
+    float2 dS[4];
+    float ckn[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-        dS[e] = P.dfinal ? P.dfinal[(((size_t)n * P.H + h) * kDim + k0 + e) * kDim + col0 + jv] : 0.0f;
+    for (int e = 0; e < 8; ++e) {
+        const float x =
+            P.dfinal ? P.dfinal[(((size_t)n * P.H + h) * kDim + k0 + e) * kDim + col0 + jv] : 0.0f;
+        if (e & 1) dS[e >> 1].y = x; else dS[e >> 1].x = x;
+    }
     if (nch > 0) {
         const long long row0 = bos + (long long)(nch - 1) * kBC;
         fetch(P, R, row0, L - (nch - 1) * kBC, h, col0, true, fw_at(row0), fw_step);
@@ -277,9 +319,9 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
         const int len = min(kBC, L - c * kBC);
         const long long row0 = bos + (long long)c * kBC;
         commit(S, R, len, eA, P.lower_bound, dtb, true);
-        float sv[8];
+        float2 sv[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) sv[e] = ckn[e];
+        for (int e = 0; e < 4; ++e) sv[e] = make_float2(ckn[2 * e], ckn[2 * e + 1]);
         if (c > 0) {   // the block before is whole
             fetch(P, R, row0 - kBC, kBC, h, col0, true, fw_at(row0 - kBC), fw_step);
             const float* ck = ck_at(c - 1);
@@ -289,18 +331,18 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
         // rebuild the block's states S_{t-1} from the checkpoint (element-wise, the same
         // arithmetic as phase 1; each thread reads back only its own states)
         for (int i = 0; i < len; ++i) {
-            S.st[i][0][tid] = make_float4(sv[0], sv[1], sv[2], sv[3]);
-            S.st[i][1][tid] = make_float4(sv[4], sv[5], sv[6], sv[7]);
+            S.st[i][0][tid] = make_float4(sv[0].x, sv[0].y, sv[1].x, sv[1].y);
+            S.st[i][1][tid] = make_float4(sv[2].x, sv[2].y, sv[3].x, sv[3].y);
             const float d = S.fw[i][jv];
-            float a[8], kk[8];
+            float2 a[4], kk[4];
             ld_planes(S.a[i], pk, a);
             ld_planes(S.kk[i], pk, kk);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) sv[e] = fmaf(kk[e], d, a[e] * sv[e]);
+            for (int e = 0; e < 4; ++e) sv[e] = fma2(kk[e], dup2(d), mul2(sv[e], a[e]));
         }
         for (int i = len - 1; i >= 0; --i) {
             const int gi = (len - 1 - i) % kGroup;   // slot of this token in its group
-            float a[8], kk[8], qq[8];
+            float2 a[4], kk[4], qq[4];
             ld_planes(S.a[i], pk, a);
             ld_planes(S.kk[i], pk, kk);
             ld_planes(S.qq[i], pk, qq);
@@ -308,39 +350,40 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
             const float dout = S.vv[i][jv], b = S.b[i];
             const float4 p0 = S.st[i][0][tid];
             const float4 p1 = S.st[i][1][tid];
-            const float sprev[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-            float sp[8], dq[8], dk[8], da[8];
-            float dd = 0.0f;
-            const float sdo = P.scale * dout;
+            const float2 sprev[4] = {make_float2(p0.x, p0.y), make_float2(p0.z, p0.w),
+                                     make_float2(p1.x, p1.y), make_float2(p1.z, p1.w)};
+            float2 sp[4], dq[4], dk[4], da[4], dd2 = make_float2(0.0f, 0.0f);
+            const float2 d2 = dup2(d), do2 = dup2(dout), sdo2 = dup2(P.scale * dout);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                sp[e] = a[e] * sprev[e];
-                dq[e] = fmaf(kk[e], d, sp[e]) * dout;   // S_t dO (scale applied at the end)
-                dS[e] = fmaf(qq[e], sdo, dS[e]);
-                dk[e] = dS[e] * d;
-                dd = fmaf(dS[e], kk[e], dd);
+            for (int e = 0; e < 4; ++e) {
+                sp[e] = mul2(sprev[e], a[e]);
+                dq[e] = mul2(fma2(kk[e], d2, sp[e]), do2);   // S_t dO (scale applied at the end)
+                dS[e] = fma2(qq[e], sdo2, dS[e]);
+                dk[e] = mul2(dS[e], d2);
+                dd2 = fma2(dS[e], kk[e], dd2);
             }
+            float dd = dd2.x + dd2.y;
             dd += __shfl_xor_sync(0xffffffffu, dd, 1);   // dd = dS^T k over the 128 keys
             dd += __shfl_xor_sync(0xffffffffu, dd, 2);
             dd += __shfl_xor_sync(0xffffffffu, dd, 4);
             dd += __shfl_xor_sync(0xffffffffu, dd, 8);
-            const float dr = -b * dd;
+            const float2 dr2 = dup2(-b * dd);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float dsp = fmaf(kk[e], dr, dS[e]);
-                dk[e] = fmaf(sp[e], dr, dk[e]);
-                da[e] = dsp * sprev[e];
-                dS[e] = a[e] * dsp;
+            for (int e = 0; e < 4; ++e) {
+                const float2 dsp = fma2(kk[e], dr2, dS[e]);
+                dk[e] = fma2(sp[e], dr2, dk[e]);
+                da[e] = mul2(dsp, sprev[e]);
+                dS[e] = mul2(a[e], dsp);
             }
             float db = dd * vr;
             const size_t row = row0 + i;
             if (kb == 0) P.dv[(row * P.H + h) * kDim + col0 + jv] = b * dd;
             // the warp's two columns (lanes l and l ^ 16) added, then kept for the group
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                dq[e] += __shfl_xor_sync(0xffffffffu, dq[e], 16);
-                dk[e] += __shfl_xor_sync(0xffffffffu, dk[e], 16);
-                da[e] += __shfl_xor_sync(0xffffffffu, da[e], 16);
+            for (int e = 0; e < 4; ++e) {
+                dq[e] = add2(dq[e], shfl16(dq[e]));
+                dk[e] = add2(dk[e], shfl16(dk[e]));
+                da[e] = add2(da[e], shfl16(da[e]));
             }
             db += __shfl_xor_sync(0xffffffffu, db, 16);
             if (lane < 16) {
@@ -357,12 +400,19 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
                 for (int g = 0; g <= gi; ++g) {
                     const size_t grow = row + gi - g;   // slot g holds the g-th token walked
                     float* out = P.part + ((grow * P.H + h) * kSlices + slice) * kPart;
-                    for (int e = tid; e < 3 * kDim + 1; e += kBwdThreads) {
-                        float sum = 0.0f;
+                    for (int e2 = tid; e2 <= 3 * kDim / 2; e2 += kBwdThreads) {   // pairs
+                        const int e = 2 * e2;
+                        float2 sum = make_float2(0.0f, 0.0f);
 #pragma unroll
-                        for (int w = 0; w < 8; ++w) sum += S.grp[g][w][e];
-                        const int sec = e >> 7;   // dq, dk, da, db
-                        out[sec * kDim + kkey(e & (kDim - 1))] = sec == 0 ? P.scale * sum : sum;
+                        for (int w = 0; w < 8; ++w)
+                            sum = add2(sum, *reinterpret_cast<const float2*>(&S.grp[g][w][e]));
+                        const int sec = e >> 7;   // dq, dk, da; the last pair holds db
+                        if (sec == 3) {
+                            out[3 * kDim] = sum.x;
+                        } else {   // positions e, e + 1 are keys kkey(e), kkey(e) + 1
+                            *reinterpret_cast<float2*>(out + sec * kDim + kkey(e & (kDim - 1))) =
+                                sec == 0 ? mul2(sum, dup2(P.scale)) : sum;
+                        }
                     }
                 }
                 __syncthreads();
@@ -373,7 +423,8 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
     if (P.d_init) {
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-            P.d_init[(((size_t)n * P.H + h) * kDim + k0 + e) * kDim + col0 + jv] = dS[e];
+            P.d_init[(((size_t)n * P.H + h) * kDim + k0 + e) * kDim + col0 + jv] =
+                (e & 1) ? dS[e >> 1].y : dS[e >> 1].x;
     }
 }
 
