@@ -16,17 +16,19 @@
 //
 // The value columns of the state are independent recurrences (k, a and b are shared),
 // so the work is cut into 8 slices of 16 value columns per (sequence, head), one CTA
-// each: thread (column j, key block b) holds S[8 b .. 8 b + 7][16 s + j], so a warp
-// holds all 128 keys of two columns and the sums over keys (r = S'^T k, dd = dS^T k)
-// are four shuffles.  Each block of 8 token rows is staged in shared memory at once.
-// Phase 1 runs the slice forward, storing its state every 8 tokens and each token's
-// d and v - r; phase 2 walks the blocks backwards, rebuilds the block's states from the
-// checkpoint (element-wise, with the stored d) into shared memory, and runs the
-// reverse steps.  dq, dk, da and db sum over value columns: within a warp by a
-// shuffle, over the 8 warps in shared memory every 2 tokens, and over the 8 slices by
-// a second kernel (all in a fixed order), which also applies the activations.
-// This is a token-by-token pass on CUDA cores; a chunked pass on tensor cores, as the
-// forward is, would be much faster.
+// of 4 warps each.  Lane l of warp w holds S[4l .. 4l + 3][16 s + 4w .. 4w + 3]: a warp
+// holds all 128 keys of 4 columns, so the sums over value columns (dq, dk, da) are
+// sums in registers, and the sums over keys (r = S'^T k, dd = dS^T k, one per column)
+// are one reduce-scatter and broadcast over the warp (10 shuffles for the 4 columns).
+// Each block of 8 token rows is staged in shared memory at once, its raw rows loaded
+// into registers one block ahead.  Phase 1 runs the slice forward, storing its state
+// every 8 tokens and each token's d and v - r; phase 2 walks the blocks backwards,
+// rebuilds the block's states from the checkpoint (the same arithmetic as phase 1,
+// element-wise, with the stored d) into shared memory, and runs the reverse steps.
+// The 4 warps' sums of dq, dk, da and db wait in shared memory and are added every 4
+// tokens; the 8 slices' sums are added by a second kernel (every sum in a fixed
+// order), which also applies the activations.  This is a token-by-token pass on CUDA
+// cores; a chunked pass on tensor cores, as the forward is, would be much faster.
 #include <atomic>
 
 #include "kda_internal.cuh"
@@ -37,24 +39,25 @@ namespace {
 
 constexpr int kSlices = 8;          // value slices per (sequence, head)
 constexpr int kSliceV = kDim / kSlices;   // 16 value columns
-constexpr int kBwdThreads = 256;    // 128 keys x 2 halves of 8 columns
+constexpr int kBwdWarps = 4;        // 4 value columns each
+constexpr int kBwdThreads = 32 * kBwdWarps;
 constexpr int kPart = 388;          // partial sums per (row, head, slice): dq, dk, da [128], db
-constexpr int kGroup = 2;           // tokens whose per-warp partial sums wait in shared memory
-constexpr int kBC = 8;              // tokens per checkpoint (and per staged block of rows):
-                                    // small enough for two CTAs per SM
+constexpr int kGroup = 4;           // tokens whose per-warp partial sums wait in shared memory
+constexpr int kBC = 8;              // tokens per checkpoint (and per staged block of rows)
+constexpr int kCkFloats = kDim * kSliceV;   // one slice's state: 16 floats per thread
 
 struct BwdSmem {
-    float4 st[kBC][2][kBwdThreads];     // S_{t-1} of each token of the block: a thread's 8
-                                        // values as two float4 planes (no bank conflicts)
+    float4 st[kBC][4][kBwdThreads];     // S_{t-1} of each token of the block: a thread's
+                                        // 16 values as 4 float4 planes (one per column)
     float a[kBC][kDim];                  // the block's decays
     float kk[kBC][kDim];                 // keys
     float qq[kBC][kDim];                 // queries (reverse phase)
     float vv[kBC][kSliceV];             // the slice's values (forward) or dL/d(out) (reverse)
     float fw[kBC][2 * kSliceV];         // d and v - r of the slice (reverse)
     float b[kBC];                       // sigmoid(beta)
-    // reverse: per-warp sums over the warp's two columns of dq, dk, da (128 keys each)
-    // and db, for a group of 4 tokens; summed over the 8 warps once per group
-    float grp[kGroup][8][3 * kDim + 4];
+    // reverse: per-warp sums over the warp's 4 columns of dq, dk, da (128 keys each) and
+    // db, for a group of tokens; summed over the 4 warps once per group
+    float grp[kGroup][kBwdWarps][3 * kDim + 4];
 };
 
 __device__ __forceinline__ float bf(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
@@ -75,21 +78,14 @@ __device__ __forceinline__ long long ck_slot(int n, long long bos, int c) {
     return (long long)n + c + bos / kBC;
 }
 
-// Position of key channel c in the staged rows and in the per-warp column sums: the 8
-// keys of key block kb = c / 8 sit in two planes, keys 0-3 at 4 kb and keys 4-7 at
-// 64 + 4 kb, so that the 16 key blocks of a warp read or write 16 consecutive float4 per
-// plane (no bank conflicts).  kkey is the inverse.
-__device__ __forceinline__ int kpos(int c) { return ((c & 4) << 4) + ((c >> 3) << 2) + (c & 3); }
-__device__ __forceinline__ int kkey(int p) { return ((p & 63) >> 2) * 8 + ((p >> 6) << 2) + (p & 3); }
-
 // A block's raw token rows, loaded into registers one block ahead of their use, so that
 // their memory latency overlaps the block before: keys, gate inputs (and queries on the
-// way back) as thread (row, 4 channels); in x, the slice's 16 values or dL/d(out)
+// way back) as thread (row, 8 channels); in x, the slice's 16 values or dL/d(out)
 // (threads 0-15, 8 columns each), the beta logit (threads 16-23) or the stored d and
-// v - r on the way back (threads 128-191, 4 floats each).  Rows past the sequence's end
+// v - r on the way back (threads 64-127, 4 floats each).  Rows past the sequence's end
 // are not read.
 struct Rows {
-    uint2 k, g, q;
+    uint4 k, g, q;
     uint4 x;
 };
 
@@ -97,12 +93,12 @@ __device__ __forceinline__ void fetch(const BwdProblem& P, Rows& R, long long ro
                                       int h, int col0, bool reverse, const float* fw0,
                                       size_t fw_step) {
     const int tid = threadIdx.x;
-    const int i = tid >> 5, c4 = 4 * (tid & 31);
+    const int i = tid >> 4, c8 = 8 * (tid & 15);
     if (i < len) {
-        const size_t rk = ((size_t)(row0 + i) * P.H + h) * kDim + c4;
-        R.k = *reinterpret_cast<const uint2*>(P.k + rk);
-        R.g = *reinterpret_cast<const uint2*>(P.g + rk);
-        if (reverse) R.q = *reinterpret_cast<const uint2*>(P.q + rk);
+        const size_t rk = ((size_t)(row0 + i) * P.H + h) * kDim + c8;
+        R.k = *reinterpret_cast<const uint4*>(P.k + rk);
+        R.g = *reinterpret_cast<const uint4*>(P.g + rk);
+        if (reverse) R.q = *reinterpret_cast<const uint4*>(P.q + rk);
     }
     if (tid < 2 * kBC) {
         const int r = tid >> 1, hv = tid & 1;
@@ -113,53 +109,58 @@ __device__ __forceinline__ void fetch(const BwdProblem& P, Rows& R, long long ro
     } else if (tid < 3 * kBC) {
         const int r = tid - 2 * kBC;
         if (r < len) R.x.x = __float_as_uint(bf(P.beta, (size_t)(row0 + r) * P.H + h));
-    } else if (reverse && tid >= 128 && tid < 128 + 8 * kBC) {
-        const int r = (tid - 128) >> 3, f4 = 4 * ((tid - 128) & 7);
+    } else if (reverse && tid >= 64 && tid < 64 + 8 * kBC) {
+        const int r = (tid - 64) >> 3, f4 = 4 * ((tid - 64) & 7);
         if (r < len) R.x = *reinterpret_cast<const uint4*>(fw0 + (size_t)r * fw_step + f4);
     }
 }
 
-__device__ __forceinline__ void unpack4(uint2 w, float (&x)[4]) {
-    x[0] = __uint_as_float(w.x << 16);
-    x[1] = __uint_as_float(w.x & 0xFFFF0000u);
-    x[2] = __uint_as_float(w.y << 16);
-    x[3] = __uint_as_float(w.y & 0xFFFF0000u);
+__device__ __forceinline__ void unpack8(uint4 w, float (&x)[8]) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        x[2 * j] = __uint_as_float(u[j] << 16);
+        x[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ void st8(float* p, const float (&x)[8]) {
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(p + 4) = make_float4(x[4], x[5], x[6], x[7]);
 }
 
 // The fetched rows into shared memory (decays and b formed on the way), then a barrier.
-// dtb: dt_bias of the thread's 4 channels.
+// dtb: dt_bias of the thread's 8 channels.
 __device__ __forceinline__ void commit(BwdSmem& S, const Rows& R, int len, float eA,
-                                       float lower_bound, const float (&dtb)[4], bool reverse) {
+                                       float lower_bound, const float (&dtb)[8], bool reverse) {
     const int tid = threadIdx.x;
-    const int i = tid >> 5, p = kpos(4 * (tid & 31));
+    const int i = tid >> 4, c8 = 8 * (tid & 15);
     if (i < len) {
-        float kx[4], gx[4], a[4];
-        unpack4(R.k, kx);
-        unpack4(R.g, gx);
+        float kx[8], gx[8], a[8];
+        unpack8(R.k, kx);
+        unpack8(R.g, gx);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) a[e] = expf(lower_bound * sigm(eA * (gx[e] + dtb[e])));
-        *reinterpret_cast<float4*>(&S.a[i][p]) = make_float4(a[0], a[1], a[2], a[3]);
-        *reinterpret_cast<float4*>(&S.kk[i][p]) = make_float4(kx[0], kx[1], kx[2], kx[3]);
+        for (int e = 0; e < 8; ++e) a[e] = expf(lower_bound * sigm(eA * (gx[e] + dtb[e])));
+        st8(&S.a[i][c8], a);
+        st8(&S.kk[i][c8], kx);
         if (reverse) {
-            float qx[4];
-            unpack4(R.q, qx);
-            *reinterpret_cast<float4*>(&S.qq[i][p]) = make_float4(qx[0], qx[1], qx[2], qx[3]);
+            float qx[8];
+            unpack8(R.q, qx);
+            st8(&S.qq[i][c8], qx);
         }
     }
     if (tid < 2 * kBC) {
         const int r = tid >> 1, hv = tid & 1;
         if (r < len) {
-            float lo[4], hi[4];
-            unpack4(make_uint2(R.x.x, R.x.y), lo);
-            unpack4(make_uint2(R.x.z, R.x.w), hi);
-            *reinterpret_cast<float4*>(&S.vv[r][8 * hv]) = make_float4(lo[0], lo[1], lo[2], lo[3]);
-            *reinterpret_cast<float4*>(&S.vv[r][8 * hv + 4]) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+            float x[8];
+            unpack8(R.x, x);
+            st8(&S.vv[r][8 * hv], x);
         }
     } else if (tid < 3 * kBC) {
         const int r = tid - 2 * kBC;
         if (r < len) S.b[r] = sigm(__uint_as_float(R.x.x));
-    } else if (reverse && tid >= 128 && tid < 128 + 8 * kBC) {
-        const int r = (tid - 128) >> 3, f4 = 4 * ((tid - 128) & 7);
+    } else if (reverse && tid >= 64 && tid < 64 + 8 * kBC) {
+        const int r = (tid - 64) >> 3, f4 = 4 * ((tid - 64) & 7);
         if (r < len)
             *reinterpret_cast<float4*>(&S.fw[r][f4]) =
                 make_float4(__uint_as_float(R.x.x), __uint_as_float(R.x.y),
@@ -197,22 +198,37 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     return upk2(z);
 }
 __device__ __forceinline__ float2 dup2(float x) { return make_float2(x, x); }
-__device__ __forceinline__ float2 shfl16(float2 a) {
-    return make_float2(__shfl_xor_sync(0xffffffffu, a.x, 16), __shfl_xor_sync(0xffffffffu, a.y, 16));
+
+// The sums over the warp's 32 lanes of 4 per-column partial sums p[0..3], returned in
+// every lane: lanes halve the columns they keep at xor 16 and xor 8 (after which lane l
+// keeps column 2 (l >> 4 & 1) + (l >> 3 & 1)), sum that one over xor 4, 2, 1, and
+// fetch the four results from lanes 0, 8, 16 and 24.  A fixed order: every lane gets
+// the same bits.
+__device__ __forceinline__ void warp_sum4(float (&p)[4], int lane) {
+    const bool h16 = lane & 16, h8 = lane & 8;
+    float k0 = h16 ? p[2] : p[0], k1 = h16 ? p[3] : p[1];
+    const float s0 = h16 ? p[0] : p[2], s1 = h16 ? p[1] : p[3];
+    k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+    k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+    float k = h8 ? k1 : k0;
+    k += __shfl_xor_sync(0xffffffffu, h8 ? k0 : k1, 8);
+    k += __shfl_xor_sync(0xffffffffu, k, 4);
+    k += __shfl_xor_sync(0xffffffffu, k, 2);
+    k += __shfl_xor_sync(0xffffffffu, k, 1);
+    p[0] = __shfl_sync(0xffffffffu, k, 0);
+    p[1] = __shfl_sync(0xffffffffu, k, 8);
+    p[2] = __shfl_sync(0xffffffffu, k, 16);
+    p[3] = __shfl_sync(0xffffffffu, k, 24);
 }
 
-// A thread's 8 keys of a staged row (or of a column-sum row) as 4 pairs: keys 8 kb + 0-3
-// from the first plane, 4-7 from the second.
-__device__ __forceinline__ void ld_planes(const float* row, int pk, float2 (&x)[4]) {
-    const float4 u = *reinterpret_cast<const float4*>(row + pk);
-    const float4 w = *reinterpret_cast<const float4*>(row + 64 + pk);
-    x[0] = make_float2(u.x, u.y); x[1] = make_float2(u.z, u.w);
-    x[2] = make_float2(w.x, w.y); x[3] = make_float2(w.z, w.w);
+__device__ __forceinline__ void ld_keys(const float* row, int lane, float2 (&x)[2]) {
+    const float4 u = *reinterpret_cast<const float4*>(row + 4 * lane);
+    x[0] = make_float2(u.x, u.y);
+    x[1] = make_float2(u.z, u.w);
 }
 
-__device__ __forceinline__ void st_planes(float* row, int pk, const float2 (&x)[4]) {
-    *reinterpret_cast<float4*>(row + pk) = make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
-    *reinterpret_cast<float4*>(row + 64 + pk) = make_float4(x[2].x, x[2].y, x[3].x, x[3].y);
+__device__ __forceinline__ float4 f4(const float2 (&x)[2]) {
+    return make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
 }
 
 __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const int* valid) {
@@ -227,71 +243,83 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
     const int L = P.cu_seqlens ? P.cu_seqlens[n + 1] - P.cu_seqlens[n] : P.T;
     const int nch = (L + kBC - 1) / kBC;
     const int col0 = kSliceV * slice;
+    const int j0 = 4 * warp;               // the warp's first column within the slice
     const float eA = expf(P.A_log[h]);
     const size_t fw_step = (size_t)P.H * kSlices * (2 * kSliceV);           // between rows
     const auto fw_at = [&](size_t row) {   // d (16) and v - r (16) of this slice at a row
         return P.fw + ((row * P.H + h) * kSlices + slice) * (2 * kSliceV);
     };
-    const auto ck_at = [&](int c) {        // checkpoint of block c: [key][16 columns]
-        return P.ck + ((ck_slot(n, bos, c) * P.H + h) * kSlices + slice) * (kDim * kSliceV);
+    // checkpoint of block c: the slice's state, 16 floats per thread (4 float4, one per
+    // column), written and read back by the same thread
+    const auto ck_at = [&](int c) {
+        return P.ck + ((ck_slot(n, bos, c) * P.H + h) * kSlices + slice) * kCkFloats + 16 * tid;
     };
-    float dtb[4];
+    float dtb[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) dtb[e] = P.dt_bias[(size_t)h * kDim + 4 * (tid & 31) + e];
-    // Thread (column jv = tid / 16, key block kb = tid % 16) holds S[8 kb .. + 7][jv] in
-    // both phases: a warp holds all 128 keys of two columns, so r = S'^T k and dd = dS^T k
-    // are sums over 16 lanes (four shuffles, no barrier per token).
-    const int jv = tid >> 4, kb = tid & 15, k0 = 8 * kb, pk = 4 * kb;
+    for (int e = 0; e < 8; ++e) dtb[e] = P.dt_bias[(size_t)h * kDim + 8 * (tid & 15) + e];
+    // element (key 4 lane + 2 p + x, column j0 + c) of the slice's state in [c][p].x|y
+    const auto state_index = [&](int key, int c) {
+        return (((size_t)n * P.H + h) * kDim + key) * kDim + col0 + j0 + c;
+    };
     Rows R{};
 
     // ---- phase 1: forward over the slice, checkpoints and per-token d, v - r ----------
     {
-        float2 st[4];   // keys k0 + 2e, k0 + 2e + 1
+        float2 st[4][2];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float x = 0.0f;
-            if (P.init_state) {
-                const size_t si = (((size_t)n * P.H + h) * kDim + k0 + e) * kDim + col0 + jv;
-                x = P.init_dtype == KDA_F32 ? static_cast<const float*>(P.init_state)[si]
-                                            : __bfloat162float(static_cast<const __nv_bfloat16*>(P.init_state)[si]);
-            }
-            if (e & 1) st[e >> 1].y = x; else st[e >> 1].x = x;
-        }
-        if (nch > 0) fetch(P, R, bos, min(kBC, L), h, col0, false, nullptr, 0);
-        for (int c = 0; c < nch; ++c) {
-            float* ck = ck_at(c);
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                ck[(k0 + 2 * e) * kSliceV + jv] = st[e].x;
-                ck[(k0 + 2 * e + 1) * kSliceV + jv] = st[e].y;
+                float x = 0.0f;
+                if (P.init_state) {
+                    const size_t si = state_index(4 * lane + e, c);
+                    x = P.init_dtype == KDA_F32
+                            ? static_cast<const float*>(P.init_state)[si]
+                            : __bfloat162float(static_cast<const __nv_bfloat16*>(P.init_state)[si]);
+                }
+                if (e & 1) st[c][e >> 1].y = x; else st[c][e >> 1].x = x;
             }
+        if (nch > 0) fetch(P, R, bos, min(kBC, L), h, col0, false, nullptr, 0);
+        for (int c = 0; c < nch; ++c) {
+            float4* ck = reinterpret_cast<float4*>(ck_at(c));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ck[j] = f4(st[j]);
             const int len = min(kBC, L - c * kBC);
             const long long row0 = bos + (long long)c * kBC;
             commit(S, R, len, eA, P.lower_bound, dtb, false);
             if (c + 1 < nch)
                 fetch(P, R, row0 + kBC, min(kBC, L - (c + 1) * kBC), h, col0, false, nullptr, 0);
             for (int i = 0; i < len; ++i) {
-                float2 a[4], kk[4], r2 = make_float2(0.0f, 0.0f);
-                ld_planes(S.a[i], pk, a);
-                ld_planes(S.kk[i], pk, kk);
+                float2 a[2], kk[2];
+                ld_keys(S.a[i], lane, a);
+                ld_keys(S.kk[i], lane, kk);
+                const float4 v4 = *reinterpret_cast<const float4*>(&S.vv[i][j0]);
+                const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+                const float b = S.b[i];
+                float r[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    st[e] = mul2(st[e], a[e]);
-                    r2 = fma2(st[e], kk[e], r2);
+                for (int j = 0; j < 4; ++j) {
+                    float2 rp = make_float2(0.0f, 0.0f);
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        st[j][p] = mul2(st[j][p], a[p]);
+                        rp = fma2(st[j][p], kk[p], rp);
+                    }
+                    r[j] = rp.x + rp.y;
                 }
-                float r = r2.x + r2.y;
-                r += __shfl_xor_sync(0xffffffffu, r, 1);
-                r += __shfl_xor_sync(0xffffffffu, r, 2);
-                r += __shfl_xor_sync(0xffffffffu, r, 4);
-                r += __shfl_xor_sync(0xffffffffu, r, 8);
-                const float vr = S.vv[i][jv] - r;
-                const float d = S.b[i] * vr;
+                warp_sum4(r, lane);
+                float d[4], vr[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) st[e] = fma2(kk[e], dup2(d), st[e]);
-                if (kb == 0) {   // lanes 0 and 16: this column's d and v - r
+                for (int j = 0; j < 4; ++j) {
+                    vr[j] = v[j] - r[j];
+                    d[j] = b * vr[j];
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) st[j][p] = fma2(kk[p], dup2(d[j]), st[j][p]);
+                }
+                if (lane == 0) {   // the warp's 4 columns of d and v - r
                     float* f = fw_at(row0 + i);
-                    f[jv] = d;
-                    f[kSliceV + jv] = vr;
+                    *reinterpret_cast<float4*>(f + j0) = make_float4(d[0], d[1], d[2], d[3]);
+                    *reinterpret_cast<float4*>(f + kSliceV + j0) = make_float4(vr[0], vr[1], vr[2], vr[3]);
                 }
             }
             __syncthreads();   // the staged rows are replaced by the next block's
@@ -300,119 +328,130 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
     __syncthreads();   // d and v - r are read by other threads below
 
     // ---- phase 2: reverse, block by block from the last ---------------------------------
-    float2 dS[4];
-    float ckn[8];
+    float2 dS[4][2];
+    float4 ckn[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const float x =
-            P.dfinal ? P.dfinal[(((size_t)n * P.H + h) * kDim + k0 + e) * kDim + col0 + jv] : 0.0f;
-        if (e & 1) dS[e >> 1].y = x; else dS[e >> 1].x = x;
-    }
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float x = P.dfinal ? P.dfinal[state_index(4 * lane + e, c)] : 0.0f;
+            if (e & 1) dS[c][e >> 1].y = x; else dS[c][e >> 1].x = x;
+        }
     if (nch > 0) {
         const long long row0 = bos + (long long)(nch - 1) * kBC;
         fetch(P, R, row0, L - (nch - 1) * kBC, h, col0, true, fw_at(row0), fw_step);
-        const float* ck = ck_at(nch - 1);
+        const float4* ck = reinterpret_cast<const float4*>(ck_at(nch - 1));
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ckn[e] = ck[(k0 + e) * kSliceV + jv];   // written by this thread
+        for (int j = 0; j < 4; ++j) ckn[j] = ck[j];   // written by this thread
     }
     for (int c = nch - 1; c >= 0; --c) {
         const int len = min(kBC, L - c * kBC);
         const long long row0 = bos + (long long)c * kBC;
         commit(S, R, len, eA, P.lower_bound, dtb, true);
-        float2 sv[4];
+        float2 sv[4][2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sv[e] = make_float2(ckn[2 * e], ckn[2 * e + 1]);
+        for (int j = 0; j < 4; ++j) {
+            sv[j][0] = make_float2(ckn[j].x, ckn[j].y);
+            sv[j][1] = make_float2(ckn[j].z, ckn[j].w);
+        }
         if (c > 0) {   // the block before is whole
             fetch(P, R, row0 - kBC, kBC, h, col0, true, fw_at(row0 - kBC), fw_step);
-            const float* ck = ck_at(c - 1);
+            const float4* ck = reinterpret_cast<const float4*>(ck_at(c - 1));
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ckn[e] = ck[(k0 + e) * kSliceV + jv];
+            for (int j = 0; j < 4; ++j) ckn[j] = ck[j];
         }
-        // rebuild the block's states S_{t-1} from the checkpoint (element-wise, the same
-        // arithmetic as phase 1; each thread reads back only its own states)
+        // rebuild the block's states S_{t-1} from the checkpoint (the same arithmetic as
+        // phase 1; each thread reads back only its own states)
         for (int i = 0; i < len; ++i) {
-            S.st[i][0][tid] = make_float4(sv[0].x, sv[0].y, sv[1].x, sv[1].y);
-            S.st[i][1][tid] = make_float4(sv[2].x, sv[2].y, sv[3].x, sv[3].y);
-            const float d = S.fw[i][jv];
-            float2 a[4], kk[4];
-            ld_planes(S.a[i], pk, a);
-            ld_planes(S.kk[i], pk, kk);
+            float2 a[2], kk[2];
+            ld_keys(S.a[i], lane, a);
+            ld_keys(S.kk[i], lane, kk);
+            const float4 d4 = *reinterpret_cast<const float4*>(&S.fw[i][j0]);
+            const float d[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sv[e] = fma2(kk[e], dup2(d), mul2(sv[e], a[e]));
+            for (int j = 0; j < 4; ++j) {
+                S.st[i][j][tid] = f4(sv[j]);
+#pragma unroll
+                for (int p = 0; p < 2; ++p) sv[j][p] = fma2(kk[p], dup2(d[j]), mul2(sv[j][p], a[p]));
+            }
         }
         for (int i = len - 1; i >= 0; --i) {
             const int gi = (len - 1 - i) % kGroup;   // slot of this token in its group
-            float2 a[4], kk[4], qq[4];
-            ld_planes(S.a[i], pk, a);
-            ld_planes(S.kk[i], pk, kk);
-            ld_planes(S.qq[i], pk, qq);
-            const float d = S.fw[i][jv], vr = S.fw[i][kSliceV + jv];
-            const float dout = S.vv[i][jv], b = S.b[i];
-            const float4 p0 = S.st[i][0][tid];
-            const float4 p1 = S.st[i][1][tid];
-            const float2 sprev[4] = {make_float2(p0.x, p0.y), make_float2(p0.z, p0.w),
-                                     make_float2(p1.x, p1.y), make_float2(p1.z, p1.w)};
-            float2 sp[4], dq[4], dk[4], da[4], dd2 = make_float2(0.0f, 0.0f);
-            const float2 d2 = dup2(d), do2 = dup2(dout), sdo2 = dup2(P.scale * dout);
+            float2 a[2], kk[2], qq[2];
+            ld_keys(S.a[i], lane, a);
+            ld_keys(S.kk[i], lane, kk);
+            ld_keys(S.qq[i], lane, qq);
+            const float4 d4 = *reinterpret_cast<const float4*>(&S.fw[i][j0]);
+            const float4 vr4 = *reinterpret_cast<const float4*>(&S.fw[i][kSliceV + j0]);
+            const float4 do4 = *reinterpret_cast<const float4*>(&S.vv[i][j0]);
+            const float d[4] = {d4.x, d4.y, d4.z, d4.w};
+            const float vr[4] = {vr4.x, vr4.y, vr4.z, vr4.w};
+            const float dout[4] = {do4.x, do4.y, do4.z, do4.w};
+            const float b = S.b[i];
+            float2 sprev[4][2];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                sp[e] = mul2(sprev[e], a[e]);
-                dq[e] = mul2(fma2(kk[e], d2, sp[e]), do2);   // S_t dO (scale applied at the end)
-                dS[e] = fma2(qq[e], sdo2, dS[e]);
-                dk[e] = mul2(dS[e], d2);
-                dd2 = fma2(dS[e], kk[e], dd2);
+            for (int j = 0; j < 4; ++j) {
+                const float4 s4 = S.st[i][j][tid];
+                sprev[j][0] = make_float2(s4.x, s4.y);
+                sprev[j][1] = make_float2(s4.z, s4.w);
             }
-            float dd = dd2.x + dd2.y;
-            dd += __shfl_xor_sync(0xffffffffu, dd, 1);   // dd = dS^T k over the 128 keys
-            dd += __shfl_xor_sync(0xffffffffu, dd, 2);
-            dd += __shfl_xor_sync(0xffffffffu, dd, 4);
-            dd += __shfl_xor_sync(0xffffffffu, dd, 8);
-            const float2 dr2 = dup2(-b * dd);
+            const float2 zero = make_float2(0.0f, 0.0f);
+            float2 dq[2] = {zero, zero}, dk[2] = {zero, zero}, da[2] = {zero, zero};
+            float dd[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 dsp = fma2(kk[e], dr2, dS[e]);
-                dk[e] = fma2(sp[e], dr2, dk[e]);
-                da[e] = mul2(dsp, sprev[e]);
-                dS[e] = mul2(a[e], dsp);
+            for (int j = 0; j < 4; ++j) {
+                float2 ddp = zero;
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const float2 sp = mul2(sprev[j][p], a[p]);
+                    // S_t dO (scale applied when the warps' sums are added)
+                    dq[p] = fma2(fma2(kk[p], dup2(d[j]), sp), dup2(dout[j]), dq[p]);
+                    dS[j][p] = fma2(qq[p], dup2(P.scale * dout[j]), dS[j][p]);
+                    dk[p] = fma2(dS[j][p], dup2(d[j]), dk[p]);
+                    ddp = fma2(dS[j][p], kk[p], ddp);
+                }
+                dd[j] = ddp.x + ddp.y;
             }
-            float db = dd * vr;
+            warp_sum4(dd, lane);   // dd = dS^T k over the 128 keys, per column
+            float db = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 dr = dup2(-b * dd[j]);
+                db = fmaf(dd[j], vr[j], db);
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const float2 sp = mul2(sprev[j][p], a[p]);
+                    const float2 dsp = fma2(kk[p], dr, dS[j][p]);
+                    dk[p] = fma2(sp, dr, dk[p]);
+                    da[p] = fma2(dsp, sprev[j][p], da[p]);
+                    dS[j][p] = mul2(a[p], dsp);
+                }
+            }
             const size_t row = row0 + i;
-            if (kb == 0) P.dv[(row * P.H + h) * kDim + col0 + jv] = b * dd;
-            // the warp's two columns (lanes l and l ^ 16) added, then kept for the group
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                dq[e] = add2(dq[e], shfl16(dq[e]));
-                dk[e] = add2(dk[e], shfl16(dk[e]));
-                da[e] = add2(da[e], shfl16(da[e]));
+            if (lane == 0) {
+                *reinterpret_cast<float4*>(P.dv + (row * P.H + h) * kDim + col0 + j0) =
+                    make_float4(b * dd[0], b * dd[1], b * dd[2], b * dd[3]);
+                S.grp[gi][warp][3 * kDim] = db;
             }
-            db += __shfl_xor_sync(0xffffffffu, db, 16);
-            if (lane < 16) {
-                float* gp = S.grp[gi][warp];
-                st_planes(gp, pk, dq);
-                st_planes(gp + kDim, pk, dk);
-                st_planes(gp + 2 * kDim, pk, da);
-                if (lane == 0) gp[3 * kDim] = db;
-            }
+            float* gp = S.grp[gi][warp];
+            *reinterpret_cast<float4*>(gp + 4 * lane) = f4(dq);
+            *reinterpret_cast<float4*>(gp + kDim + 4 * lane) = f4(dk);
+            *reinterpret_cast<float4*>(gp + 2 * kDim + 4 * lane) = f4(da);
             if (gi == kGroup - 1 || i == 0) {
-                // the group's tokens (rows row .. row + gi): sum the 8 warps in order and
-                // write this slice's partial sums in key order
+                // the group's tokens (rows row .. row + gi): sum the 4 warps in order and
+                // write this slice's partial sums
                 __syncthreads();
                 for (int g = 0; g <= gi; ++g) {
                     const size_t grow = row + gi - g;   // slot g holds the g-th token walked
                     float* out = P.part + ((grow * P.H + h) * kSlices + slice) * kPart;
                     for (int e2 = tid; e2 <= 3 * kDim / 2; e2 += kBwdThreads) {   // pairs
                         const int e = 2 * e2;
-                        float2 sum = make_float2(0.0f, 0.0f);
+                        float2 sum = zero;
 #pragma unroll
-                        for (int w = 0; w < 8; ++w)
+                        for (int w = 0; w < kBwdWarps; ++w)
                             sum = add2(sum, *reinterpret_cast<const float2*>(&S.grp[g][w][e]));
-                        const int sec = e >> 7;   // dq, dk, da; the last pair holds db
-                        if (sec == 3) {
-                            out[3 * kDim] = sum.x;
-                        } else {   // positions e, e + 1 are keys kkey(e), kkey(e) + 1
-                            *reinterpret_cast<float2*>(out + sec * kDim + kkey(e & (kDim - 1))) =
-                                sec == 0 ? mul2(sum, dup2(P.scale)) : sum;
-                        }
+                        if (e == 3 * kDim) out[e] = sum.x;   // db
+                        else *reinterpret_cast<float2*>(out + e) = e < kDim ? mul2(sum, dup2(P.scale)) : sum;
                     }
                 }
                 __syncthreads();
@@ -422,9 +461,12 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
     }
     if (P.d_init) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            P.d_init[(((size_t)n * P.H + h) * kDim + k0 + e) * kDim + col0 + jv] =
-                (e & 1) ? dS[e >> 1].y : dS[e >> 1].x;
+        for (int e = 0; e < 4; ++e) {
+            const int p = e >> 1;
+            const auto x = [&](int j) { return (e & 1) ? dS[j][p].y : dS[j][p].x; };
+            *reinterpret_cast<float4*>(P.d_init + state_index(4 * lane + e, 0)) =
+                make_float4(x(0), x(1), x(2), x(3));
+        }
     }
 }
 
@@ -498,7 +540,7 @@ std::atomic<bool> g_bwd_attr[64];
 size_t bwd_scratch_floats(int N, long long rows, int H, size_t* ck, size_t* fw, size_t* part,
                           size_t* blk) {
     const long long slots = N + rows / kBC + 1;
-    *ck = (size_t)slots * H * kSlices * kDim * kSliceV;
+    *ck = (size_t)slots * H * kSlices * kCkFloats;
     *fw = (size_t)rows * H * kSlices * 2 * kSliceV;
     *part = (size_t)rows * H * kSlices * kPart;
     *blk = (size_t)((rows + kRowBlock - 1) / kRowBlock) * H * (kDim + 1);
