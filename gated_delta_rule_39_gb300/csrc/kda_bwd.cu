@@ -23,8 +23,9 @@
 // Each block of 8 token rows is staged in shared memory at once, its raw rows loaded
 // into registers one block ahead.  Phase 1 runs the slice forward, storing its state
 // every 8 tokens and each token's d and v - r; phase 2 walks the blocks backwards,
-// rebuilds the block's states from the checkpoint (the same arithmetic as phase 1,
-// element-wise, with the stored d) into shared memory, and runs the reverse steps.
+// and each block's halves backwards: it rebuilds the half's states from the checkpoint
+// (the same arithmetic as phase 1, element-wise, with the stored d) into shared memory
+// and runs the reverse steps over them.
 // The 4 warps' sums of dq, dk, da and db wait in shared memory and are added every 4
 // tokens; the 8 slices' sums are added by a second kernel (every sum in a fixed
 // order), which also applies the activations.  This is a token-by-token pass on CUDA
@@ -44,10 +45,12 @@ constexpr int kBwdThreads = 32 * kBwdWarps;
 constexpr int kPart = 388;          // partial sums per (row, head, slice): dq, dk, da [128], db
 constexpr int kGroup = 4;           // tokens whose per-warp partial sums wait in shared memory
 constexpr int kBC = 8;              // tokens per checkpoint (and per staged block of rows)
+constexpr int kHalf = kBC / 2;      // states rebuilt at a time (half a block): with these
+                                    // sizes three CTAs fit on an SM
 constexpr int kCkFloats = kDim * kSliceV;   // one slice's state: 16 floats per thread
 
 struct BwdSmem {
-    float4 st[kBC][4][kBwdThreads];     // S_{t-1} of each token of the block: a thread's
+    float4 st[kHalf][4][kBwdThreads];   // S_{t-1} of each token of half a block: a thread's
                                         // 16 values as 4 float4 planes (one per column)
     float a[kBC][kDim];                  // the block's decays
     float kk[kBC][kDim];                 // keys
@@ -231,7 +234,7 @@ __device__ __forceinline__ float4 f4(const float2 (&x)[2]) {
     return make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
 }
 
-__global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const int* valid) {
+__global__ void __launch_bounds__(kBwdThreads, 3) bwd_kernel(BwdProblem P, const int* valid) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     BwdSmem& S = *reinterpret_cast<BwdSmem*>(smem_raw);
     if (valid && !*valid) return;   // malformed cu_seqlens: the sequence map says so
@@ -360,101 +363,112 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_kernel(BwdProblem P, const
 #pragma unroll
             for (int j = 0; j < 4; ++j) ckn[j] = ck[j];
         }
-        // rebuild the block's states S_{t-1} from the checkpoint (the same arithmetic as
-        // phase 1; each thread reads back only its own states)
-        for (int i = 0; i < len; ++i) {
-            float2 a[2], kk[2];
-            ld_keys(S.a[i], lane, a);
-            ld_keys(S.kk[i], lane, kk);
-            const float4 d4 = *reinterpret_cast<const float4*>(&S.fw[i][j0]);
-            const float d[4] = {d4.x, d4.y, d4.z, d4.w};
+        // The block's two halves, the later first: rebuild the half's states S_{t-1} from
+        // the checkpoint (the same arithmetic as phase 1, stepping over the first half
+        // for the later one; each thread reads back only its own states), then run the
+        // reverse steps over the half.
+        for (int lo = len > kHalf ? kHalf : 0; lo >= 0; lo -= kHalf) {
+            const int hi = min(len, lo + kHalf);
+            float2 s2[4][2];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                S.st[i][j][tid] = f4(sv[j]);
-#pragma unroll
-                for (int p = 0; p < 2; ++p) sv[j][p] = fma2(kk[p], dup2(d[j]), mul2(sv[j][p], a[p]));
+                s2[j][0] = sv[j][0];
+                s2[j][1] = sv[j][1];
             }
-        }
-        for (int i = len - 1; i >= 0; --i) {
-            const int gi = (len - 1 - i) % kGroup;   // slot of this token in its group
-            float2 a[2], kk[2], qq[2];
-            ld_keys(S.a[i], lane, a);
-            ld_keys(S.kk[i], lane, kk);
-            ld_keys(S.qq[i], lane, qq);
-            const float4 d4 = *reinterpret_cast<const float4*>(&S.fw[i][j0]);
-            const float4 vr4 = *reinterpret_cast<const float4*>(&S.fw[i][kSliceV + j0]);
-            const float4 do4 = *reinterpret_cast<const float4*>(&S.vv[i][j0]);
-            const float d[4] = {d4.x, d4.y, d4.z, d4.w};
-            const float vr[4] = {vr4.x, vr4.y, vr4.z, vr4.w};
-            const float dout[4] = {do4.x, do4.y, do4.z, do4.w};
-            const float b = S.b[i];
-            float2 sprev[4][2];
+            for (int i = 0; i < hi; ++i) {
+                float2 a[2], kk[2];
+                ld_keys(S.a[i], lane, a);
+                ld_keys(S.kk[i], lane, kk);
+                const float4 d4 = *reinterpret_cast<const float4*>(&S.fw[i][j0]);
+                const float d[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 s4 = S.st[i][j][tid];
-                sprev[j][0] = make_float2(s4.x, s4.y);
-                sprev[j][1] = make_float2(s4.z, s4.w);
-            }
-            const float2 zero = make_float2(0.0f, 0.0f);
-            float2 dq[2] = {zero, zero}, dk[2] = {zero, zero}, da[2] = {zero, zero};
-            float dd[4];
+                for (int j = 0; j < 4; ++j) {
+                    if (i >= lo) S.st[i - lo][j][tid] = f4(s2[j]);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float2 ddp = zero;
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const float2 sp = mul2(sprev[j][p], a[p]);
-                    // S_t dO (scale applied when the warps' sums are added)
-                    dq[p] = fma2(fma2(kk[p], dup2(d[j]), sp), dup2(dout[j]), dq[p]);
-                    dS[j][p] = fma2(qq[p], dup2(P.scale * dout[j]), dS[j][p]);
-                    dk[p] = fma2(dS[j][p], dup2(d[j]), dk[p]);
-                    ddp = fma2(dS[j][p], kk[p], ddp);
-                }
-                dd[j] = ddp.x + ddp.y;
-            }
-            warp_sum4(dd, lane);   // dd = dS^T k over the 128 keys, per column
-            float db = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 dr = dup2(-b * dd[j]);
-                db = fmaf(dd[j], vr[j], db);
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const float2 sp = mul2(sprev[j][p], a[p]);
-                    const float2 dsp = fma2(kk[p], dr, dS[j][p]);
-                    dk[p] = fma2(sp, dr, dk[p]);
-                    da[p] = fma2(dsp, sprev[j][p], da[p]);
-                    dS[j][p] = mul2(a[p], dsp);
+                    for (int p = 0; p < 2; ++p) s2[j][p] = fma2(kk[p], dup2(d[j]), mul2(s2[j][p], a[p]));
                 }
             }
-            const size_t row = row0 + i;
-            if (lane == 0) {
-                *reinterpret_cast<float4*>(P.dv + (row * P.H + h) * kDim + col0 + j0) =
-                    make_float4(b * dd[0], b * dd[1], b * dd[2], b * dd[3]);
-                S.grp[gi][warp][3 * kDim] = db;
-            }
-            float* gp = S.grp[gi][warp];
-            *reinterpret_cast<float4*>(gp + 4 * lane) = f4(dq);
-            *reinterpret_cast<float4*>(gp + kDim + 4 * lane) = f4(dk);
-            *reinterpret_cast<float4*>(gp + 2 * kDim + 4 * lane) = f4(da);
-            if (gi == kGroup - 1 || i == 0) {
-                // the group's tokens (rows row .. row + gi): sum the 4 warps in order and
-                // write this slice's partial sums
-                __syncthreads();
-                for (int g = 0; g <= gi; ++g) {
-                    const size_t grow = row + gi - g;   // slot g holds the g-th token walked
-                    float* out = P.part + ((grow * P.H + h) * kSlices + slice) * kPart;
-                    for (int e2 = tid; e2 <= 3 * kDim / 2; e2 += kBwdThreads) {   // pairs
-                        const int e = 2 * e2;
-                        float2 sum = zero;
+            for (int i = hi - 1; i >= lo; --i) {
+                const int gi = (len - 1 - i) % kGroup;   // slot of this token in its group
+                float2 a[2], kk[2], qq[2];
+                ld_keys(S.a[i], lane, a);
+                ld_keys(S.kk[i], lane, kk);
+                ld_keys(S.qq[i], lane, qq);
+                const float4 d4 = *reinterpret_cast<const float4*>(&S.fw[i][j0]);
+                const float4 vr4 = *reinterpret_cast<const float4*>(&S.fw[i][kSliceV + j0]);
+                const float4 do4 = *reinterpret_cast<const float4*>(&S.vv[i][j0]);
+                const float d[4] = {d4.x, d4.y, d4.z, d4.w};
+                const float vr[4] = {vr4.x, vr4.y, vr4.z, vr4.w};
+                const float dout[4] = {do4.x, do4.y, do4.z, do4.w};
+                const float b = S.b[i];
+                float2 sprev[4][2];
 #pragma unroll
-                        for (int w = 0; w < kBwdWarps; ++w)
-                            sum = add2(sum, *reinterpret_cast<const float2*>(&S.grp[g][w][e]));
-                        if (e == 3 * kDim) out[e] = sum.x;   // db
-                        else *reinterpret_cast<float2*>(out + e) = e < kDim ? mul2(sum, dup2(P.scale)) : sum;
+                for (int j = 0; j < 4; ++j) {
+                    const float4 s4 = S.st[i - lo][j][tid];
+                    sprev[j][0] = make_float2(s4.x, s4.y);
+                    sprev[j][1] = make_float2(s4.z, s4.w);
+                }
+                const float2 zero = make_float2(0.0f, 0.0f);
+                float2 dq[2] = {zero, zero}, dk[2] = {zero, zero}, da[2] = {zero, zero};
+                float dd[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float2 ddp = zero;
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        const float2 sp = mul2(sprev[j][p], a[p]);
+                        // S_t dO (scale applied when the warps' sums are added)
+                        dq[p] = fma2(fma2(kk[p], dup2(d[j]), sp), dup2(dout[j]), dq[p]);
+                        dS[j][p] = fma2(qq[p], dup2(P.scale * dout[j]), dS[j][p]);
+                        dk[p] = fma2(dS[j][p], dup2(d[j]), dk[p]);
+                        ddp = fma2(dS[j][p], kk[p], ddp);
+                    }
+                    dd[j] = ddp.x + ddp.y;
+                }
+                warp_sum4(dd, lane);   // dd = dS^T k over the 128 keys, per column
+                float db = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 dr = dup2(-b * dd[j]);
+                    db = fmaf(dd[j], vr[j], db);
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        const float2 sp = mul2(sprev[j][p], a[p]);
+                        const float2 dsp = fma2(kk[p], dr, dS[j][p]);
+                        dk[p] = fma2(sp, dr, dk[p]);
+                        da[p] = fma2(dsp, sprev[j][p], da[p]);
+                        dS[j][p] = mul2(a[p], dsp);
                     }
                 }
-                __syncthreads();
+                const size_t row = row0 + i;
+                if (lane == 0) {
+                    *reinterpret_cast<float4*>(P.dv + (row * P.H + h) * kDim + col0 + j0) =
+                        make_float4(b * dd[0], b * dd[1], b * dd[2], b * dd[3]);
+                    S.grp[gi][warp][3 * kDim] = db;
+                }
+                float* gp = S.grp[gi][warp];
+                *reinterpret_cast<float4*>(gp + 4 * lane) = f4(dq);
+                *reinterpret_cast<float4*>(gp + kDim + 4 * lane) = f4(dk);
+                *reinterpret_cast<float4*>(gp + 2 * kDim + 4 * lane) = f4(da);
+                if (gi == kGroup - 1 || i == 0) {
+                    // the group's tokens (rows row .. row + gi): sum the 4 warps in order and
+                    // write this slice's partial sums
+                    __syncthreads();
+                    for (int g = 0; g <= gi; ++g) {
+                        const size_t grow = row + gi - g;   // slot g holds the g-th token walked
+                        float* out = P.part + ((grow * P.H + h) * kSlices + slice) * kPart;
+                        for (int e2 = tid; e2 <= 3 * kDim / 2; e2 += kBwdThreads) {   // pairs
+                            const int e = 2 * e2;
+                            float2 sum = zero;
+#pragma unroll
+                            for (int w = 0; w < kBwdWarps; ++w)
+                                sum = add2(sum, *reinterpret_cast<const float2*>(&S.grp[g][w][e]));
+                            if (e == 3 * kDim) out[e] = sum.x;   // db
+                            else *reinterpret_cast<float2*>(out + e) = e < kDim ? mul2(sum, dup2(P.scale)) : sum;
+                        }
+                    }
+                    __syncthreads();
+                }
             }
         }
         __syncthreads();   // the block's staged rows and states are replaced by the next one
