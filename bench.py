@@ -463,23 +463,26 @@ def run_cuda(args, world, rank, local, pg):
         d = make_decode_inputs(rank)
         runner = DecodeRunner(d, device, stream)
     else:
-        if args.heads:
+        if args.heads or args.tokens:
             w = synth.WORKLOADS[name]
-            d = synth.make_inputs(w.B, w.T, args.heads, seed=rank, init_dtype=w.init_dtype)
+            d = synth.make_inputs(w.B, args.tokens or w.T, args.heads or w.H, seed=rank,
+                                  init_dtype=w.init_dtype)
         else:
             d = synth.make_workload(name, seed=rank)
-        runner = Runner(d, device, stream, args.segments)
+        runner = (BwdRunner(d, device, stream, rank) if args.bwd
+                  else Runner(d, device, stream, args.segments))
     B, T, H, N = runner.B, runner.T, runner.H, runner.N
 
     # ---- timed region: K steps, launch timing on the launch stream -------------
     sampler = ClockSampler(local) if rank == 0 else None
     elapsed_ms, prof = timed_steps(runner, args.steps, args.warmup, pg, device, sampler)
     elapsed_ms = max_over_ranks(pg, elapsed_ms, device)
-    main = workload_line(name, d, elapsed_ms, prof, args.steps, world, runner.calls, decode)
+    main = workload_line(name, d, elapsed_ms, prof, args.steps, world, runner.calls, decode,
+                         bwd=args.bwd)
 
     # ---- end-to-end through the host-buffer entry point ---------------------------
     e2e = None
-    if not args.no_e2e and runner.calls == 1 and not decode:
+    if not args.no_e2e and runner.calls == 1 and not decode and not args.bwd:
         hx = {n: torch.from_numpy(np.ascontiguousarray(d[n]).view(np.int16)).view(torch.bfloat16)
               .pin_memory() for n in ("q", "k", "v", "g", "beta")}
         s0 = d.get("initial_state")
@@ -519,13 +522,15 @@ def run_cuda(args, world, rank, local, pg):
     # ---- CPU oracle on a bounded sample (rank 0, N = 1 only) -----------------------
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(d, name, target_s=args.cpu_seconds)
+        cpu = (cpu_baseline_bwd(runner, target_s=args.cpu_seconds) if args.bwd
+               else cpu_baseline(d, name, target_s=args.cpu_seconds))
 
     clocks = sampler.summary() if sampler else None
 
     # ---- the pages' other workloads, one nested object each (rank 0 prints) --------
     others = {}
-    if not args.heads and not args.no_other_workloads and name == WORKLOAD:
+    if (not args.heads and not args.tokens and not args.bwd and not args.no_other_workloads
+            and name == WORKLOAD):
         for other in OTHER_WORKLOADS:
             od = synth.make_workload(other, seed=rank)
             orun = Runner(od, device, stream)
@@ -570,8 +575,9 @@ def run_cuda(args, world, rank, local, pg):
         torch.cuda.empty_cache()
 
     if rank == 0:
-        if args.heads:
-            line_workload = f"{name} with H={H} (profiling case, not a bench line)"
+        if args.heads or args.tokens or args.bwd:
+            line_workload = (f"{'backward of ' if args.bwd else ''}{name} with T={T}, H={H} "
+                             "(profiling case, not a bench line)")
         else:
             line_workload = name
         s0 = d.get("initial_state")
@@ -723,6 +729,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--heads", type=int, default=0,
                     help="profiling only: run the workload with this many heads instead")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling only: run the workload with this many tokens instead")
+    ap.add_argument("--bwd", action="store_true",
+                    help="profiling only: time the backward pass (kda_bwd) on the workload's "
+                         "inputs instead of the forward")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="time this workload instead of the headline one (profiling)")
     ap.add_argument("--segments", type=int, default=0,

@@ -65,14 +65,20 @@ struct BwdSmem {
 
 __device__ __forceinline__ float bf(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
 
-__device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
+// sigmoid and the decay from CUDA's fast exponential and reciprocal intrinsics (relative
+// error ~1e-7, far inside the gradients' tolerance; every kernel of the pass uses these
+// same two functions, so phase 1, phase 2 and the finish kernel see the same bits)
+__device__ __forceinline__ float sigm(float x) { return __frcp_rn(1.0f + __expf(-x)); }
+__device__ __forceinline__ float decay_of(float x, float lower_bound) {
+    return __expf(lower_bound * sigm(x));
+}
 
 // the decay of key channel c at token row t, and x (the sigmoid's argument)
 __device__ __forceinline__ float decay(const BwdProblem& P, size_t row, int h, int c, float eA,
                                       float* xo = nullptr) {
     const float x = eA * (bf(P.g, (row * P.H + h) * kDim + c) + P.dt_bias[(size_t)h * kDim + c]);
     if (xo) *xo = x;
-    return expf(P.lower_bound * sigm(x));
+    return decay_of(x, P.lower_bound);
 }
 
 // Checkpoint slot of block c (of 8 tokens) of sequence n (first token bos): distinct for
@@ -143,7 +149,7 @@ __device__ __forceinline__ void commit(BwdSmem& S, const Rows& R, int len, float
         unpack8(R.k, kx);
         unpack8(R.g, gx);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) a[e] = expf(lower_bound * sigm(eA * (gx[e] + dtb[e])));
+        for (int e = 0; e < 8; ++e) a[e] = decay_of(eA * (gx[e] + dtb[e]), lower_bound);
         st8(&S.a[i][c8], a);
         st8(&S.kk[i][c8], kx);
         if (reverse) {
