@@ -460,17 +460,22 @@ __global__ void __launch_bounds__(kBwdThreads, 3) bwd_kernel(BwdProblem P, const
                     // the group's tokens (rows row .. row + gi): sum the 4 warps in order and
                     // write this slice's partial sums
                     __syncthreads();
-                    for (int g = 0; g <= gi; ++g) {
-                        const size_t grow = row + gi - g;   // slot g holds the g-th token walked
-                        float* out = P.part + ((grow * P.H + h) * kSlices + slice) * kPart;
-                        for (int e2 = tid; e2 <= 3 * kDim / 2; e2 += kBwdThreads) {   // pairs
-                            const int e = 2 * e2;
-                            float2 sum = zero;
+                    if (tid < kPart / 4) {   // one float4 of each token's 388 sums per thread
+                        const int e = 4 * tid;   // dq (scaled), dk, da; the last holds db
+                        const float2 sc = dup2(e < kDim ? P.scale : 1.0f);
+                        for (int g = 0; g <= gi; ++g) {
+                            const size_t grow = row + gi - g;   // slot g: the g-th token walked
+                            float2 lo = zero, hi = zero;
 #pragma unroll
-                            for (int w = 0; w < kBwdWarps; ++w)
-                                sum = add2(sum, *reinterpret_cast<const float2*>(&S.grp[g][w][e]));
-                            if (e == 3 * kDim) out[e] = sum.x;   // db
-                            else *reinterpret_cast<float2*>(out + e) = e < kDim ? mul2(sum, dup2(P.scale)) : sum;
+                            for (int w = 0; w < kBwdWarps; ++w) {
+                                const float4 x = *reinterpret_cast<const float4*>(&S.grp[g][w][e]);
+                                lo = add2(lo, make_float2(x.x, x.y));
+                                hi = add2(hi, make_float2(x.z, x.w));
+                            }
+                            lo = mul2(lo, sc);
+                            hi = mul2(hi, sc);
+                            *reinterpret_cast<float4*>(P.part + ((grow * P.H + h) * kSlices + slice) * kPart + e) =
+                                make_float4(lo.x, lo.y, hi.x, hi.y);
                         }
                     }
                     __syncthreads();
