@@ -212,7 +212,9 @@ int kda_fwd_host(const void* q, const void* k, const void* v, const void* g,
  * d_out, dv and d_initial_state must be 16-byte aligned.  Scratch:
  * kda_bwd_workspace_bytes() from the stream-ordered allocator (state checkpoints every
  * 8 tokens, each token's d and v - r, per-slice partial sums; about 21 KB per token
- * and head).  Asynchronous on `stream`; a malformed cu_seqlens sets KDA_ERR_BAD_SEQLENS
+ * and head, so one call of more than ~12 M token-heads does not fit in a GB300's
+ * memory and returns KDA_ERR_ALLOC; split such a call over the sequence with
+ * d_final_state and d_initial_state carried between the parts).  Asynchronous on `stream`; a malformed cu_seqlens sets KDA_ERR_BAD_SEQLENS
  * in the error word and writes nothing.  Results are deterministic (fixed summation
  * order).  The work: 8 CTAs per (sequence, head), each owning 16 value columns of the
  * state, on CUDA cores; then a kernel that sums their partial dq, dk and decay
