@@ -630,11 +630,22 @@ def cpu_baseline(d, workload: str = WORKLOAD, target_s: float = 12.0):
     else:
         n_heads, t = probe, t_probe
     tokens_equiv = d["q"].shape[0] * T * n_heads / H
-    return {"value": tokens_equiv / t, "unit": "tokens/s", "cores": min(threads, n_heads),
-            "kind": "oracle",
-            "sample": f"{n_heads} of {H} heads x {d['q'].shape[0] * T} tokens of {workload}; "
-                      f"tokens/s counts "
-                      f"a token as all {H} heads ({t:.1f} s)"}
+    rec = {"value": tokens_equiv / t, "unit": "tokens/s", "cores": min(threads, n_heads),
+           "kind": "oracle",
+           "sample": f"{n_heads} of {H} heads x {d['q'].shape[0] * T} tokens of {workload}; "
+                     f"tokens/s counts "
+                     f"a token as all {H} heads ({t:.1f} s)"}
+    if d.get("cu_seqlens") is None and d["q"].shape[0] == 1 and T >= 1024:
+        # one thread on the first 1,024 tokens of head 0, extrapolated to all heads
+        sl = {n: conv[n][:, :1024] for n in conv}
+        t0 = time.perf_counter()
+        oracle.kda_fwd(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], d["scale"], d["A_log"],
+                       d["dt_bias"], d["lower_bound"], initial_state=s0, heads=[0], n_threads=1)
+        t1 = time.perf_counter() - t0
+        rec["one_thread"] = {"value": 1024 / H / t1, "unit": "tokens/s", "cores": 1,
+                             "sample": f"first 1024 tokens of head 0 ({t1:.2f} s), "
+                                       f"extrapolated: a token counts as all {H} heads"}
+    return rec
 
 
 def cpu_baseline_bwd(brun, target_s: float = 3.0):
