@@ -934,7 +934,12 @@ __device__ void solve(const Problem& P, const SeqMap& M, const Unit& U0, Smem& S
 //   O    += U^T A_qk^T
 // The state and U are read from tensor memory as fp32 A operands (kind::tf32).
 // One unit's chunks; g0 as for the loader, ui = this CTA's units with tokens before it.
+// kZ: every unit starts from a zero state (no initial state given), so the first
+// chunk's [O|U] MMAs would add exact zeros: they are left out, and u, the first O
+// product and the first state update start fresh accumulators instead (the results
+// are bit for bit those of a zero initial state).
 // Returns the chunks whose MMAs and commits were all issued (fewer if a wait gave up).
+template <bool kZ>
 __device__ __forceinline__ int mma_unit(const Unit& U, Smem& S, uint32_t tmem, int* err, int g0,
                                         int ui) {
     constexpr uint32_t id_u = tc::idesc_f16_f32(128, 16);
@@ -962,15 +967,20 @@ __device__ __forceinline__ int mma_unit(const Unit& U, Smem& S, uint32_t tmem, i
             if (!mbar_wait(&S.s_done, (unsigned)((g - 1) & 1), err)) break;
         }
         tc::fence_after_sync();
+        // with a zero state (kZ, first chunk) the products below that read it vanish
+        uint32_t acc = 1;
+        if constexpr (kZ) acc = c == 0 ? 0u : 1u;
         // [O|U] = S^T [Q 2^G ; -w]^T over the 16 key-channel steps (the first one starts
         // a fresh accumulator), then U += u^T = V^T (T diag b)^T
-        tc::mma_ts_tf32(uo, sc, d_xb + so, id_s, 0);
+        if (acc) {
+            tc::mma_ts_tf32(uo, sc, d_xb + so, id_s, 0);
 #pragma unroll
-        for (int kk = 1; kk < 16; ++kk)
-            tc::mma_ts_tf32(uo, sc + 8 * kk,
-                            d_xb + so + (uint64_t)(((kk >> 2) * X_ROWS * 128 + (kk & 3) * 32) >> 4),
-                            id_s, 1);
-        tc::mma_ss(uo + 16, d_vt + so, d_tbt + so, id_u, 1);
+            for (int kk = 1; kk < 16; ++kk)
+                tc::mma_ts_tf32(uo, sc + 8 * kk,
+                                d_xb + so + (uint64_t)(((kk >> 2) * X_ROWS * 128 + (kk & 3) * 32) >> 4),
+                                id_s, 1);
+        }
+        tc::mma_ss(uo + 16, d_vt + so, d_tbt + so, id_u, acc);
         // one wait for both the [O|U] MMAs and the epilogue's rescale: a wait costs
         // this thread ~100 cycles even on a completed barrier
         tc::commit(smem_u32(&S.scaled));
@@ -981,8 +991,9 @@ __device__ __forceinline__ int mma_unit(const Unit& U, Smem& S, uint32_t tmem, i
         tc::fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
-            tc::mma_ts_tf32(sn, uo + 16 + 8 * kk, d_kdt + so + (uint64_t)((kk * 256) >> 4), id_k, 1);
-            tc::mma_ts_tf32(uo, uo + 16 + 8 * kk, d_aqk + so + (uint64_t)((kk * 256) >> 4), id_q, 1);
+            const uint32_t a = kk == 0 ? acc : 1u;
+            tc::mma_ts_tf32(sn, uo + 16 + 8 * kk, d_kdt + so + (uint64_t)((kk * 256) >> 4), id_k, a);
+            tc::mma_ts_tf32(uo, uo + 16 + 8 * kk, d_aqk + so + (uint64_t)((kk * 256) >> 4), id_q, a);
         }
         tc::commit(smem_u32(&S.s_done));
         tc::commit(smem_u32(&S.empty[slot]));
@@ -990,18 +1001,18 @@ __device__ __forceinline__ int mma_unit(const Unit& U, Smem& S, uint32_t tmem, i
     return c;
 }
 
-template <bool kP>
+template <bool kP, bool kZ>
 __device__ void mma_issuer(const Problem& P, const SeqMap& M, const Unit& U0, Smem& S,
                            uint32_t tmem, int* err) {
     int c = 0;   // chunks of this CTA whose commits were all issued
     if constexpr (!kP) {
-        c = mma_unit(U0, S, tmem, err, 0, 0);
+        c = mma_unit<kZ>(U0, S, tmem, err, 0, 0);
     } else {
         int ui = 0;
         for (int k = 0;; ++k) {
             Unit U;
             if (!read_unit(S, k, err, false, U)) break;
-            const int done = mma_unit(U, S, tmem, err, c, ui);
+            const int done = mma_unit<kZ>(U, S, tmem, err, c, ui);
             c += done;
             if (done < U.nch) break;   // a wait gave up
             if (U.nch > 0) ++ui;
@@ -1053,7 +1064,9 @@ __device__ __forceinline__ void scale32(uint32_t (&x)[32], const float* gc) {
     }
 }
 
-// One unit; g0 as for the loader.  Returns false if a wait gave up.
+// One unit; g0 as for the loader.  kZ: zero initial state (nothing to write or rescale
+// for the first chunk; the hand-offs stay the same).  Returns false if a wait gave up.
+template <bool kZ>
 __device__ __forceinline__ bool epilogue_unit(const Problem& P, const Unit& U, Smem& S,
                                               uint32_t tmem, int ew, int lane, int* err, int g0) {
     const int v = 32 * ew + lane;
@@ -1069,30 +1082,34 @@ __device__ __forceinline__ bool epilogue_unit(const Problem& P, const Unit& U, S
         return true;
     }
     // initial state S0 into buffer 0, then S0 Diag(2^G_last of chunk 0) into buffer 1
+    if constexpr (!kZ) {
 #pragma unroll 1
-    for (int piece = 0; piece < 4; ++piece) {
-        uint32_t x[32];
+        for (int piece = 0; piece < 4; ++piece) {
+            uint32_t x[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int c = 32 * piece + i;
-            x[i] = __float_as_uint(P.init_state ? state_in(P, sbase + (size_t)c * kDim) : 0.0f);
+            for (int i = 0; i < 32; ++i) {
+                const int c = 32 * piece + i;
+                x[i] = __float_as_uint(P.init_state ? state_in(P, sbase + (size_t)c * kDim) : 0.0f);
+            }
+            tc::st32(tl + TM_S + 32 * piece, x);
         }
-        tc::st32(tl + TM_S + 32 * piece, x);
+        tc::wait_st();
     }
-    tc::wait_st();
     tc::fence_before_sync();
     mbar_arrive(&S.init_ready);
     ok = mbar_wait(&S.full[g0 % kRing], (unsigned)((g0 / kRing) & 1), err);
     if (!__all_sync(0xffffffffu, ok)) return false;
+    if constexpr (!kZ) {
 #pragma unroll 1
-    for (int piece = 0; piece < 4; ++piece) {
-        uint32_t x[32];
-        tc::ld32(tl + TM_S + 32 * piece, x);
-        tc::wait_ld();
-        scale32(x, S.st[g0 % kRing].gc + 32 * piece);
-        tc::st32(tl + TM_S + 128 + 32 * piece, x);
+        for (int piece = 0; piece < 4; ++piece) {
+            uint32_t x[32];
+            tc::ld32(tl + TM_S + 32 * piece, x);
+            tc::wait_ld();
+            scale32(x, S.st[g0 % kRing].gc + 32 * piece);
+            tc::st32(tl + TM_S + 128 + 32 * piece, x);
+        }
+        tc::wait_st();
     }
-    tc::wait_st();
     tc::fence_before_sync();
     mbar_arrive(&S.scaled);
 
@@ -1153,17 +1170,17 @@ __device__ __forceinline__ bool epilogue_unit(const Problem& P, const Unit& U, S
     return true;
 }
 
-template <bool kP>
+template <bool kP, bool kZ>
 __device__ void epilogue(const Problem& P, const SeqMap& M, const Unit& U0, Smem& S, uint32_t tmem,
                          int ew, int lane, int* err) {
     if constexpr (!kP) {
-        epilogue_unit(P, U0, S, tmem, ew, lane, err, 0);
+        epilogue_unit<kZ>(P, U0, S, tmem, ew, lane, err, 0);
     } else {
         int g = 0;
         for (int k = 0;; ++k) {
             Unit U;
             if (!read_unit(S, k, err, true, U)) return;
-            if (!epilogue_unit(P, U, S, tmem, ew, lane, err, g)) return;
+            if (!epilogue_unit<kZ>(P, U, S, tmem, ew, lane, err, g)) return;
             g += U.nch;
         }
     }
@@ -1171,8 +1188,8 @@ __device__ void epilogue(const Problem& P, const SeqMap& M, const Unit& U0, Smem
 
 // kP: persistent (a grid of at most one CTA per SM takes the units from a device
 // counter, longest first); otherwise one CTA per unit.  Every unit's arithmetic is the
-// same either way.
-template <bool kP>
+// same either way.  kZ: no initial state (every unit starts from zero).
+template <bool kP, bool kZ>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_kernel(Problem P, SeqMap M, const __grid_constant__ RawMaps TM, int* err) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1259,11 +1276,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const Role role = role_of(warp);
     if (role == kEpi) {
-        epilogue<kP>(P, M, U, S, tmem, warp, lane, err);
+        epilogue<kP, kZ>(P, M, U, S, tmem, warp, lane, err);
         tc::fence_before_sync();
         mbar_arrive(&S.epi_done);
     } else if (role == kMma) {
-        if (lane == 0) mma_issuer<kP>(P, M, U, S, tmem, err);
+        if (lane == 0) mma_issuer<kP, kZ>(P, M, U, S, tmem, err);
         __syncwarp();
         // free tensor memory once the epilogue is done with it (after a timeout the
         // epilogue stops at its next wait, so a longer limit than a pipeline wait's)
@@ -1325,10 +1342,16 @@ cudaError_t launch_fused(const Problem& P, const SeqMap& M, int* err, cudaStream
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !g_attr_set[dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(fused_kernel<false>,
+        cudaError_t e = cudaFuncSetAttribute(fused_kernel<false, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(fused_kernel<true>,
+            e = cudaFuncSetAttribute(fused_kernel<true, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fused_kernel<false, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fused_kernel<true, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         int sms = 0;
@@ -1356,10 +1379,15 @@ cudaError_t launch_fused(const Problem& P, const SeqMap& M, int* err, cudaStream
         if (e == cudaSuccess) e = encode_rows(&TM.g, P.g, P.H, rows);
         if (e != cudaSuccess) return e;
     }   // else no tokens: the loader issues nothing
-    if (persist)
-        fused_kernel<true><<<(unsigned)sms, kThreads, smem, s>>>(P, M, TM, err);
+    const bool zero = P.init_state == nullptr;   // every unit starts from a zero state
+    if (persist && zero)
+        fused_kernel<true, true><<<(unsigned)sms, kThreads, smem, s>>>(P, M, TM, err);
+    else if (persist)
+        fused_kernel<true, false><<<(unsigned)sms, kThreads, smem, s>>>(P, M, TM, err);
+    else if (zero)
+        fused_kernel<false, true><<<(unsigned)ctas, kThreads, smem, s>>>(P, M, TM, err);
     else
-        fused_kernel<false><<<(unsigned)ctas, kThreads, smem, s>>>(P, M, TM, err);
+        fused_kernel<false, false><<<(unsigned)ctas, kThreads, smem, s>>>(P, M, TM, err);
     return cudaGetLastError();
 }
 

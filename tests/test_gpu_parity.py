@@ -412,3 +412,42 @@ def test_varlen_short_20000_sampled_heads():
     heads, every sequence of each."""
     d = synth.make_workload("varlen_short_20000_h16")
     _check(d, heads=[0, 7, 15], final_dtype=None, tag="short20000")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", ["fixed", "varlen", "short_persistent"])
+def test_no_initial_state_equals_zero_state(case):
+    """Without an initial state every unit starts from zero, and the kernel leaves out
+    the first chunk's products with the state (they would add exact zeros).  The
+    results must be bit for bit those of an explicit all-zero fp32 initial state, on
+    one CTA per unit (fixed length, varlen) and on persistent CTAs (many short
+    sequences)."""
+    import torch
+    import gated_delta_rule_39_gb300 as kda
+    if case == "fixed":
+        d = synth.make_inputs(2, 300, 3, seed=91)
+    elif case == "varlen":
+        d = synth.make_inputs(1, 135, 3, seed=92, lengths=[17, 0, 48, 1, 69])
+    else:
+        rng = np.random.default_rng(93)
+        lens = [int(x) for x in rng.integers(0, 21, size=2000)]
+        d = synth.make_inputs(1, sum(lens), 1, seed=93, lengths=lens)
+    x = upload(d)
+    B, T, H, _ = d["q"].shape
+    N = d["N"]
+    zero = torch.zeros((N, H, 128, 128), dtype=torch.float32, device="cuda")
+    res = []
+    for s0 in (None, zero):
+        out = torch.full((B, T, H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        fs = torch.full((N, H, 128, 128), float("nan"), device="cuda")
+        kda.kda_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], d["scale"], out, x["A_log"],
+                    x["dt_bias"], d["lower_bound"], initial_state=s0, final_state=fs,
+                    cu_seqlens=x["cu_seqlens"])
+        torch.cuda.synchronize()
+        assert kda.kda_fwd_get_error() == 0
+        res.append((out, fs))
+    assert torch.equal(res[0][0], res[1][0])
+    assert torch.equal(res[0][1], res[1][1])
+    ro, rs = run_oracle(d)
+    assert out_error(to_f64(res[0][0]), ro)["ok"]
+    assert state_error(to_f64(res[0][1]), rs)["ok"]
