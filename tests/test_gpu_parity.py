@@ -419,9 +419,9 @@ def test_varlen_short_20000_sampled_heads():
 def test_no_initial_state_equals_zero_state(case):
     """Without an initial state every unit starts from zero, and the kernel leaves out
     the first chunk's products with the state (they would add exact zeros).  The
-    results must be bit for bit those of an explicit all-zero fp32 initial state, on
-    one CTA per unit (fixed length, varlen) and on persistent CTAs (many short
-    sequences)."""
+    results must be bit for bit those of an explicit all-zero fp32 initial state (and
+    the outputs the same without a final state), on one CTA per unit (fixed length,
+    varlen) and on persistent CTAs (many short sequences)."""
     import torch
     import gated_delta_rule_39_gb300 as kda
     if case == "fixed":
@@ -448,6 +448,13 @@ def test_no_initial_state_equals_zero_state(case):
         res.append((out, fs))
     assert torch.equal(res[0][0], res[1][0])
     assert torch.equal(res[0][1], res[1][1])
+    # and without a final state: the same outputs
+    out = torch.full((B, T, H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    kda.kda_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], d["scale"], out, x["A_log"],
+                x["dt_bias"], d["lower_bound"], cu_seqlens=x["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert kda.kda_fwd_get_error() == 0
+    assert torch.equal(out, res[0][0])
     ro, rs = run_oracle(d)
     assert out_error(to_f64(res[0][0]), ro)["ok"]
     assert state_error(to_f64(res[0][1]), rs)["ok"]
