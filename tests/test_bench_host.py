@@ -80,3 +80,15 @@ def test_algorithmic_work_counts_state_traffic_per_call():
     d["initial_state"] = None
     b2, _, _ = bench.algorithmic_work(d, 2)
     assert b2 == bench.BYTES_PER_TH * 128 + 2 * 128 * 128 * ((0 + 4) + (4 + 4))
+
+
+def test_cpu_baseline_one_thread_figure():
+    """Fixed-length workloads of at least 1,024 tokens carry a one-thread oracle figure
+    (the first 1,024 tokens of head 0, extrapolated); varlen ones do not."""
+    d = synth.make_inputs(1, 1024, 2, seed=0, init_dtype="bf16")
+    rec = bench.cpu_baseline(d, "fixed", target_s=0.1)
+    assert rec["kind"] == "oracle" and rec["value"] > 0
+    one = rec["one_thread"]
+    assert one["cores"] == 1 and one["value"] > 0 and "first 1024 tokens" in one["sample"]
+    dv = synth.make_inputs(1, 1100, 1, seed=0, lengths=[600, 500])
+    assert "one_thread" not in bench.cpu_baseline(dv, "varlen", target_s=0.1)
