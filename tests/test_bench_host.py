@@ -4,6 +4,7 @@ import json
 import os
 
 import bench
+import synth
 
 
 def _sampler_with(tmp_path, monkeypatch, rows):
