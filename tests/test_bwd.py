@@ -124,3 +124,15 @@ def test_bwd_argument_errors():
     assert call(dA=None) == -1                   # KDA_ERR_NULL
     assert call(dv=base + 10 * row * 4 + 4) == -4   # KDA_ERR_ALIGN
     assert kda.kda_bwd_workspace_bytes(1, T, H) > 13 * 1024 * T * H
+
+
+@pytest.mark.gpu
+def test_bwd_many_short_sequences():
+    """600 sequences of 0-24 tokens (empty ones, single partial blocks, one block and a
+    bit) in one varlen call, two heads, with an initial state and dL/d(final state)."""
+    rng = np.random.default_rng(84)
+    lens = [int(x) for x in rng.integers(0, 25, size=600)]
+    d = synth.make_inputs(1, sum(lens), 2, seed=84, lengths=lens, init_dtype="bf16")
+    dfinal = np.random.default_rng(85).standard_normal((len(lens), 2, 128, 128))
+    gpu, ref = _run(d, _dout(d["v"].shape, 86), dfinal)
+    _compare(gpu, ref)
