@@ -1065,10 +1065,14 @@ __device__ __forceinline__ void scale32(uint32_t (&x)[32], const float* gc) {
 }
 
 // One unit; g0 as for the loader.  kZ: zero initial state (nothing to write or rescale
-// for the first chunk; the hand-offs stay the same).  Returns false if a wait gave up.
+// for the first chunk).  pre: this unit's first-chunk arrivals (init_ready, scaled) were
+// made at the end of the unit before; post: make the next unit's at the end of this one,
+// right after the last tensor-memory read and before the output stores (persistent CTAs
+// with kZ, where those arrivals wait for nothing else).  Returns false if a wait gave up.
 template <bool kZ>
 __device__ __forceinline__ bool epilogue_unit(const Problem& P, const Unit& U, Smem& S,
-                                              uint32_t tmem, int ew, int lane, int* err, int g0) {
+                                              uint32_t tmem, int ew, int lane, int* err, int g0,
+                                              bool pre = false, bool post = false) {
     const int v = 32 * ew + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * ew) << 16);   // this warp's lane quarter
     const size_t sbase = ((size_t)U.n * P.H + U.h) * kDim * kDim + v;   // + c * kDim
@@ -1095,10 +1099,12 @@ __device__ __forceinline__ bool epilogue_unit(const Problem& P, const Unit& U, S
         }
         tc::wait_st();
     }
-    tc::fence_before_sync();
-    mbar_arrive(&S.init_ready);
-    ok = mbar_wait(&S.full[g0 % kRing], (unsigned)((g0 / kRing) & 1), err);
-    if (!__all_sync(0xffffffffu, ok)) return false;
+    if (!pre) {
+        tc::fence_before_sync();
+        mbar_arrive(&S.init_ready);
+        ok = mbar_wait(&S.full[g0 % kRing], (unsigned)((g0 / kRing) & 1), err);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+    }
     if constexpr (!kZ) {
 #pragma unroll 1
         for (int piece = 0; piece < 4; ++piece) {
@@ -1110,8 +1116,10 @@ __device__ __forceinline__ bool epilogue_unit(const Problem& P, const Unit& U, S
         }
         tc::wait_st();
     }
-    tc::fence_before_sync();
-    mbar_arrive(&S.scaled);
+    if (!pre) {
+        tc::fence_before_sync();
+        mbar_arrive(&S.scaled);
+    }
 
     // slot / phase of chunk c in the operand ring, and the [O|U] buffer of chunk c - 1
     int slot = (g0 + 1) % kRing, phase = ((g0 + 1) / kRing) & 1, uob = 0;
@@ -1155,6 +1163,11 @@ __device__ __forceinline__ bool epilogue_unit(const Problem& P, const Unit& U, S
             uint32_t o[16];
             tc::ld16(tl + TM_UO + 32u * uob, o);
             tc::wait_ld();
+            if (post && !more) {   // tensor memory read for the last time: the next unit may start
+                tc::fence_before_sync();
+                mbar_arrive(&S.init_ready);
+                mbar_arrive(&S.scaled);
+            }
             const int len = min(kChunk, U.L - (c - 1) * kChunk);
 #pragma unroll
             for (int t = 0; t < kChunk; ++t)
@@ -1177,10 +1190,12 @@ __device__ void epilogue(const Problem& P, const SeqMap& M, const Unit& U0, Smem
         epilogue_unit<kZ>(P, U0, S, tmem, ew, lane, err, 0);
     } else {
         int g = 0;
+        bool pre = false;   // the arrivals of the next unit with tokens were made early
         for (int k = 0;; ++k) {
             Unit U;
             if (!read_unit(S, k, err, true, U)) return;
-            if (!epilogue_unit<kZ>(P, U, S, tmem, ew, lane, err, g)) return;
+            if (!epilogue_unit<kZ>(P, U, S, tmem, ew, lane, err, g, pre, kZ)) return;
+            if (U.nch > 0) pre = kZ;   // a unit without tokens makes and takes no arrivals
             g += U.nch;
         }
     }
