@@ -136,3 +136,13 @@ def test_bwd_many_short_sequences():
     dfinal = np.random.default_rng(85).standard_normal((len(lens), 2, 128, 128))
     gpu, ref = _run(d, _dout(d["v"].shape, 86), dfinal)
     _compare(gpu, ref)
+
+
+@pytest.mark.gpu
+def test_bwd_long_sequence():
+    """One 65,536-token sequence, one head (8,192 checkpoint blocks): the reverse pass
+    carries the state gradient over the whole sequence."""
+    d = synth.make_inputs(1, 65536, 1, seed=87, init_dtype="f32")
+    dfinal = np.random.default_rng(88).standard_normal((1, 1, 128, 128))
+    gpu, ref = _run(d, _dout(d["v"].shape, 89), dfinal)
+    _compare(gpu, ref)
