@@ -477,8 +477,10 @@ def run_cuda(args, world, rank, local, pg):
     sampler = ClockSampler(local) if rank == 0 else None
     elapsed_ms, prof = timed_steps(runner, args.steps, args.warmup, pg, device, sampler)
     elapsed_ms = max_over_ranks(pg, elapsed_ms, device)
-    main = workload_line(name, d, elapsed_ms, prof, args.steps, world, runner.calls, decode,
-                         bwd=args.bwd)
+    # a profiling case (another size, or the backward) has no traffic record of its own
+    profiling = bool(args.heads or args.tokens or args.bwd)
+    main = workload_line(name + " (profiling)" if profiling else name, d, elapsed_ms, prof,
+                         args.steps, world, runner.calls, decode, bwd=args.bwd)
 
     # ---- end-to-end through the host-buffer entry point ---------------------------
     e2e = None
